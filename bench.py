@@ -1,0 +1,411 @@
+"""Benchmark of the segment transition cache hot path on GB300.
+
+One step = the whole hot path over one synthetic request: build the
+(T_C, S_{C|0}) pair of every segment body, then the fused request assembly
+(seam advance through the first w tokens of each inner segment, emitting their
+outputs, and composition S <- T_C S + S_{C|0} in prompt order).
+
+Default workload: 1 layer x 32 heads, d_k = d_v = 128, bf16 q/k/v, fp32 gates
+and state, 8 segments x 4096 tokens (32k), w = 8, composed from a zero state.
+A second measurement times warm-cache composition alone: 30 layers x 32 heads,
+a pool of 256 fp32 pairs per head, 64 requests x 16 segments.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
+independent request (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "segment tokens/s (build) and compositions/s, % tensor/HBM roofline, 1 GB300"
+
+# Algorithmic work per unit ("Measurement").
+D = 128
+FLOP_PER_CHUNK_WY = 3 * 2 * 64 * 64 * D + 2 * 2 * 64 * D * (2 * D)  # G, U, W; W.X and K^T.R per 64-token chunk
+FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
+FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
+BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "sm_max_mhz": j.get("sm_max_mhz", 2070.0),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+                "source": "fallback"}
+
+
+def fp32_simt_peak_tflops(sm_mhz):
+    # 152 SMs x 128 FP32 lanes x 2 FLOP per FMA at the given clock.
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", sel], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+class RequestStep:
+    """Device-resident inputs and outputs of one request; step() runs the hot path once."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        import torch
+
+        import linear_attention_state_gb300 as hy
+        self.hy = hy
+        self.w = w
+        tok = w.draw_request(dev)
+        self.k, self.v = tok["k"], tok["v"]
+        self.alpha, self.beta = tok["alpha"], tok["beta"]
+        pos = torch.tensor(w.seam_positions(), device=dev)
+        shp = (1, w.n_seg - 1, w.w, w.H)
+        self.seam_q = tok["q"][pos].reshape(*shp, w.d).contiguous()
+        self.seam_k = tok["k"][pos].reshape(*shp, w.d).contiguous()
+        self.seam_v = tok["v"][pos].reshape(*shp, w.d).contiguous()
+        self.seam_a = tok["alpha"][pos].reshape(shp).contiguous()
+        self.seam_b = tok["beta"][pos].reshape(shp).contiguous()
+        del tok
+        self.bounds_list = w.body_bounds()
+        self.bounds = torch.tensor(self.bounds_list, dtype=torch.int64, device=dev)
+        self.max_len = max(e - b for b, e in self.bounds_list)
+        self.T = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
+        self.S = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
+        self.idx = torch.arange(w.n_seg, dtype=torch.int32, device=dev)[None]
+        self.S_out = torch.empty((1, w.H, w.d, w.d), device=dev)
+        self.o = torch.empty((1, w.n_seg - 1, w.w, w.H, w.d), device=dev)
+        self.body_head_tokens = sum(e - b for b, e in self.bounds_list) * w.H
+        self.tokens = w.n_seg * w.seg_len * w.layers
+        self.compositions = w.n_seg * w.H
+        self.seam_head_tokens = (w.n_seg - 1) * w.w * w.H
+
+    def step(self, ev=None):
+        hy = self.hy
+        if ev is not None:
+            ev[0].record()
+        hy.segment_build_batched(self.k, self.v, self.bounds, self.alpha, self.beta, family=self.w.family,
+                                 max_len=self.max_len, out=(self.T, self.S))
+        if ev is not None:
+            ev[1].record()
+        hy.assemble(self.T, self.S, self.idx, self.seam_k, self.seam_v, self.seam_a, self.seam_b,
+                    seam_q=self.seam_q, family=self.w.family, out=self.S_out, o_out=self.o)
+        if ev is not None:
+            ev[2].record()
+
+    def host_copies(self):
+        """Pinned host copies of the step's inputs (for the end-to-end measurement)."""
+        names = ["k", "v", "alpha", "beta", "seam_q", "seam_k", "seam_v", "seam_a", "seam_b"]
+        return {n: getattr(self, n).cpu().pin_memory() for n in names}
+
+
+def run_timed(fn, steps, warmup, sync_all, kernel_events=True):
+    """Times `steps` calls of fn after `warmup` untimed ones, with CUDA events on the current stream.
+
+    With kernel_events, fn records three events per step (before, between and after
+    its two launches) and the per-launch durations are returned too.
+    """
+    import torch
+    for _ in range(warmup):
+        fn(None)
+    sync_all()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start.record()
+    for i in range(steps):
+        fn(evs[i] if kernel_events else None)
+    end.record()
+    sync_all()
+    total_ms = start.elapsed_time(end)
+    if not kernel_events:
+        return total_ms, [], []
+    k1 = [e[0].elapsed_time(e[1]) for e in evs]
+    k2 = [e[1].elapsed_time(e[2]) for e in evs]
+    return total_ms, k1, k2
+
+
+def cpu_baseline(w, n_heads, threads):
+    """The oracle, as it stands, on a sample of heads of the same request: pairs, seams, compose."""
+    import numpy as np
+
+    import oracle
+    tok = w.draw_request("cpu")
+    heads = list(range(n_heads))
+    bounds = w.body_bounds()
+    seam_pos = w.seam_positions()
+
+    def one_head(h):
+        f = lambda t: t[:, h].double().numpy()  # noqa: E731
+        k, v, q, a, b = f(tok["k"]), f(tok["v"]), f(tok["q"]), f(tok["alpha"]), f(tok["beta"])
+        Ts, Ss = [], []
+        for (b0, e0) in bounds:
+            T, S = oracle.segment_pair(w.family, k[b0:e0], v[b0:e0], a[b0:e0], b[b0:e0])
+            Ts.append(T.reshape(-1))
+            Ss.append(S)
+        S = np.zeros((w.d, w.d))
+        for j in range(w.n_seg):
+            if j >= 1 and w.w > 0:
+                s0 = j * w.seg_len
+                S, _ = oracle.run(w.family, k[s0:s0 + w.w], v[s0:s0 + w.w], a[s0:s0 + w.w], b[s0:s0 + w.w],
+                                  q=q[s0:s0 + w.w], S0=S)
+            S = oracle.compose(w.family, Ts[j][None], Ss[j][None], S_init=S)
+        return S
+
+    t0 = time.perf_counter()
+    oracle.parallel_map(one_head, heads, threads=threads)
+    dt = time.perf_counter() - t0
+    del seam_pos
+    tokens_equiv = w.n_seg * w.seg_len * w.layers * n_heads / w.H
+    return tokens_equiv / dt, dt
+
+
+def compose_pool_measure(steps, warmup, dev, peaks):
+    """Warm-cache composition: 30 layers x 32 heads, pool of 256 fp32 pairs, 64 requests x 16 segments."""
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import workloads as W
+    pw = W.COMPOSE_POOL
+    H, d, P = pw.H, pw.d, pw.pool
+    pool_T = torch.empty((P, H, d, d), device=dev)
+    pool_S = torch.empty((P, H, d, d), device=dev)
+    # Pool pairs: built (untimed) from 1024 seeded gated-delta tokens each.
+    for p in range(P):
+        tok = pw.pair_inputs(p, dev)
+        T, S = hy.segment_build(tok["k"], tok["v"], tok["alpha"], tok["beta"], family="gated_delta")
+        pool_T[p].copy_(T)
+        pool_S[p].copy_(S)
+        del tok, T, S
+    idx = pw.request_indices(dev)
+    out = torch.empty((pw.B, H, d, d), device=dev)
+    torch.cuda.synchronize()
+
+    def fn(ev):
+        if ev is not None:
+            ev[0].record()
+        hy.compose(pool_T, pool_S, idx, family="gated_delta", out=out)
+        if ev is not None:
+            ev[1].record()
+            ev[2].record()
+
+    total_ms, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+    comps = pw.B * pw.n * H
+    avg = sum(k1) / len(k1) / 1e3
+    bytes_ = comps * BYTES_PER_COMPOSITION
+    st = hy.stream_status()
+    res = {"workload": pw.name, "compositions_per_s": comps / (total_ms / 1e3 / steps), "ms_per_step": total_ms / steps,
+           "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                        "peak_source": peaks["source"]},
+           "status": st}
+    del pool_T, pool_S
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-compose", action="store_true", help="skip the warm-cache composition measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import workloads as W
+    w = W.BUILD_32K
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    from linear_attention_state_gb300 import build as B
+    if rank == 0 or world == 1:
+        B.build_library()
+    if world > 1:
+        dist.barrier()
+    import linear_attention_state_gb300 as hy
+    hy.load()
+    peaks = load_peaks()
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    req = RequestStep(w, dev)
+    status0 = hy.stream_status()
+    clocks = ClockSampler(local)
+    total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all)
+    clk = clocks.stop()
+    status = hy.stream_status()
+    t = torch.tensor([total_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    step_s = total_ms / 1e3 / args.steps
+    value = req.tokens * world / step_s
+
+    # dominant kernel: the build
+    avg_build_s = sum(k_build) / len(k_build) / 1e3
+    avg_asm_s = sum(k_asm) / len(k_asm) / 1e3
+    flops_rec = FLOP_PER_HEAD_TOKEN_RECURRENT * req.body_head_tokens
+    sm_mhz = clk["sm_mhz"] or peaks["sm_max_mhz"]
+    alu_peak = fp32_simt_peak_tflops(peaks["sm_max_mhz"])
+    roof = {"bound": "alu", "achieved": flops_rec / avg_build_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": flops_rec / avg_build_s / 1e12 / alu_peak, "traffic": None,
+            "kernel": "recurrent_kernel (build, fp32 SIMT)",
+            "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock",
+            "flop_per_unit": FLOP_PER_HEAD_TOKEN_RECURRENT, "units_per_launch": req.body_head_tokens}
+
+    # end to end through the API with host buffers
+    host = req.host_copies()
+    S_host = torch.empty(req.S_out.shape, pin_memory=True)
+    o_host = torch.empty(req.o.shape, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = S_host.numel() * 4 + o_host.numel() * 4
+
+    def e2e_step(ev):
+        for n, x in host.items():
+            getattr(req, n).copy_(x, non_blocking=True)
+        req.step(None)
+        S_host.copy_(req.S_out, non_blocking=True)
+        o_host.copy_(req.o, non_blocking=True)
+
+    e2e_ms, _, _ = run_timed(e2e_step, args.steps, min(args.warmup, 3), sync_all, kernel_events=False)
+    e2e_value = req.tokens * world / (e2e_ms / 1e3 / args.steps)
+
+    compose = None
+    if not args.no_compose:
+        del host
+        compose = compose_pool_measure(args.steps, args.warmup, dev, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        threads = os.cpu_count() or 1
+        n_heads = min(w.H, max(1, threads))
+        v_cpu, dt = cpu_baseline(w, n_heads, threads)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n_heads} of {w.H} heads of the same request, all 8 segments (pairs, seams, compose), "
+                         f"float64, {dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.layers, "heads": w.heads, "d": w.d, "segments": w.n_seg,
+                       "segment_tokens": w.seg_len, "seam_w": w.w, "inputs": "bf16 q/k/v, fp32 gates and state",
+                       "l2": "inputs larger than L2 (k+v 537 MB per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "build": {"body_head_tokens_per_s": req.body_head_tokens / avg_build_s, "ms": avg_build_s * 1e3},
+            "assemble": {"compositions_per_s": req.compositions / avg_asm_s,
+                         "seam_head_tokens_per_s": req.seam_head_tokens / avg_asm_s, "ms": avg_asm_s * 1e3},
+            "roofline": roof,
+            "compose_pool": compose,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"], "window": "warm-up and timed steps"},
+            "device_status": [status0, status],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the float64 oracle on the host cores, K timed steps of a bounded sample."""
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    n_heads = min(w.H, max(1, threads // 4))
+    for _ in range(args.warmup):
+        cpu_baseline(w, 1, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_baseline(w, n_heads, threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = w.n_seg * w.seg_len * w.layers * n_heads / w.H / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "sample": f"{n_heads} of {w.H} heads per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_heads} of {w.H} heads of the request per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * hypic.h -- C ABI of libhypic, the GB300 (sm_103a) linear-attention segment
+ * transition cache.
+ *
+ * The method (HYPIC reading notes: "HYPIC: Accelerating Hybrid-Attention LLM
+ * Serving with Position-Independent Caching"):
+ *   every linear-attention head runs S_i = T_i S_{i-1} + u_i, o_i = q_i^T S_i
+ *   (paper Eq. (2)).  A segment C = (1..m) is cached as the affine map
+ *   F_C(S) = T_C S + S_{C|0} with T_C = T_m...T_1 and
+ *   S_{C|0} = sum_t T_m...T_{t+1} u_t (Method 2).  Reuse composes the cached
+ *   pairs in prompt order, S <- T_C S + S_{C|0} (paper Eq. (6)), after the
+ *   running state has been advanced through the first w "seam" tokens of each
+ *   inner segment (Method 5, seam windows).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pointers: every tensor pointer is DEVICE memory owned by the caller,
+ *   contiguous, 16-byte aligned, in the layout stated.  The library never
+ *   allocates, frees or keeps a pointer after the call returns.
+ * Execution: every call only enqueues work on `stream` (NULL = the legacy
+ *   default stream) and returns; results are ready when the stream is.
+ * Shapes: d_k == d_v in {16, 32, 64, 128}; H >= 0; counts >= 0.  An empty
+ *   batch (H, B or n_seg == 0) is a no-op that returns HYPIC_OK.
+ * Errors: arguments are checked on the host before anything is enqueued and
+ *   give HYPIC_EINVAL (bad pointer, size or layout) or HYPIC_EUNSUPPORTED
+ *   (valid but not implemented shape); a failed launch gives HYPIC_ECUDA.
+ *   Checks that need device data (pool indices, segment bounds) and bounded
+ *   waits inside kernels record the first error in a per-device status word
+ *   instead of faulting; hypic_stream_status() returns and clears it.
+ * Families (paper Table 1), with the storage form of T_C (paper Table 3):
+ *   SCALAR_CONST  T_i = gamma_h I,                u_i = k v^T   T_C: 1 float
+ *   SCALAR        T_i = a_i I,                    u_i = k v^T   T_C: 1 float
+ *   DIAG          T_i = diag(alpha_i),            u_i = k v^T   T_C: d_k floats
+ *   DELTA         T_i = I - b_i k k^T,            u_i = b k v^T T_C: d_k x d_k
+ *   GATED_DELTA   T_i = a_i (I - b_i k k^T),      u_i = b k v^T T_C: d_k x d_k
+ * Token layouts: k, q, v [tokens, H, d] in the shape's in_dtype (fp32 or
+ *   bf16); alpha fp32 [tokens, H] (SCALAR, GATED_DELTA), [tokens, H, d_k]
+ *   (DIAG), [H] (SCALAR_CONST), ignored for DELTA; beta fp32 [tokens, H]
+ *   (DELTA, GATED_DELTA only).  States and pairs are fp32, row index = key
+ *   channel: S [.., H, d_k, d_v], T [.., H, t_size].
+ */
+#ifndef HYPIC_H
+#define HYPIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (so this header needs no CUDA header). */
+typedef struct CUstream_st *hypic_stream_t;
+
+typedef enum {
+    HYPIC_OK = 0,
+    HYPIC_EINVAL = -1,      /* bad argument (null, misaligned, negative size, bad enum) */
+    HYPIC_EUNSUPPORTED = -2,/* valid request the library does not implement */
+    HYPIC_ECUDA = -3,       /* a CUDA runtime call or launch failed */
+    HYPIC_ETIMEOUT = -4,    /* a bounded wait inside a kernel ran out */
+    HYPIC_ENOSPACE = -5,    /* workspace smaller than the size query returned */
+    HYPIC_EDEVICE = -6      /* a device-side check failed (index or bound out of range) */
+} hypic_status;
+
+typedef enum {
+    HYPIC_FAM_SCALAR_CONST = 0,
+    HYPIC_FAM_SCALAR = 1,
+    HYPIC_FAM_DIAG = 2,
+    HYPIC_FAM_DELTA = 3,
+    HYPIC_FAM_GATED_DELTA = 4
+} hypic_family;
+
+typedef enum { HYPIC_F32 = 0, HYPIC_BF16 = 1 } hypic_dtype;
+
+typedef struct {
+    int32_t H;        /* heads (layers may be folded in: layer-major)       */
+    int32_t d_k;      /* key width; must equal d_v                           */
+    int32_t d_v;      /* value width                                         */
+    int32_t family;   /* hypic_family                                        */
+    int32_t in_dtype; /* hypic_dtype of k, q, v                              */
+} hypic_shape;
+
+/* Number of floats of one head's T_C: 1, d_k or d_k*d_k by family; 0 if invalid. */
+int64_t hypic_t_size(const hypic_shape *shape);
+
+/*
+ * Segment build: (T_C, S_{C|0}) of one segment body for every head.
+ * Defines: Method 2 (T_C = T_m...T_1, S_{C|0} from a zero state) and the
+ * two-pass build of paper Sec. 5 (S_0 = 0 with writes -> S_{C|0}; S_0 = I with
+ * u = 0 -> T_C), which this library evaluates in one pass over the
+ * augmented state [T | S].
+ *   k, v, q   [len, H, d]   q may be NULL; it is read only when o_out != NULL
+ *   alpha, beta             gate layouts above, over the same len tokens
+ *   T_out     [H, t_size]   S_out [H, d_k, d_v]
+ *   o_out     [len, H, d_v] nullable: o_t = q_t^T S_t of the segment run from
+ *                           a zero state (the independent-prefill outputs)
+ *   ws, ws_bytes            workspace of at least hypic_build_workspace_bytes()
+ * len == 0 gives T_C = I and S_{C|0} = 0.
+ */
+hypic_status hypic_segment_build(const hypic_shape *shape, const void *k, const void *v,
+                                 const void *q, const float *alpha, const float *beta, int64_t len,
+                                 float *T_out, float *S_out, float *o_out, void *ws, size_t ws_bytes,
+                                 hypic_stream_t stream);
+
+/*
+ * Batched segment build over n_seg bodies that sit anywhere on one token axis.
+ *   seg_bounds DEVICE int64 [n_seg][2]: [begin, end) token range of body i;
+ *              0 <= begin <= end <= n_tokens and end - begin <= max_len, else
+ *              the body is skipped and HYPIC_EDEVICE is recorded.
+ *   n_tokens   extent of the token axis of k, v, q, alpha, beta
+ *   T_out [n_seg, H, t_size], S_out [n_seg, H, d_k, d_v]
+ *   o_out [n_tokens, H, d_v] nullable, written at the bodies' token rows.
+ */
+hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg,
+                                         const int64_t *seg_bounds, int64_t max_len, int64_t n_tokens,
+                                         const void *k, const void *v, const void *q, const float *alpha,
+                                         const float *beta, float *T_out, float *S_out, float *o_out,
+                                         void *ws, size_t ws_bytes, hypic_stream_t stream);
+
+/* Workspace bytes the build needs for n_seg bodies of at most max_len tokens. */
+size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
+
+/*
+ * Compose: S = T[i_{n-1}](...(T[i_0] S_init + S0[i_0])...) + S0[i_{n-1}] for
+ * each of B requests and every head -- paper Eq. (6) evaluated as n
+ * sequential S <- T_C S + S_{C|0} (Method 2).  The pairs live in a pool and
+ * each request lists its own order:
+ *   idx     DEVICE int32 [B, n], entries in [0, pool_size) (else HYPIC_EDEVICE)
+ *   pool_T  [pool_size, H, t_size]   pool_S [pool_size, H, d_k, d_v]
+ *   S_init  [B, H, d_k, d_v] or NULL (zero state)
+ *   S_out   [B, H, d_k, d_v]; may be the same pointer as S_init.
+ */
+hypic_status hypic_compose(const hypic_shape *shape, int32_t B, int32_t n, const int32_t *idx,
+                           int64_t pool_size, const float *pool_T, const float *pool_S,
+                           const float *S_init, float *S_out, hypic_stream_t stream);
+
+/*
+ * Inclusive scan over affine maps (Method 2 composition rule
+ * (T2,S2) o (T1,S1) = (T2 T1, T2 S1 + S2), associative, not commutative):
+ *   (Tp_0, Sp_0) = (T_0, S_0),  (Tp_i, Sp_i) = (T_i, S_i) o (Tp_{i-1}, Sp_{i-1}).
+ *   T, T_prefix [n, H, t_size];  S, S_prefix [n, H, d_k, d_v].
+ *   Outputs must not overlap inputs.  ws may be NULL when
+ *   hypic_scan_workspace_bytes() returns 0.
+ */
+hypic_status hypic_affine_scan(const hypic_shape *shape, int32_t n, const float *T, const float *S,
+                               float *T_prefix, float *S_prefix, void *ws, size_t ws_bytes,
+                               hypic_stream_t stream);
+size_t hypic_scan_workspace_bytes(const hypic_shape *shape, int32_t n);
+
+/*
+ * Seam advance (Method 5, seam windows): run the recurrence from the current
+ * running state through w seam tokens of each of B requests, emitting
+ * o_i = q_i^T S_i (post-update state, paper Eq. (2)).
+ *   S_inout [B, H, d_k, d_v]           updated in place
+ *   q, k, v [B, w, H, d]               alpha, beta: gate layouts over B*w tokens
+ *   o_out   [B, w, H, d_v] or NULL
+ */
+hypic_status hypic_seam_advance(const hypic_shape *shape, int32_t B, float *S_inout, const void *q,
+                                const void *k, const void *v, const float *alpha, const float *beta,
+                                int32_t w, float *o_out, hypic_stream_t stream);
+
+/*
+ * Request assembly, fused: for each request b and head, starting from S_init
+ * (or zero), for j = 0..n-1: if j >= 1 and w > 0, advance through the w seam
+ * tokens of segment j and emit their outputs; then S <- T[idx[b,j]] S +
+ * S0[idx[b,j]].  Segment 0 (the system prompt) has no seam (Method 5).
+ *   seam_q, seam_k, seam_v [B, n-1, w, H, d]; seam_alpha, seam_beta: gate
+ *   layouts over B*(n-1)*w tokens; o_out [B, n-1, w, H, d_v] or NULL.
+ *   Other arguments as hypic_compose.  w == 0 is hypic_compose.
+ */
+hypic_status hypic_assemble(const hypic_shape *shape, int32_t B, int32_t n, int32_t w,
+                            const int32_t *idx, int64_t pool_size, const float *pool_T,
+                            const float *pool_S, const void *seam_q, const void *seam_k,
+                            const void *seam_v, const float *seam_alpha, const float *seam_beta,
+                            const float *S_init, float *S_out, float *o_out, hypic_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns and clears the status word of the current
+ * device: HYPIC_OK, HYPIC_EDEVICE or HYPIC_ETIMEOUT (first error recorded by
+ * any kernel since the last call), or HYPIC_ECUDA if the stream itself failed.
+ */
+hypic_status hypic_stream_status(hypic_stream_t stream);
+
+/* Static, never NULL. */
+const char *hypic_strerror(hypic_status status);
+
+/* Incremented on any incompatible change of this header. */
+int32_t hypic_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYPIC_H */

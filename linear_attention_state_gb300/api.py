@@ -1,0 +1,201 @@
+"""Python calls with the C ABI's names, on torch CUDA tensors.
+
+Argument marshalling only: every step of the path runs in libhypic's CUDA
+kernels.  Outputs are allocated with torch on the inputs' device; calls are
+enqueued on torch's current stream.  See ``include/hypic.h`` for layouts.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib as L
+
+_DT = {torch.float32: "f32", torch.bfloat16: "bf16"}
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def t_size(family: str, d: int) -> int:
+    return 1 if family in ("scalar_const", "scalar") else (d if family == "diag" else d * d)
+
+
+def _t_shape(family, lead, d):
+    if family in ("scalar_const", "scalar"):
+        return (*lead,)
+    if family == "diag":
+        return (*lead, d)
+    return (*lead, d, d)
+
+
+def _in_dtype(k):
+    try:
+        return _DT[k.dtype]
+    except KeyError:
+        raise ValueError(f"inputs must be float32 or bfloat16, got {k.dtype}") from None
+
+
+def _gates(family, alpha, beta):
+    alpha = _cuda(alpha, "alpha", torch.float32, allow_none=family == "delta")
+    beta = _cuda(beta, "beta", torch.float32, allow_none=family not in ("delta", "gated_delta"))
+    return alpha, beta
+
+
+def segment_build(k, v, alpha=None, beta=None, q=None, family="gated_delta", want_o=False, stream=None):
+    """(T_C, S_{C|0}[, o]) of one segment body: k, v, q [len, H, d]."""
+    lib = L.load()
+    _cuda(k, "k"), _cuda(v, "v", k.dtype)
+    n, H, d = k.shape
+    alpha, beta = _gates(family, alpha, beta)
+    if want_o:
+        _cuda(q, "q", k.dtype)
+    sh = L.shape(H, d, family, _in_dtype(k))
+    T = torch.empty((H, t_size(family, d)), device=k.device, dtype=torch.float32)
+    S = torch.empty((H, d, d), device=k.device, dtype=torch.float32)
+    o = torch.empty((n, H, d), device=k.device, dtype=torch.float32) if want_o else None
+    ws_bytes = lib.hypic_build_workspace_bytes(ctypes.byref(sh), 1, n)
+    ws = torch.empty(ws_bytes, device=k.device, dtype=torch.uint8) if ws_bytes else None
+    st = lib.hypic_segment_build(ctypes.byref(sh), _p(k), _p(v), _p(q if want_o else None), _p(alpha), _p(beta), n,
+                                 _p(T), _p(S), _p(o), _p(ws), ws_bytes, _stream(stream))
+    L.check(st, "hypic_segment_build")
+    T = T.view(_t_shape(family, (H,), d))
+    return (T, S, o) if want_o else (T, S)
+
+
+def segment_build_batched(k, v, bounds, alpha=None, beta=None, q=None, family="gated_delta", max_len=None,
+                          want_o=False, out=None, stream=None):
+    """Pairs of n_seg bodies [begin, end) = bounds[i] (int64 [n_seg, 2] on the device) of one token axis."""
+    lib = L.load()
+    _cuda(k, "k"), _cuda(v, "v", k.dtype)
+    _cuda(bounds, "bounds", torch.int64)
+    n_tok, H, d = k.shape
+    n_seg = bounds.shape[0]
+    alpha, beta = _gates(family, alpha, beta)
+    if want_o:
+        _cuda(q, "q", k.dtype)
+    if max_len is None:
+        max_len = int((bounds[:, 1] - bounds[:, 0]).max().item()) if n_seg else 0
+    sh = L.shape(H, d, family, _in_dtype(k))
+    if out is None:
+        T = torch.empty((n_seg, H, t_size(family, d)), device=k.device, dtype=torch.float32)
+        S = torch.empty((n_seg, H, d, d), device=k.device, dtype=torch.float32)
+    else:
+        T, S = out
+        _cuda(T, "T_out", torch.float32), _cuda(S, "S_out", torch.float32)
+    o = torch.zeros((n_tok, H, d), device=k.device, dtype=torch.float32) if want_o else None
+    ws_bytes = lib.hypic_build_workspace_bytes(ctypes.byref(sh), n_seg, max_len)
+    ws = torch.empty(ws_bytes, device=k.device, dtype=torch.uint8) if ws_bytes else None
+    st = lib.hypic_segment_build_batched(ctypes.byref(sh), n_seg, _p(bounds), max_len, n_tok, _p(k), _p(v),
+                                         _p(q if want_o else None), _p(alpha), _p(beta), _p(T), _p(S), _p(o),
+                                         _p(ws), ws_bytes, _stream(stream))
+    L.check(st, "hypic_segment_build_batched")
+    T = T.view(_t_shape(family, (n_seg, H), d))
+    return (T, S, o) if want_o else (T, S)
+
+
+def compose(pool_T, pool_S, idx, S_init=None, family="gated_delta", out=None, stream=None):
+    """S_out [B, H, d, d]: each request b composes pool entries idx[b, 0..n-1] in order."""
+    lib = L.load()
+    _cuda(pool_S, "pool_S", torch.float32), _cuda(pool_T, "pool_T", torch.float32)
+    _cuda(idx, "idx", torch.int32)
+    P, H, d, _ = pool_S.shape
+    B, n = idx.shape
+    if S_init is not None:
+        _cuda(S_init, "S_init", torch.float32)
+    S_out = out if out is not None else torch.empty((B, H, d, d), device=pool_S.device, dtype=torch.float32)
+    sh = L.shape(H, d, family, "f32")
+    st = lib.hypic_compose(ctypes.byref(sh), B, n, _p(idx), P, _p(pool_T), _p(pool_S), _p(S_init), _p(S_out),
+                           _stream(stream))
+    L.check(st, "hypic_compose")
+    return S_out
+
+
+def affine_scan(T, S, family="gated_delta", stream=None):
+    """Inclusive prefix scan of n pairs: T [n, H, ...], S [n, H, d, d]."""
+    lib = L.load()
+    _cuda(T, "T", torch.float32), _cuda(S, "S", torch.float32)
+    n, H, d, _ = S.shape
+    sh = L.shape(H, d, family, "f32")
+    Tp = torch.empty_like(T)
+    Sp = torch.empty_like(S)
+    ws_bytes = lib.hypic_scan_workspace_bytes(ctypes.byref(sh), n)
+    ws = torch.empty(ws_bytes, device=S.device, dtype=torch.uint8) if ws_bytes else None
+    st = lib.hypic_affine_scan(ctypes.byref(sh), n, _p(T), _p(S), _p(Tp), _p(Sp), _p(ws), ws_bytes,
+                               _stream(stream))
+    L.check(st, "hypic_affine_scan")
+    return Tp, Sp
+
+
+def seam_advance(S, k, v, alpha=None, beta=None, q=None, family="gated_delta", want_o=True, stream=None):
+    """Advance S [B, H, d, d] in place through seam tokens k, v, q [B, w, H, d]; returns o [B, w, H, d]."""
+    lib = L.load()
+    _cuda(S, "S", torch.float32), _cuda(k, "k"), _cuda(v, "v", k.dtype)
+    B, w, H, d = k.shape
+    alpha, beta = _gates(family, alpha, beta)
+    if want_o:
+        _cuda(q, "q", k.dtype)
+    o = torch.empty((B, w, H, d), device=k.device, dtype=torch.float32) if want_o else None
+    sh = L.shape(H, d, family, _in_dtype(k))
+    st = lib.hypic_seam_advance(ctypes.byref(sh), B, _p(S), _p(q if want_o else None), _p(k), _p(v), _p(alpha),
+                                _p(beta), w, _p(o), _stream(stream))
+    L.check(st, "hypic_seam_advance")
+    return o
+
+
+def assemble(pool_T, pool_S, idx, seam_k, seam_v, seam_alpha=None, seam_beta=None, seam_q=None,
+             S_init=None, family="gated_delta", want_o=True, out=None, o_out=None, stream=None):
+    """Fused seam advance + compose.  Seam tokens [B, n-1, w, H, d]; returns (S_out, o [B, n-1, w, H, d])."""
+    lib = L.load()
+    _cuda(pool_S, "pool_S", torch.float32), _cuda(pool_T, "pool_T", torch.float32)
+    _cuda(idx, "idx", torch.int32)
+    P, H, d, _ = pool_S.shape
+    B, n = idx.shape
+    w = seam_k.shape[2] if seam_k is not None and seam_k.dim() == 5 else 0
+    if w > 0 and n > 1:
+        _cuda(seam_k, "seam_k"), _cuda(seam_v, "seam_v", seam_k.dtype)
+        seam_alpha, seam_beta = _gates(family, seam_alpha, seam_beta)
+        if want_o:
+            _cuda(seam_q, "seam_q", seam_k.dtype)
+        in_dtype = _in_dtype(seam_k)
+    else:
+        in_dtype = "f32"
+    if S_init is not None:
+        _cuda(S_init, "S_init", torch.float32)
+    S_out = out if out is not None else torch.empty((B, H, d, d), device=pool_S.device, dtype=torch.float32)
+    o = None
+    if want_o and w > 0 and n > 1:
+        o = o_out if o_out is not None else torch.empty((B, n - 1, w, H, d), device=pool_S.device,
+                                                        dtype=torch.float32)
+    sh = L.shape(H, d, family, in_dtype)
+    st = lib.hypic_assemble(ctypes.byref(sh), B, n, w, _p(idx), P, _p(pool_T), _p(pool_S),
+                            _p(seam_q if o is not None else None), _p(seam_k), _p(seam_v), _p(seam_alpha),
+                            _p(seam_beta), _p(S_init), _p(S_out), _p(o), _stream(stream))
+    L.check(st, "hypic_assemble")
+    return S_out, o
+
+
+def stream_status(stream=None) -> int:
+    """Wait for the stream; return and clear the device status word (0 = no error recorded)."""
+    return int(L.load().hypic_stream_status(_stream(stream)))

@@ -1,0 +1,291 @@
+// libhypic C ABI: host-side argument checks, the per-device status word and
+// dispatch to the kernels.  Every check here runs before anything is enqueued.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace hypic {
+namespace {
+
+__device__ int g_status_word;  // first device-side error since the last hypic_stream_status()
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+std::once_flag g_status_once[kMaxDevices];
+cudaError_t g_status_err[kMaxDevices];
+
+// Device address of the status word on the current device (looked up once per device).
+cudaError_t status_word(int **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_status_once[dev], [dev]() {
+    void *p = nullptr;
+    g_status_err[dev] = cudaGetSymbolAddress(&p, g_status_word);
+    g_status_ptr[dev] = static_cast<int *>(p);
+  });
+  if (g_status_err[dev] != cudaSuccess) return g_status_err[dev];
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
+bool ok_opt(const void *p) { return p == nullptr || aligned16(p); }
+
+bool dense_family(int f) { return f == HYPIC_FAM_DELTA || f == HYPIC_FAM_GATED_DELTA; }
+
+// Shape checks common to every call.  Returns HYPIC_OK or the error.
+hypic_status check_shape(const hypic_shape *s) {
+  if (!s) return HYPIC_EINVAL;
+  if (s->H < 0 || s->d_k <= 0 || s->d_v <= 0) return HYPIC_EINVAL;
+  if (s->family < HYPIC_FAM_SCALAR_CONST || s->family > HYPIC_FAM_GATED_DELTA) return HYPIC_EINVAL;
+  if (s->in_dtype != HYPIC_F32 && s->in_dtype != HYPIC_BF16) return HYPIC_EINVAL;
+  if (s->d_k != s->d_v) return HYPIC_EUNSUPPORTED;
+  const int d = s->d_k;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return HYPIC_EUNSUPPORTED;
+  return HYPIC_OK;
+}
+
+// Gate pointers the family needs (alpha unless DELTA; beta for the delta families).
+hypic_status check_gates(const hypic_shape *s, const float *alpha, const float *beta) {
+  if (s->family != HYPIC_FAM_DELTA && !ok_ptr(alpha)) return HYPIC_EINVAL;
+  if (dense_family(s->family) && !ok_ptr(beta)) return HYPIC_EINVAL;
+  return HYPIC_OK;
+}
+
+hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ECUDA; }
+
+hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &seg, const void *k,
+                          const void *v, const void *q, const float *alpha, const float *beta,
+                          float *T_out, float *S_out, float *o_out, bool tokens, cudaStream_t st) {
+  if (n_seg == 0 || sh->H == 0) return HYPIC_OK;
+  if (!ok_ptr(T_out) || !ok_ptr(S_out)) return HYPIC_EINVAL;
+  if (tokens) {  // token pointers are only read when some body is non-empty
+    if (!ok_ptr(k) || !ok_ptr(v) || !ok_opt(o_out) || !ok_opt(q)) return HYPIC_EINVAL;
+    if (o_out && !ok_ptr(q)) return HYPIC_EINVAL;
+    hypic_status r = check_gates(sh, alpha, beta);
+    if (r != HYPIC_OK) return r;
+  } else {
+    o_out = nullptr;
+  }
+  int *err = nullptr;
+  cudaError_t e = status_word(&err);
+  if (e != cudaSuccess) return HYPIC_ECUDA;
+  RecurrentArgs a{};
+  a.H = sh->H;
+  a.D = sh->d_k;
+  a.fam = sh->family;
+  a.n_seg = n_seg;
+  a.seg = seg;
+  a.src = TokenSrc{k, v, q, alpha, beta, sh->in_dtype};
+  a.S_in = nullptr;
+  a.S_out = S_out;
+  a.T_out = T_out;
+  a.o_out = o_out;
+  a.err = err;
+  return from_cuda(launch_recurrent(a, st));
+}
+
+}  // namespace
+}  // namespace hypic
+
+using namespace hypic;
+
+extern "C" {
+
+int32_t hypic_abi_version(void) { return 1; }
+
+int64_t hypic_t_size(const hypic_shape *s) {
+  if (check_shape(s) != HYPIC_OK) return 0;
+  if (s->family == HYPIC_FAM_SCALAR_CONST || s->family == HYPIC_FAM_SCALAR) return 1;
+  if (s->family == HYPIC_FAM_DIAG) return s->d_k;
+  return (int64_t)s->d_k * s->d_k;
+}
+
+const char *hypic_strerror(hypic_status s) {
+  switch (s) {
+    case HYPIC_OK: return "ok";
+    case HYPIC_EINVAL: return "invalid argument";
+    case HYPIC_EUNSUPPORTED: return "unsupported shape or family";
+    case HYPIC_ECUDA: return "CUDA runtime error";
+    case HYPIC_ETIMEOUT: return "bounded wait inside a kernel ran out";
+    case HYPIC_ENOSPACE: return "workspace too small";
+    case HYPIC_EDEVICE: return "device-side check failed (index or bound out of range)";
+    default: return "unknown status";
+  }
+}
+
+size_t hypic_build_workspace_bytes(const hypic_shape *sh, int32_t n_seg, int64_t max_len) {
+  (void)sh;
+  (void)n_seg;
+  (void)max_len;
+  return 0;
+}
+
+size_t hypic_scan_workspace_bytes(const hypic_shape *sh, int32_t n) {
+  (void)sh;
+  (void)n;
+  return 0;
+}
+
+hypic_status hypic_segment_build(const hypic_shape *sh, const void *k, const void *v, const void *q,
+                                 const float *alpha, const float *beta, int64_t len, float *T_out,
+                                 float *S_out, float *o_out, void *ws, size_t ws_bytes,
+                                 hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (len < 0) return HYPIC_EINVAL;
+  if (ws_bytes < hypic_build_workspace_bytes(sh, 1, len)) return HYPIC_ENOSPACE;
+  (void)ws;
+  SegMap m{nullptr, 0, 0, len, len, len};
+  return build_common(sh, 1, m, k, v, q, alpha, beta, T_out, S_out, o_out, len > 0, (cudaStream_t)stream);
+}
+
+hypic_status hypic_segment_build_batched(const hypic_shape *sh, int32_t n_seg, const int64_t *seg_bounds,
+                                         int64_t max_len, int64_t n_tokens, const void *k, const void *v,
+                                         const void *q, const float *alpha, const float *beta,
+                                         float *T_out, float *S_out, float *o_out, void *ws,
+                                         size_t ws_bytes, hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (n_seg < 0 || max_len < 0 || n_tokens < 0) return HYPIC_EINVAL;
+  if (n_seg > 0 && !ok_ptr(seg_bounds)) return HYPIC_EINVAL;
+  if (ws_bytes < hypic_build_workspace_bytes(sh, n_seg, max_len)) return HYPIC_ENOSPACE;
+  (void)ws;
+  SegMap m{seg_bounds, 0, 0, 0, max_len, n_tokens};
+  return build_common(sh, n_seg, m, k, v, q, alpha, beta, T_out, S_out, o_out, n_tokens > 0,
+                      (cudaStream_t)stream);
+}
+
+hypic_status hypic_seam_advance(const hypic_shape *sh, int32_t B, float *S_inout, const void *q,
+                                const void *k, const void *v, const float *alpha, const float *beta,
+                                int32_t w, float *o_out, hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (B < 0 || w < 0) return HYPIC_EINVAL;
+  if (B == 0 || sh->H == 0 || w == 0) return HYPIC_OK;
+  if (!ok_ptr(S_inout) || !ok_opt(o_out)) return HYPIC_EINVAL;
+  if (!ok_ptr(k) || !ok_ptr(v) || (o_out && !ok_ptr(q))) return HYPIC_EINVAL;
+  r = check_gates(sh, alpha, beta);
+  if (r != HYPIC_OK) return r;
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  RecurrentArgs a{};
+  a.H = sh->H;
+  a.D = sh->d_k;
+  a.fam = sh->family;
+  a.n_seg = B;
+  a.seg = SegMap{nullptr, w, 0, w, w, (int64_t)B * w};
+  a.src = TokenSrc{k, v, q, alpha, beta, sh->in_dtype};
+  a.S_in = S_inout;
+  a.S_out = S_inout;
+  a.T_out = nullptr;
+  a.o_out = o_out;
+  a.err = err;
+  return from_cuda(launch_recurrent(a, (cudaStream_t)stream));
+}
+
+static hypic_status chain_common(const hypic_shape *sh, int32_t B, int32_t n, int32_t w, const int32_t *idx,
+                                 int64_t pool_size, const float *pool_T, const float *pool_S,
+                                 const void *seam_q, const void *seam_k, const void *seam_v,
+                                 const float *seam_alpha, const float *seam_beta, const float *S_init,
+                                 float *S_out, float *o_out, cudaStream_t st) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (B < 0 || n < 0 || w < 0 || pool_size < 0) return HYPIC_EINVAL;
+  if (B == 0 || sh->H == 0) return HYPIC_OK;
+  if (!ok_ptr(S_out) || !ok_opt(S_init) || !ok_opt(o_out)) return HYPIC_EINVAL;
+  if (n > 0 && (!ok_ptr(idx) || !ok_ptr(pool_T) || !ok_ptr(pool_S) || pool_size == 0)) return HYPIC_EINVAL;
+  const bool seams = w > 0 && n > 1;
+  if (seams) {
+    if (!ok_ptr(seam_k) || !ok_ptr(seam_v) || (o_out && !ok_ptr(seam_q))) return HYPIC_EINVAL;
+    r = check_gates(sh, seam_alpha, seam_beta);
+    if (r != HYPIC_OK) return r;
+  }
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  ChainArgs a{};
+  a.H = sh->H;
+  a.D = sh->d_k;
+  a.fam = sh->family;
+  a.B = B;
+  a.n = n;
+  a.w = seams ? w : 0;
+  a.idx = idx;
+  a.pool_size = pool_size;
+  a.pool_T = pool_T;
+  a.pool_S = pool_S;
+  a.S_init = S_init;
+  a.S_out = S_out;
+  a.scan = 0;
+  a.seam = TokenSrc{seam_k, seam_v, seam_q, seam_alpha, seam_beta, sh->in_dtype};
+  a.o_out = seams ? o_out : nullptr;
+  a.err = err;
+  return from_cuda(launch_chain(a, st));
+}
+
+hypic_status hypic_compose(const hypic_shape *sh, int32_t B, int32_t n, const int32_t *idx, int64_t pool_size,
+                           const float *pool_T, const float *pool_S, const float *S_init, float *S_out,
+                           hypic_stream_t stream) {
+  return chain_common(sh, B, n, 0, idx, pool_size, pool_T, pool_S, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, S_init, S_out, nullptr, (cudaStream_t)stream);
+}
+
+hypic_status hypic_assemble(const hypic_shape *sh, int32_t B, int32_t n, int32_t w, const int32_t *idx,
+                            int64_t pool_size, const float *pool_T, const float *pool_S, const void *seam_q,
+                            const void *seam_k, const void *seam_v, const float *seam_alpha,
+                            const float *seam_beta, const float *S_init, float *S_out, float *o_out,
+                            hypic_stream_t stream) {
+  return chain_common(sh, B, n, w, idx, pool_size, pool_T, pool_S, seam_q, seam_k, seam_v, seam_alpha,
+                      seam_beta, S_init, S_out, o_out, (cudaStream_t)stream);
+}
+
+hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T, const float *S,
+                               float *T_prefix, float *S_prefix, void *ws, size_t ws_bytes,
+                               hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (n < 0) return HYPIC_EINVAL;
+  if (ws_bytes < hypic_scan_workspace_bytes(sh, n)) return HYPIC_ENOSPACE;
+  (void)ws;
+  if (n == 0 || sh->H == 0) return HYPIC_OK;
+  if (!ok_ptr(T) || !ok_ptr(S) || !ok_ptr(T_prefix) || !ok_ptr(S_prefix)) return HYPIC_EINVAL;
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  ChainArgs a{};
+  a.H = sh->H;
+  a.D = sh->d_k;
+  a.fam = sh->family;
+  a.B = 1;
+  a.n = n;
+  a.w = 0;
+  a.idx = nullptr;
+  a.pool_size = n;
+  a.pool_T = T;
+  a.pool_S = S;
+  a.S_init = nullptr;
+  a.S_out = nullptr;
+  a.scan = 1;
+  a.T_rec = T_prefix;
+  a.S_rec = S_prefix;
+  a.seam = TokenSrc{nullptr, nullptr, nullptr, nullptr, nullptr, sh->in_dtype};
+  a.o_out = nullptr;
+  a.err = err;
+  return from_cuda(launch_chain(a, (cudaStream_t)stream));
+}
+
+hypic_status hypic_stream_status(hypic_stream_t stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HYPIC_ECUDA;
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return HYPIC_ECUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return HYPIC_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HYPIC_ECUDA;
+  return (hypic_status)host;
+}
+
+}  // extern "C"

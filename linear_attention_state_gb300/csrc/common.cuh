@@ -1,0 +1,74 @@
+// Internal declarations shared by the libhypic translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hypic.h"
+
+namespace hypic {
+
+// Tensor-of-tokens view: element (tok, h, i) of k/q/v lives at (tok*H + h)*D + i.
+struct TokenSrc {
+  const void *k, *v, *q;
+  const float *alpha, *beta;
+  int in_dtype;  // HYPIC_F32 or HYPIC_BF16
+};
+
+// Records the first device-side error in the status word (never traps).
+__device__ __forceinline__ void set_error(int *err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+template <typename Tin>
+__device__ __forceinline__ float to_f32(Tin x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// ---- launchers (host) -------------------------------------------------------------------
+
+// Which rows of the token axis form segment s: bounds[2s], bounds[2s+1] if bounds is
+// non-null, else [s*uni_stride + uni_offset, + uni_len).
+struct SegMap {
+  const int64_t *bounds;
+  int64_t uni_stride, uni_offset, uni_len;
+  int64_t max_len;   // a body longer than this is rejected (EDEVICE)
+  int64_t n_tokens;  // token-axis extent (bounds check), < 0 = unchecked
+};
+
+struct RecurrentArgs {
+  int H, D, fam;
+  int n_seg;
+  SegMap seg;
+  TokenSrc src;
+  const float *S_in;  // [n_seg, H, D, D] or null (zero)
+  float *S_out;       // [n_seg, H, D, D]
+  float *T_out;       // [n_seg, H, t_size] (build) or null (advance only)
+  float *o_out;       // [tokens, H, D] or null
+  int *err;
+};
+cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t st);
+
+struct ChainArgs {
+  int H, D, fam;
+  int B, n, w;
+  const int32_t *idx;  // [B, n] or null: step j of chain uses pool entry j
+  int64_t pool_size;
+  const float *pool_T;  // [P, H, t_size]
+  const float *pool_S;  // [P, H, D, D]
+  const float *S_init;  // [B, H, D, D] or null
+  float *S_out;         // final [B, H, D, D]
+  // scan mode: record every prefix; T half of the augmented state goes to T_rec
+  int scan;
+  float *T_rec;  // [n, H, t_size]
+  float *S_rec;  // [n, H, D, D]
+  TokenSrc seam;  // seam tokens [B, n-1, w, H, D]
+  float *o_out;   // [B, n-1, w, H, D] or null
+  int *err;
+};
+cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st);
+
+}  // namespace hypic

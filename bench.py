@@ -34,6 +34,9 @@ FLOP_PER_CHUNK_WY = 3 * 2 * 64 * 64 * D + 2 * 2 * 64 * D * (2 * D)  # G, U, W; W
 FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
+# dram__bytes_read.sum + dram__bytes_write.sum of one build_tc_kernel launch on this workload,
+# from the committed ncu capture (None until taken for the current kernel).
+BUILD_TC_TRAFFIC = None
 
 
 def load_peaks():
@@ -133,6 +136,13 @@ class RequestStep:
         self.idx = torch.arange(w.n_seg, dtype=torch.int32, device=dev)[None]
         self.S_out = torch.empty((1, w.H, w.d, w.d), device=dev)
         self.o = torch.empty((1, w.n_seg - 1, w.w, w.H, w.d), device=dev)
+        ws_bytes = hy.build_workspace_bytes(w.H, w.d, w.n_seg, self.max_len, family=w.family, in_dtype=w.in_dtype)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+        # kernels per step: build (prep + chain per head block, or one recurrent launch) + assemble
+        per_block = ws_bytes // max(1, w.H) if ws_bytes else 0
+        blocks = -(-w.H // max(1, ws_bytes // per_block)) if ws_bytes else 0
+        self.launches_per_step = (2 * blocks if ws_bytes and os.environ.get("HYPIC_BUILD_PATH") != "recurrent"
+                                  else 1) + 1
         self.body_head_tokens = sum(e - b for b, e in self.bounds_list) * w.H
         self.tokens = w.n_seg * w.seg_len * w.layers
         self.compositions = w.n_seg * w.H
@@ -143,7 +153,7 @@ class RequestStep:
         if ev is not None:
             ev[0].record()
         hy.segment_build_batched(self.k, self.v, self.bounds, self.alpha, self.beta, family=self.w.family,
-                                 max_len=self.max_len, out=(self.T, self.S))
+                                 max_len=self.max_len, out=(self.T, self.S), ws=self.ws)
         if ev is not None:
             ev[1].record()
         hy.assemble(self.T, self.S, self.idx, self.seam_k, self.seam_v, self.seam_a, self.seam_b,
@@ -317,14 +327,22 @@ def main():
     # dominant kernel: the build
     avg_build_s = sum(k_build) / len(k_build) / 1e3
     avg_asm_s = sum(k_asm) / len(k_asm) / 1e3
-    flops_rec = FLOP_PER_HEAD_TOKEN_RECURRENT * req.body_head_tokens
-    sm_mhz = clk["sm_mhz"] or peaks["sm_max_mhz"]
-    alu_peak = fp32_simt_peak_tflops(peaks["sm_max_mhz"])
-    roof = {"bound": "alu", "achieved": flops_rec / avg_build_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
-            "frac": flops_rec / avg_build_s / 1e12 / alu_peak, "traffic": None,
-            "kernel": "recurrent_kernel (build, fp32 SIMT)",
-            "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock",
-            "flop_per_unit": FLOP_PER_HEAD_TOKEN_RECURRENT, "units_per_launch": req.body_head_tokens}
+    if os.environ.get("HYPIC_BUILD_PATH") == "recurrent":
+        flops = FLOP_PER_HEAD_TOKEN_RECURRENT * req.body_head_tokens
+        alu_peak = fp32_simt_peak_tflops(peaks["sm_max_mhz"])
+        roof = {"bound": "alu", "achieved": flops / avg_build_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": flops / avg_build_s / 1e12 / alu_peak, "traffic": None,
+                "kernel": "recurrent_kernel (build, fp32 SIMT)",
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock",
+                "flop_per_unit": FLOP_PER_HEAD_TOKEN_RECURRENT, "units_per_launch": req.body_head_tokens}
+    else:
+        flops = FLOP_PER_HEAD_TOKEN_WY * req.body_head_tokens
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": flops / avg_build_s / 1e12, "peak": pk, "unit": "TFLOP/s",
+                "frac": flops / avg_build_s / 1e12 / pk, "traffic": BUILD_TC_TRAFFIC,
+                "kernel": "build: wy_prep_kernel + chain_tc_kernel (chunked WY, tcgen05)",
+                "peak_source": f"{peaks['source']} dense bf16 (burst)",
+                "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY, "units_per_launch": req.body_head_tokens}
 
     # end to end through the API with host buffers
     host = req.host_copies()
@@ -357,11 +375,12 @@ def main():
                "sample": f"{n_heads} of {w.H} heads of the same request, all 8 segments (pairs, seams, compose), "
                          f"float64, {dt:.1f} s wall"}
 
+    dtype = "f32" if os.environ.get("HYPIC_BUILD_PATH") == "recurrent" else "bf16"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "config": {"workload": w.name, "layers": w.layers, "heads": w.heads, "d": w.d, "segments": w.n_seg,
                        "segment_tokens": w.seg_len, "seam_w": w.w, "inputs": "bf16 q/k/v, fp32 gates and state",
                        "l2": "inputs larger than L2 (k+v 537 MB per step), no flush",
@@ -373,7 +392,7 @@ def main():
             "compose_pool": compose,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": req.launches_per_step * args.steps,
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"], "window": "warm-up and timed steps"},
             "device_status": [status0, status],

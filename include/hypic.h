@@ -58,7 +58,7 @@ typedef enum {
     HYPIC_EUNSUPPORTED = -2,/* valid request the library does not implement */
     HYPIC_ECUDA = -3,       /* a CUDA runtime call or launch failed */
     HYPIC_ETIMEOUT = -4,    /* a bounded wait inside a kernel ran out */
-    HYPIC_ENOSPACE = -5,    /* workspace smaller than the size query returned */
+    HYPIC_ENOSPACE = -5,    /* workspace too small for the request */
     HYPIC_EDEVICE = -6      /* a device-side check failed (index or bound out of range) */
 } hypic_status;
 
@@ -94,7 +94,7 @@ int64_t hypic_t_size(const hypic_shape *shape);
  *   T_out     [H, t_size]   S_out [H, d_k, d_v]
  *   o_out     [len, H, d_v] nullable: o_t = q_t^T S_t of the segment run from
  *                           a zero state (the independent-prefill outputs)
- *   ws, ws_bytes            workspace of at least hypic_build_workspace_bytes()
+ *   ws, ws_bytes            workspace, see hypic_build_workspace_bytes()
  * len == 0 gives T_C = I and S_{C|0} = 0.
  */
 hypic_status hypic_segment_build(const hypic_shape *shape, const void *k, const void *v,
@@ -117,7 +117,16 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
                                          const float *beta, float *T_out, float *S_out, float *o_out,
                                          void *ws, size_t ws_bytes, hypic_stream_t stream);
 
-/* Workspace bytes the build needs for n_seg bodies of at most max_len tokens. */
+/*
+ * Workspace bytes the build prefers for n_seg bodies of at most max_len tokens
+ * (0 when the shape runs without one).  The d = 128 bf16 delta-family build
+ * keeps one 33,280-byte operand record per (64-token chunk, head) in it; it
+ * processes the heads in blocks that fit the workspace it is given, so any size
+ * that holds one head's records (n_seg * ceil(max_len / 64) * 33,280 bytes)
+ * works, and less gives HYPIC_ENOSPACE.  The preferred size covers all heads up
+ * to about 1 GiB.  The workspace is caller-owned device memory, 16-byte aligned,
+ * and must not be used by anything else until the stream reaches the end of the call.
+ */
 size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
 
 /*

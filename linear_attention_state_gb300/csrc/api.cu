@@ -1,5 +1,7 @@
 // libhypic C ABI: host-side argument checks, the per-device status word and
 // dispatch to the kernels.  Every check here runs before anything is enqueued.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -55,11 +57,19 @@ hypic_status check_gates(const hypic_shape *s, const float *alpha, const float *
   return HYPIC_OK;
 }
 
+// HYPIC_BUILD_PATH=recurrent selects the token-by-token build even where the
+// tensor-core path applies (for comparisons); read at every call.
+bool force_recurrent() {
+  const char *v = getenv("HYPIC_BUILD_PATH");
+  return v && strcmp(v, "recurrent") == 0;
+}
+
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ECUDA; }
 
 hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &seg, const void *k,
                           const void *v, const void *q, const float *alpha, const float *beta,
-                          float *T_out, float *S_out, float *o_out, bool tokens, cudaStream_t st) {
+                          float *T_out, float *S_out, float *o_out, bool tokens, void *ws, size_t ws_bytes,
+                          cudaStream_t st) {
   if (n_seg == 0 || sh->H == 0) return HYPIC_OK;
   if (!ok_ptr(T_out) || !ok_ptr(S_out)) return HYPIC_EINVAL;
   if (tokens) {  // token pointers are only read when some body is non-empty
@@ -70,6 +80,9 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
   } else {
     o_out = nullptr;
   }
+  const bool tc = tokens && build_tc_supported(sh->d_k, sh->family, sh->in_dtype, o_out != nullptr) &&
+                  !force_recurrent();
+  if (tc && (ws_bytes < build_tc_min_workspace(n_seg, seg.max_len) || !ok_ptr(ws))) return HYPIC_ENOSPACE;
   int *err = nullptr;
   cudaError_t e = status_word(&err);
   if (e != cudaSuccess) return HYPIC_ECUDA;
@@ -85,6 +98,7 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
   a.T_out = T_out;
   a.o_out = o_out;
   a.err = err;
+  if (tc) return from_cuda(launch_build_tc(a, ws, ws_bytes, st));
   return from_cuda(launch_recurrent(a, st));
 }
 
@@ -118,10 +132,9 @@ const char *hypic_strerror(hypic_status s) {
 }
 
 size_t hypic_build_workspace_bytes(const hypic_shape *sh, int32_t n_seg, int64_t max_len) {
-  (void)sh;
-  (void)n_seg;
-  (void)max_len;
-  return 0;
+  if (check_shape(sh) != HYPIC_OK || n_seg <= 0 || max_len <= 0) return 0;
+  if (!build_tc_supported(sh->d_k, sh->family, sh->in_dtype, false)) return 0;
+  return build_tc_workspace_bytes(sh->H, n_seg, max_len);
 }
 
 size_t hypic_scan_workspace_bytes(const hypic_shape *sh, int32_t n) {
@@ -137,10 +150,9 @@ hypic_status hypic_segment_build(const hypic_shape *sh, const void *k, const voi
   hypic_status r = check_shape(sh);
   if (r != HYPIC_OK) return r;
   if (len < 0) return HYPIC_EINVAL;
-  if (ws_bytes < hypic_build_workspace_bytes(sh, 1, len)) return HYPIC_ENOSPACE;
-  (void)ws;
   SegMap m{nullptr, 0, 0, len, len, len};
-  return build_common(sh, 1, m, k, v, q, alpha, beta, T_out, S_out, o_out, len > 0, (cudaStream_t)stream);
+  return build_common(sh, 1, m, k, v, q, alpha, beta, T_out, S_out, o_out, len > 0, ws, ws_bytes,
+                      (cudaStream_t)stream);
 }
 
 hypic_status hypic_segment_build_batched(const hypic_shape *sh, int32_t n_seg, const int64_t *seg_bounds,
@@ -152,11 +164,9 @@ hypic_status hypic_segment_build_batched(const hypic_shape *sh, int32_t n_seg, c
   if (r != HYPIC_OK) return r;
   if (n_seg < 0 || max_len < 0 || n_tokens < 0) return HYPIC_EINVAL;
   if (n_seg > 0 && !ok_ptr(seg_bounds)) return HYPIC_EINVAL;
-  if (ws_bytes < hypic_build_workspace_bytes(sh, n_seg, max_len)) return HYPIC_ENOSPACE;
-  (void)ws;
   SegMap m{seg_bounds, 0, 0, 0, max_len, n_tokens};
-  return build_common(sh, n_seg, m, k, v, q, alpha, beta, T_out, S_out, o_out, n_tokens > 0,
-                      (cudaStream_t)stream);
+  return build_common(sh, n_seg, m, k, v, q, alpha, beta, T_out, S_out, o_out, n_tokens > 0 && max_len > 0, ws,
+                      ws_bytes, (cudaStream_t)stream);
 }
 
 hypic_status hypic_seam_advance(const hypic_shape *sh, int32_t B, float *S_inout, const void *q,

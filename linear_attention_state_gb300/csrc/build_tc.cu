@@ -1,0 +1,594 @@
+// Chunked tensor-core segment build for the delta families at d_k = d_v = 128, bf16 inputs.
+//
+// What it computes (HYPIC reading notes: Method 2 segment pair, paper Sec. 5
+// two-pass build, Method 3 Table 3 remark that the delta-type build can use the
+// per-step low-rank structure): (T_C, S_{C|0}) of a segment body, as the end
+// value of the augmented state X = [T | S] (d_k x 2d) started from [I | 0] and
+// run through the gated-delta recurrence with writes only in the S columns.
+//
+// Chunked (WY) form, 64 tokens per chunk.  With G_t = sum_{r<=t} log a_r inside
+// the chunk (kept in base 2 here) and gamma_t = exp(G_t), the per-token rule
+//   S_t = a_t S_{t-1} + k_t w_t^T,  w_t^T = b_t (v_t^T - a_t k_t^T S_{t-1})
+// unrolls to
+//   (I + L) Wm = diag(b) V - diag(b gamma) K X,  L_ts = b_t exp(G_t - G_s) k_t.k_s (s < t)
+//   X_new      = gamma_C X + K^T diag(exp(G_C - G_t)) Wm.
+// With A = (I + L)^{-1}: Wm = U - Wk X, U = A diag(b) V, Wk = A diag(b gamma) K.
+//
+// Two kernels per block of heads:
+//   wy_prep_kernel  (one CTA per chunk and head, all chunks in parallel): the
+//     state-independent part.  TMA loads K; gates and their log-cumsum; Gram =
+//     K K^T on tcgen05 (M = 64); L; A = (I + L)^{-1} in fp32 by 2 x 2 blocked
+//     forward substitution; A diag(b gamma) and A diag(b) split into bf16 hi + lo
+//     and stored to the workspace as ready-made 128-byte-swizzled operand tiles,
+//     with the per-token scales exp(G_C - G_t) and gamma_C.
+//   chain_tc_kernel (one CTA per segment, head and column half of X): the state-
+//     dependent chain.  Each CTA keeps its 128 x 128 fp32 half of X in tensor
+//     memory for the whole segment (the T half has no writes, the S half does;
+//     they evolve independently).  Per chunk: TMA brings K, V and the chunk's
+//     workspace tiles (double buffered); tcgen05 forms Wk^T = K^T (A diag(b g))^T
+//     and U^T = V^T (A diag(b))^T (hi + lo); X is split hi + lo into shared memory
+//     and gamma_C X written back as the accumulator; P^T = X^T Wk^T (hi.hi +
+//     hi.lo + lo.hi); R^T = (U^T - P^T) diag(exp(G_C - G_t)) split hi + lo;
+//     X += K^T R.
+// Operands are fp32-accurate to about 2^-16 relative (bf16 hi + lo; K and V are
+// exact in bf16) and every product accumulates in fp32 in TMEM.  Padded tokens of
+// a ragged last chunk get b = 0 and a = 1, which makes them exact identity steps.
+#include <cuda_bf16.h>
+
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace hypic {
+namespace {
+
+using namespace tc;
+
+constexpr int C = 64;    // tokens per chunk
+constexpr int D = 128;   // d_k = d_v
+constexpr int NT = 128;  // threads per CTA
+
+// Workspace record of one (chunk, head): four 8 KB K-major [64 t][64 s] tiles and the scales.
+constexpr uint32_t WS_ABH = 0, WS_ABL = 8192, WS_AVH = 16384, WS_AVL = 24576, WS_SC = 32768;
+constexpr uint32_t WS_REC = 33280;  // bytes per (chunk, head)
+constexpr size_t WS_CAP = (size_t)1 << 30;  // preferred workspace size bound
+
+struct BuildTcArgs {
+  int H;       // heads of the token tensors
+  int h0, Hb;  // this launch covers heads [h0, h0 + Hb)
+  int n_seg;
+  const int64_t *bounds;  // [n_seg][2] or null: single segment [0, len0)
+  int64_t len0, max_len, n_tokens;
+  int max_chunks;
+  int fam;
+  const float *alpha, *beta;
+  float *T_out, *S_out;
+  uint8_t *ws;
+  int *err;
+};
+
+__device__ __forceinline__ bool seg_bounds(const BuildTcArgs &a, int s, int64_t &beg, int64_t &end) {
+  if (a.bounds) {
+    beg = a.bounds[2 * s];
+    end = a.bounds[2 * s + 1];
+  } else {
+    beg = 0;
+    end = a.len0;
+  }
+  return beg >= 0 && end >= beg && end - beg <= a.max_len && end <= a.n_tokens;
+}
+
+__device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, int hh) {
+  return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * WS_REC;
+}
+
+// hi = bf16(v), lo = bf16(v - hi) for 8 values, packed for one 16-byte store each.
+__device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 hp = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+    const float2 hf = __bfloat1622float2(hp);
+    const __nv_bfloat162 lp = __floats2bfloat162_rn(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+    h[q] = *reinterpret_cast<const uint32_t *>(&hp);
+    l[q] = *reinterpret_cast<const uint32_t *>(&lp);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Kernel 1: per (segment, chunk, head) -- gates, Gram, L, A = (I + L)^{-1}, operand tiles.
+constexpr uint32_t P_OFF_K = 0;                    // 16 KB K chunk, two [64 t][64 i] boxes
+constexpr uint32_t P_OFF_L = 16384;                // fp32 [64][64]
+constexpr uint32_t P_OFF_A = P_OFF_L + 16384;      // fp32 [64][64]
+constexpr uint32_t P_OFF_T = P_OFF_A + 16384;      // fp32 [32][32]
+constexpr uint32_t P_SMEM = P_OFF_T + 4096 + 1024;  // + alignment slack
+
+__global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, BuildTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float sG[C], sBv[C], sBG[C];
+  __shared__ int ok_flag;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *sL = reinterpret_cast<float *>(sm + P_OFF_L);
+  float *sA = reinterpret_cast<float *>(sm + P_OFF_A);
+  float *sT = reinterpret_cast<float *>(sm + P_OFF_T);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int hh = blockIdx.x % a.Hb;
+  const int c = (blockIdx.x / a.Hb) % a.max_chunks;
+  const int s = (blockIdx.x / a.Hb) / a.max_chunks;
+  const int h = a.h0 + hh;
+  int64_t beg, end;
+  if (!seg_bounds(a, s, beg, end)) return;  // reported by the chain kernel
+  if ((int64_t)c * C >= end - beg) return;
+  const int64_t t0 = beg + (int64_t)c * C;
+
+  if (tid == 0) {
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    mbar_fence_init();
+    ok_flag = 1;
+    mbar_arrive_expect_tx(&bar_tma, 16384);
+    tma_load_2d(sm + P_OFF_K, &mapK, &bar_tma, h * D, (int)t0);
+    tma_load_2d(sm + P_OFF_K + 8192, &mapK, &bar_tma, h * D + 64, (int)t0);
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 64);
+    tmem_relinquish();
+  }
+  // gates: G_t = inclusive log2-cumsum of a, masked beyond the body
+  if (tid < C) {
+    const int64_t tok = t0 + tid;
+    float av = 1.f, bv = 0.f;
+    if (tok < end) {
+      bv = a.beta[tok * a.H + h];
+      if (a.fam == HYPIC_FAM_GATED_DELTA) av = a.alpha[tok * a.H + h];
+    }
+    float g = log2f(av);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, g, o);
+      if (lane >= o) g += y;
+    }
+    sG[tid] = g;
+    sBv[tid] = bv;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (tid >= 32 && tid < C) sG[tid] += sG[31];
+  if (tid == 0) {
+    if (!mbar_wait_cycles(&bar_tma, 0, a.err)) ok_flag = 0;
+    if (ok_flag) {
+      const uint32_t kb = smem_u32(sm + P_OFF_K);
+      const uint32_t id = idesc_f32acc(1, 1, 0, 0, 64, 64);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_f16(tmem, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id, kk > 0);
+      }
+      mma_commit(&bar_mma);
+      if (!mbar_wait_cycles(&bar_mma, 0, a.err)) ok_flag = 0;
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (tid < C) sBG[tid] = sBv[tid] * exp2f(sG[tid]);
+  if (ok_flag) {
+    // L_ts = b_t 2^(G_t - G_s) Gram_ts (s < t); Gram row t sits in lane 32(t/16) + t%16.
+    const int t = warp * 16 + lane;
+    const float Gt = lane < 16 ? sG[t] : 0.f;
+    const float bt = lane < 16 ? sBv[t] : 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < C; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      tmem_ld_wait();
+      if (lane < 16) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int sc = c0 + q;
+          sL[t * C + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[q] : 0.f;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (!ok_flag) return;
+
+  // Diagonal 32 x 32 blocks of A by column-wise forward substitution (threads 0..63).
+  if (tid < C) {
+    const int base = (tid >> 5) * 32, cl = tid & 31;
+    float x[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) x[r] = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < 32; ++r) {
+      const float *Lr = sL + (base + r) * C + base;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int q = 0; q + 3 < r; q += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(Lr + q);
+        a0 = fmaf(l4.x, x[q], a0);
+        a1 = fmaf(l4.y, x[q + 1], a1);
+        a2 = fmaf(l4.z, x[q + 2], a2);
+        a3 = fmaf(l4.w, x[q + 3], a3);
+      }
+#pragma unroll
+      for (int q = (r / 4) * 4; q < r; ++q) a0 = fmaf(Lr[q], x[q], a0);
+      if (r > cl) x[r] = -((a0 + a1) + (a2 + a3));
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) sA[(base + r) * C + base + cl] = x[r];
+    if (base == 0) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) sA[r * C + 32 + cl] = 0.f;
+    }
+  }
+  __syncthreads();
+  // T = L21 A11 (32 x 32).
+  for (int e = tid; e < 1024; e += NT) {
+    const int r = e >> 5, cc = e & 31;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) acc = fmaf(sL[(32 + r) * C + k], sA[k * C + cc], acc);
+    sT[r * 32 + cc] = acc;
+  }
+  __syncthreads();
+  // A21 = -A22 T.
+  for (int e = tid; e < 1024; e += NT) {
+    const int r = e >> 5, cc = e & 31;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) acc = fmaf(sA[(32 + r) * C + 32 + k], sT[k * 32 + cc], acc);
+    sA[(32 + r) * C + cc] = -acc;
+  }
+  __syncthreads();
+
+  // Operand tiles: A diag(b gamma) and A diag(b), split hi + lo, 128-byte-swizzled K-major.
+  uint8_t *rec = ws_rec(a, s, c, hh);
+  for (int e = tid; e < C * 8; e += NT) {
+    const int t = e >> 3, q = e & 7;
+    float vb[8], vv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float av = sA[t * C + 8 * q + j];
+      vb[j] = av * sBG[8 * q + j];
+      vv[j] = av * sBv[8 * q + j];
+    }
+    uint4 hi, lo;
+    const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)q);
+    split8(vb, hi, lo);
+    *reinterpret_cast<uint4 *>(rec + WS_ABH + off) = hi;
+    *reinterpret_cast<uint4 *>(rec + WS_ABL + off) = lo;
+    split8(vv, hi, lo);
+    *reinterpret_cast<uint4 *>(rec + WS_AVH + off) = hi;
+    *reinterpret_cast<uint4 *>(rec + WS_AVL + off) = lo;
+  }
+  float *sc = reinterpret_cast<float *>(rec + WS_SC);
+  if (tid < C) sc[tid] = exp2f(sG[C - 1] - sG[tid]);
+  if (tid == 0) sc[C] = exp2f(sG[C - 1]);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Kernel 2: per (segment, head, column half) -- the chunk chain on tensor memory.
+constexpr uint32_t OFF_KV = 0;                          // 2 stages x (K 16 KB + V 16 KB)
+constexpr uint32_t OFF_WS = 65536;                      // 2 stages x 33 KB workspace records
+constexpr uint32_t WS_STAGE = 33792;                    // record rounded up to 1024
+constexpr uint32_t OFF_XR = OFF_WS + 2 * WS_STAGE;      // 64 KB: X^T hi|lo, later R^T hi|lo
+constexpr uint32_t SMEM_BYTES = OFF_XR + 65536 + 1024;  // + alignment slack
+
+constexpr uint32_t TM_X = 0;    // 128 cols: X half, lanes = rows i
+constexpr uint32_t TM_P = 128;  // 64 cols: P^T, lanes = columns n of the half
+constexpr uint32_t TM_W = 192;  // 64 cols: Wk^T, lanes = i
+constexpr uint32_t TM_U = 256;  // 64 cols: U^T, lanes = j
+constexpr uint32_t TM_COLS = 512;
+
+__global__ void __launch_bounds__(NT, 1)
+    chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                    BuildTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_tma[2], bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid / 32;
+  const int half = blockIdx.x & 1;  // 0: T columns, 1: S columns
+  const int hh = (blockIdx.x >> 1) % a.Hb;
+  const int s = (blockIdx.x >> 1) / a.Hb;
+  const int h = a.h0 + hh;
+  const bool isS = half == 1;
+
+  int64_t beg, end;
+  if (!seg_bounds(a, s, beg, end)) {
+    if (tid == 0 && !isS) set_error(a.err, HYPIC_EDEVICE);
+    return;
+  }
+  const int nchunks = (int)((end - beg + C - 1) / C);
+
+  if (tid == 0) {
+    mbar_init(&bar_tma[0], 1);
+    mbar_init(&bar_tma[1], 1);
+    mbar_init(&bar_mma, 1);
+    mbar_fence_init();
+    abort_flag = 0;
+    prefetch_tmap(&mapK);
+    if (isS) prefetch_tmap(&mapV);
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  auto issue = [&](int c) {
+    const int st = c & 1;
+    const int row = (int)(beg + (int64_t)c * C);
+    uint8_t *kv = sm + OFF_KV + st * 32768;
+    uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+    const uint8_t *rec = ws_rec(a, s, c, hh);
+    mbar_arrive_expect_tx(&bar_tma[st], isS ? 32768u + WS_REC : 16384u + 16384u + 512u);
+    tma_load_2d(kv, &mapK, &bar_tma[st], h * D, row);
+    tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, row);
+    if (isS) {
+      tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, row);
+      tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, row);
+      bulk_load(wsd, rec, WS_REC, &bar_tma[st]);
+    } else {
+      bulk_load(wsd, rec, 16384, &bar_tma[st]);
+      bulk_load(wsd + WS_SC, rec + WS_SC, 512, &bar_tma[st]);
+    }
+  };
+  if (tid == 0) {
+    if (nchunks > 0) issue(0);
+    if (nchunks > 1) issue(1);
+  }
+
+  // X starts at [I | 0]: this CTA's half is I (T) or 0 (S).
+  for (int c0 = 0; c0 < D; c0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == tid) ? 1.f : 0.f;
+    tmem_st16(tmem + lane_base + TM_X + c0, v);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  uint32_t mph = 0;
+  const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);  // A = K^T or V^T (MN-major), B K-major
+  const uint32_t id_p = idesc_f32acc(1, 1, 1, 1, 128, 64);   // A = X^T (MN-major), B = Wk^T (MN-major)
+  const uint32_t id_x = idesc_f32acc(1, 1, 1, 0, 128, 128);  // A = K^T (MN-major), B = R K-major
+
+  auto wait_mma = [&]() -> bool {
+    if (tid == 0 && !mbar_wait_cycles(&bar_mma, mph, a.err)) abort_flag = 1;
+    mph ^= 1u;
+    __syncthreads();
+    tc_fence_after();
+    return abort_flag == 0;
+  };
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c & 1;
+    const uint32_t kbase = sb + OFF_KV + st * 32768;
+    const uint32_t vbase = kbase + 16384;
+    uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+    const uint32_t wsb = sb + OFF_WS + st * WS_STAGE;
+    if (tid == 0 && !mbar_wait_cycles(&bar_tma[st], (c >> 1) & 1, a.err)) abort_flag = 1;
+    __syncthreads();
+    if (abort_flag) break;
+    const float *sR = reinterpret_cast<const float *>(wsd + WS_SC);
+    const float gamma_C = sR[C];
+
+    // Wk^T = K^T (A diag(b gamma))^T and U^T = V^T (A diag(b))^T: M = 128, N = 64, K = 64.
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ak = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
+        mma_f16(tmem + TM_W, ak, sdesc_sw128(wsb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
+        mma_f16(tmem + TM_W, ak, sdesc_sw128(wsb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
+        if (isS) {
+          const uint64_t av = sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+          mma_f16(tmem + TM_U, av, sdesc_sw128(wsb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
+          mma_f16(tmem + TM_U, av, sdesc_sw128(wsb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
+        }
+      }
+      mma_commit(&bar_mma);
+    }
+
+    // X -> X^T hi/lo (MN-major A, two 64-column blocks); gamma_C X back into TMEM.
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + TM_X + c0, v);
+      tmem_ld_wait();
+      const uint32_t blk = (uint32_t)c0 >> 6;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint4 hi, lo;
+        split8(v + 8 * hf, hi, lo);
+        const uint32_t off = blk * 16384 + sw128_offset((uint32_t)tid, ((uint32_t)(c0 & 63) >> 3) + hf);
+        *reinterpret_cast<uint4 *>(sm + OFF_XR + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + OFF_XR + 32768 + off) = lo;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] *= gamma_C;
+      tmem_st16(tmem + lane_base + TM_X + c0, v);
+    }
+    tmem_st_wait();
+    if (!wait_mma()) break;  // Wk^T, U^T ready; the A tiles in the stage are consumed
+
+    // Wk^T (lanes i, columns t) -> MN-major B tile [i][t] hi/lo, over the consumed A tiles.
+#pragma unroll 1
+    for (int c0 = 0; c0 < C; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + TM_W + c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint4 hi, lo;
+        split8(v + 8 * hf, hi, lo);
+        const uint32_t off = sw128_offset((uint32_t)tid, ((uint32_t)c0 >> 3) + hf);
+        *reinterpret_cast<uint4 *>(wsd + off) = hi;
+        *reinterpret_cast<uint4 *>(wsd + 16384 + off) = lo;
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // P^T = X^T Wk^T: M = 128 (n), N = 64 (t), K = 128 (i); hi.hi + hi.lo + lo.hi.
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t xh = sdesc_sw128(sb + OFF_XR + kk * 2048, 16384, 1024);
+        const uint64_t xl = sdesc_sw128(sb + OFF_XR + 32768 + kk * 2048, 16384, 1024);
+        const uint64_t wh = sdesc_sw128(wsb + kk * 2048, 16384, 1024);
+        const uint64_t wl = sdesc_sw128(wsb + 16384 + kk * 2048, 16384, 1024);
+        mma_f16(tmem + TM_P, xh, wh, id_p, kk > 0);
+        mma_f16(tmem + TM_P, xh, wl, id_p, 1);
+        mma_f16(tmem + TM_P, xl, wh, id_p, 1);
+      }
+      mma_commit(&bar_mma);
+    }
+    if (!wait_mma()) break;
+
+    // R^T[n][t] = (U^T - P^T)[n][t] exp(G_C - G_t) -> K-major B tile [n][t] hi/lo.
+#pragma unroll 1
+    for (int c0 = 0; c0 < C; c0 += 16) {
+      float p[16], u[16];
+      tmem_ld16(tmem + lane_base + TM_P + c0, p);
+      if (isS) tmem_ld16(tmem + lane_base + TM_U + c0, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) p[q] = ((isS ? u[q] : 0.f) - p[q]) * sR[c0 + q];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint4 hi, lo;
+        split8(p + 8 * hf, hi, lo);
+        const uint32_t off = sw128_offset((uint32_t)tid, ((uint32_t)c0 >> 3) + hf);
+        *reinterpret_cast<uint4 *>(sm + OFF_XR + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + OFF_XR + 16384 + off) = lo;
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // X += K^T R: M = 128 (i), N = 128 (n), K = 64 (t).
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ak = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
+        mma_f16(tmem + TM_X, ak, sdesc_sw128(sb + OFF_XR + kk * 32, 16, 1024), id_x, 1);
+        mma_f16(tmem + TM_X, ak, sdesc_sw128(sb + OFF_XR + 16384 + kk * 32, 16, 1024), id_x, 1);
+      }
+      mma_commit(&bar_mma);
+    }
+    if (!wait_mma()) break;
+    // This stage is consumed: prefetch chunk c + 2 into it.
+    if (tid == 0 && c + 2 < nchunks) issue(c + 2);
+  }
+
+  if (!abort_flag) {
+    float *out = (isS ? a.S_out : a.T_out) + (((size_t)s * a.H + h) * D + tid) * D;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + TM_X + c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 16; q += 4)
+        *reinterpret_cast<float4 *>(out + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+    }
+  } else if (tid == 0) {
+    // Let any copy or MMA still in flight land before the memory is released.
+    mbar_wait_cycles(&bar_mma, mph, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_tma[0], 0, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_tma[1], 0, nullptr, 200000000LL);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+size_t bytes_per_head(int n_seg, int64_t max_len) {
+  const int64_t chunks = (max_len + C - 1) / C;
+  return (size_t)n_seg * (size_t)(chunks > 0 ? chunks : 1) * WS_REC;
+}
+
+}  // namespace
+
+bool build_tc_supported(int D_, int fam, int in_dtype, bool want_o) {
+  return D_ == D && in_dtype == HYPIC_BF16 && !want_o &&
+         (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
+}
+
+size_t build_tc_min_workspace(int n_seg, int64_t max_len) { return bytes_per_head(n_seg, max_len); }
+
+size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len) {
+  if (H <= 0 || n_seg <= 0) return 0;
+  const size_t per = bytes_per_head(n_seg, max_len);
+  size_t heads = WS_CAP / per;
+  if (heads < 1) heads = 1;
+  if (heads > (size_t)H) heads = (size_t)H;
+  return heads * per;
+}
+
+// Runs the build over head blocks that fit the workspace: prep then chain for each block.
+cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, cudaStream_t st) {
+  const size_t per = bytes_per_head(r.n_seg, r.seg.max_len);
+  const int Hb = (int)((ws_bytes / per) < (size_t)r.H ? ws_bytes / per : (size_t)r.H);
+  if (Hb < 1 || ws == nullptr) return cudaErrorMemoryAllocation;
+  BuildTcArgs a{};
+  a.H = r.H;
+  a.n_seg = r.n_seg;
+  a.bounds = r.seg.bounds;
+  a.len0 = r.seg.bounds ? 0 : r.seg.uni_len;
+  a.max_len = r.seg.max_len;
+  a.n_tokens = r.seg.n_tokens < 0 ? INT64_MAX : r.seg.n_tokens;
+  a.max_chunks = (int)((r.seg.max_len + C - 1) / C);
+  if (a.max_chunks < 1) a.max_chunks = 1;
+  a.fam = r.fam;
+  a.alpha = r.src.alpha;
+  a.beta = r.src.beta;
+  a.T_out = r.T_out;
+  a.S_out = r.S_out;
+  a.ws = static_cast<uint8_t *>(ws);
+  a.err = r.err;
+  const uint64_t n_tok = r.seg.n_tokens < 0 ? (uint64_t)1 << 31 : (uint64_t)r.seg.n_tokens;
+  CUtensorMap mk, mv;
+  if (!make_tmap_bf16_2d(&mk, r.src.k, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&mv, r.src.v, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(wy_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  for (int h0 = 0; h0 < r.H; h0 += Hb) {
+    a.h0 = h0;
+    a.Hb = (r.H - h0) < Hb ? (r.H - h0) : Hb;
+    const long long g1 = (long long)r.n_seg * a.max_chunks * a.Hb;
+    const long long g2 = (long long)r.n_seg * a.Hb * 2;
+    if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    wy_prep_kernel<<<(unsigned)g1, NT, P_SMEM, st>>>(mk, a);
+    chain_tc_kernel<<<(unsigned)g2, NT, SMEM_BYTES, st>>>(mk, mv, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace hypic

@@ -151,3 +151,20 @@ def test_binding_refuses_cpu_tensors():
     k = torch.zeros(4, 2, 16)
     with pytest.raises(ValueError, match="CUDA"):
         hy.segment_build(k, k, torch.zeros(4, 2), torch.zeros(4, 2))
+
+
+def test_build_workspace_contract(lib):
+    sh = L.shape(32, 128, "gated_delta", "bf16")
+    per_head = 8 * 64 * 33280
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(sh), 8, 4096) == 32 * per_head
+    # shapes that run without a workspace
+    for fam, dt in (("scalar", "bf16"), ("gated_delta", "f32")):
+        s2 = L.shape(32, 128, fam, dt)
+        assert lib.hypic_build_workspace_bytes(ctypes.byref(s2), 8, 4096) == 0
+    # less than one head's records: rejected on the host before any launch
+    p = _fake()
+    r = lib.hypic_segment_build(ctypes.byref(sh), p, p, None, p, p, 4096, p, p, None, p, per_head // 8 - 16,
+                                None)
+    assert r == L.HYPIC_ENOSPACE
+    r = lib.hypic_segment_build(ctypes.byref(sh), p, p, None, p, p, 4096, p, p, None, None, 0, None)
+    assert r == L.HYPIC_ENOSPACE

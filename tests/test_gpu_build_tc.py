@@ -1,0 +1,103 @@
+"""GPU parity of the chunked tensor-core build (d = 128, bf16 inputs, delta families).
+
+Bodies of ragged lengths (empty, shorter than a chunk, exact multiples, long) on
+one token axis, against the float64 oracle at the bf16-path tolerance.  Extra
+cases keep T_C far from underflow so the T half is really tested: DeltaNet
+(a = 1) and gated delta with slow decay a = exp(-softplus(z) / 1024).
+"""
+from __future__ import annotations
+
+import os
+
+import pytest
+import torch
+
+import linear_attention_state_gb300 as hy
+import workloads as W
+from refs import TOL_BF16, host_tokens, np64, ref_pair, relerr
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from linear_attention_state_gb300 import build
+    build.build_library()
+    hy.load()
+    assert hy.stream_status() == 0
+
+
+def run_case(family, lens, H, key, gate_div=None, gap=7):
+    n = sum(lens) + gap * (len(lens) + 1)
+    g = W.generator(DEV, 6000, key)
+    tok = W.draw_tokens(g, n, H, 128, family, "bf16", DEV, gate_div=gate_div, need_q=False)
+    bounds, off = [], gap
+    for L_ in lens:
+        bounds.append((off, off + L_))
+        off += L_ + gap
+    T, S = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                    tok["beta"], family=family)
+    assert hy.stream_status() == 0
+    return tok, bounds, T, S
+
+
+def check(family, tok, bounds, T, S, H):
+    host = host_tokens(tok, list(range(H)))
+    eT, eS = [], []
+    for s, (b, e) in enumerate(bounds):
+        for h in range(H):
+            Tr, Sr = ref_pair(family, host, h, b, e)
+            eT.append(relerr(np64(T[s, h]), Tr))
+            if e > b:
+                eS.append(relerr(np64(S[s, h]), Sr))
+    return max(eT), max(eS) if eS else 0.0
+
+
+@pytest.mark.parametrize("family", ["delta", "gated_delta"])
+def test_ragged_bodies(family):
+    lens = [0, 1, 37, 63, 64, 65, 128, 200, 1000]
+    H = 3
+    tok, bounds, T, S = run_case(family, lens, H, key=1 if family == "delta" else 2)
+    eT, eS = check(family, tok, bounds, T, S, H)
+    print(f"{family}: max rel err T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+    for s, (b, e) in enumerate(bounds):
+        if e == b:
+            assert torch.equal(T[s], torch.eye(128, device=DEV).expand(H, 128, 128))
+            assert float(S[s].abs().max()) == 0.0
+
+
+def test_slow_decay_keeps_T_large():
+    lens = [256, 512, 1024]
+    H = 2
+    tok, bounds, T, S = run_case("gated_delta", lens, H, key=3, gate_div=1024.0)
+    eT, eS = check("gated_delta", tok, bounds, T, S, H)
+    print(f"slow-decay GDN: T {eT:.2e} S {eS:.2e}, |T| {float(T.norm(dim=(-2, -1)).min()):.3e}")
+    assert float(T.norm(dim=(-2, -1)).min()) > 1e-3
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+
+
+def test_deltanet_four_segments_of_256():
+    lens = [256, 256, 256, 256]
+    H = 4
+    tok, bounds, T, S = run_case("delta", lens, H, key=4, gap=0)
+    eT, eS = check("delta", tok, bounds, T, S, H)
+    print(f"DeltaNet 4 x 256: T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+
+
+def test_tensor_core_path_agrees_with_recurrent_path(monkeypatch):
+    lens = [300, 64, 5]
+    H = 2
+    tok, bounds, T, S = run_case("gated_delta", lens, H, key=5)
+    monkeypatch.setenv("HYPIC_BUILD_PATH", "recurrent")
+    T2, S2 = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                      tok["beta"], family="gated_delta")
+    monkeypatch.delenv("HYPIC_BUILD_PATH")
+    assert hy.stream_status() == 0
+    for s in range(len(lens)):
+        for h in range(H):
+            assert relerr(np64(S[s, h]), np64(S2[s, h])) <= TOL_BF16
+            assert relerr(np64(T[s, h]), np64(T2[s, h]), tau=1e-30) <= TOL_BF16
+    assert os.environ.get("HYPIC_BUILD_PATH") is None

@@ -130,6 +130,35 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
 size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
 
 /*
+ * Allocation-free batched build.  No counterpart in the paper: it exists for
+ * callers that cannot allocate device memory themselves -- code embedded in a
+ * host framework that owns every device allocation through its own pool and
+ * hands out no allocator, or a serving process that must not allocate after
+ * start-up -- and so cannot pass the workspace hypic_segment_build_batched
+ * wants.  Arguments, layouts and results are those of
+ * hypic_segment_build_batched; the caller still passes inputs and outputs.
+ * It allocates nothing: where the build needs a workspace it uses a fixed
+ * scratch array of HYPIC_NOALLOC_SCRATCH_BYTES that lives in the library, so
+ * every GPU that loads the library holds that memory until the process exits.
+ * Limit: one head's operand records must fit the scratch, i.e.
+ * n_seg * ceil(max_len / 64) * 33,280 <= HYPIC_NOALLOC_SCRATCH_BYTES
+ * (n_seg * ceil(max_len / 64) <= 2016); larger requests return HYPIC_ENOSPACE
+ * before anything is enqueued.  More heads are processed in blocks that fit.
+ * The first call on a device looks up the scratch array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  All calls on a device share the one scratch array:
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * corrupt each other's results, so serialise them.  Nothing in the scratch has
+ * to start at zero; every call writes each record before reading it.
+ */
+#define HYPIC_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+hypic_status hypic_segment_build_batched_noalloc(const hypic_shape *shape, int32_t n_seg,
+                                                 const int64_t *seg_bounds, int64_t max_len, int64_t n_tokens,
+                                                 const void *k, const void *v, const void *q,
+                                                 const float *alpha, const float *beta, float *T_out,
+                                                 float *S_out, float *o_out, hypic_stream_t stream);
+
+/*
  * Compose: S = T[i_{n-1}](...(T[i_0] S_init + S0[i_0])...) + S0[i_{n-1}] for
  * each of B requests and every head -- paper Eq. (6) evaluated as n
  * sequential S <- T_C S + S_{C|0} (Method 2).  The pairs live in a pool and

@@ -227,23 +227,31 @@ def cpu_baseline(w, n_heads, threads):
     return tokens_equiv / dt, dt
 
 
-def compose_pool_measure(steps, warmup, dev, peaks):
+def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False):
     """Warm-cache composition: 30 layers x 32 heads, pool of 256 fp32 pairs, 64 requests x 16 segments."""
+    import dataclasses
+
     import torch
 
     import linear_attention_state_gb300 as hy
     import workloads as W
     pw = W.COMPOSE_POOL
+    if pool is not None or n is not None:
+        pw = dataclasses.replace(pw, pool=pool or pw.pool, n=n or pw.n,
+                                 name=f"compose_30x32_d128_pool{pool or pw.pool}_B{pw.B}x{n or pw.n}")
     H, d, P = pw.H, pw.d, pw.pool
-    pool_T = torch.empty((P, H, d, d), device=dev)
-    pool_S = torch.empty((P, H, d, d), device=dev)
-    # Pool pairs: built (untimed) from 1024 seeded gated-delta tokens each.
-    for p in range(P):
-        tok = pw.pair_inputs(p, dev)
-        T, S = hy.segment_build(tok["k"], tok["v"], tok["alpha"], tok["beta"], family="gated_delta")
-        pool_T[p].copy_(T)
-        pool_S[p].copy_(S)
-        del tok, T, S
+    if random_pairs:
+        pool_T, pool_S = W.random_pairs(P, H, d, dev, key=3)
+    else:
+        pool_T = torch.empty((P, H, d, d), device=dev)
+        pool_S = torch.empty((P, H, d, d), device=dev)
+        # Pool pairs: built (untimed) from 1024 seeded gated-delta tokens each.
+        for p in range(P):
+            tok = pw.pair_inputs(p, dev)
+            T, S = hy.segment_build(tok["k"], tok["v"], tok["alpha"], tok["beta"], family="gated_delta")
+            pool_T[p].copy_(T)
+            pool_S[p].copy_(S)
+            del tok, T, S
     idx = pw.request_indices(dev)
     out = torch.empty((pw.B, H, d, d), device=dev)
     torch.cuda.synchronize()
@@ -280,6 +288,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-compose", action="store_true", help="skip the warm-cache composition measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--compose-only", action="store_true",
+                    help="time only the warm-cache composition (profiling aid; prints its own line)")
+    ap.add_argument("--compose-pool", type=int, default=None, help="pool entries per head (default 256)")
+    ap.add_argument("--compose-n", type=int, default=None, help="segments per request (default 16)")
+    ap.add_argument("--compose-random", action="store_true", help="generator-drawn pairs instead of built ones")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -311,6 +324,14 @@ def main():
         if world > 1:
             dist.barrier()
 
+    if args.compose_only:
+        res = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
+                                   args.compose_random)
+        if rank == 0:
+            print(json.dumps({"metric": "compositions/s", "value": res["compositions_per_s"] * world,
+                              "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "compose_pool": res}))
+        return
     req = RequestStep(w, dev)
     status0 = hy.stream_status()
     clocks = ClockSampler(local)
@@ -364,7 +385,8 @@ def main():
     compose = None
     if not args.no_compose:
         del host
-        compose = compose_pool_measure(args.steps, args.warmup, dev, peaks)
+        compose = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
+                                       args.compose_random)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -13,6 +13,9 @@
 // registers at the top of the step.  The scan runs the augmented state
 // [T_p | S_p] as two blocks per head (the T half starts at I and has no
 // addend).  Scalar and diagonal families: one thread per state column.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace hypic {
@@ -339,7 +342,15 @@ cudaError_t launch_t(const ChainArgs &a, cudaStream_t st) {
 
 }  // namespace
 
+// HYPIC_COMPOSE_PATH=simt keeps the fp32 SIMT chain where the tensor-core chain applies
+// (for comparisons); read at every call.
+static bool force_simt() {
+  const char *v = getenv("HYPIC_COMPOSE_PATH");
+  return v && strcmp(v, "simt") == 0;
+}
+
 cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st) {
+  if (compose_tc_supported(a.D, a.fam) && !force_simt()) return launch_compose_tc(a, st);
   if (a.seam.in_dtype == HYPIC_BF16) return launch_t<__nv_bfloat16>(a, st);
   return launch_t<float>(a, st);
 }

@@ -79,4 +79,8 @@ struct ChainArgs {
 };
 cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st);
 
+// tcgen05 composition chain (d = 128, delta families): compose, assemble and scan.
+bool compose_tc_supported(int D, int fam);
+cudaError_t launch_compose_tc(const ChainArgs &a, cudaStream_t st);
+
 }  // namespace hypic

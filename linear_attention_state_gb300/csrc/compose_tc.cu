@@ -1,0 +1,409 @@
+// Tensor-core composition chain for the delta families at d = 128: compose, fused request
+// assembly (seam advance + compose) and the affine scan.
+//
+// Composition applies the cached pairs in prompt order, S <- T_C S + S_{C|0} (HYPIC reading
+// notes, Method 2, paper Eq. (6)); assembly first advances the running state through the w
+// seam tokens of each inner segment and emits o_i = q_i^T S_i (Method 5, seam windows).
+//
+// One CTA of 256 threads per (request, head).  Thread (j, half) owns rows 64 half .. 64 half + 63
+// of column j of the running state S.  Each step computes the transposed product on tcgen05,
+//   D = S_new^T = S^T T^T     (M = 128 columns j, N = 128 rows i, K = 128),
+// with the A operand S^T held in tensor memory (the epilogue writes it there, so S never
+// touches shared memory) and the B operand T^T = T row-major, streamed by TMA.  fp32 accuracy
+// comes from exact three-way bf16 splits of both operands, x = hi + mid + lo, each piece
+// taking the next 8 bits of the 24-bit significand by truncation (bit masks, no conversions),
+// and the six products hi.hi + hi.mid + mid.hi + hi.lo + mid.mid + lo.hi.  The products are
+// accumulated smallest first, so the fp32 accumulator's rounding is paid against the small
+// correction terms and only the final eight hi.hi steps round against the full-size value.
+// The epilogue adds S_{C|0} column j (TMA-staged), runs the next segment's seam tokens on the
+// column in registers (k . S_j, rank-1 update, q . S_j), and splits the column into the three
+// A pieces for the next step.  Grid order is head-major, so the requests that share a head's
+// pool entries run together and re-read them from L2.
+#include <cuda_bf16.h>
+
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace hypic {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int NT = 256;
+constexpr int R = 64;  // rows of the column each thread owns
+
+constexpr uint32_t OFF_TST = 0;                 // T staging, fp32, 4 boxes [128 i][32 k] swizzled
+constexpr uint32_t OFF_TB = 65536;              // 3 pieces x 2 k-blocks x [128 i][64 k] bf16 (K-major B)
+constexpr uint32_t OFF_S0 = OFF_TB + 3 * 32768;  // S0 staging, fp32 [128 i][128 j], row-major
+constexpr uint32_t SMEM_BYTES = OFF_S0 + 65536 + 1024;
+
+constexpr uint32_t TM_D = 0;    // accumulator D = S_new^T: lanes j, columns i
+constexpr uint32_t TM_A = 128;  // three A pieces of S^T, 64 columns each (two bf16 per column)
+constexpr uint32_t TM_COLS = 512;
+
+struct ComposeTcArgs {
+  int H, B, n, w;
+  int B_major;  // 0: grid is head-major (b fastest)
+  const int32_t *idx;
+  int64_t pool_size;
+  const float *S_init;
+  float *S_out;
+  int scan;
+  float *T_rec, *S_rec;
+  int fam;
+  int seam_bf16;
+  const void *seam_k, *seam_v, *seam_q;
+  const float *seam_alpha, *seam_beta;
+  float *o_out;
+  int *err;
+};
+
+// Exact three-way split of two fp32 values into bf16 pieces packed two per 32-bit word:
+// hi keeps the sign, exponent and top 7 stored significand bits (a bf16 value); the remainder
+// r = x - hi is exact in fp32 and is split the same way; lo = r - mid is then a bf16 value
+// (at most 8 significant bits remain), so x = hi + mid + lo holds exactly.
+__device__ __forceinline__ void split3_pair(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const float ha = __uint_as_float(ua & 0xFFFF0000u), hb = __uint_as_float(ub & 0xFFFF0000u);
+  const float ra = a - ha, rb = b - hb;
+  const uint32_t ura = __float_as_uint(ra), urb = __float_as_uint(rb);
+  const float ma = __uint_as_float(ura & 0xFFFF0000u), mb = __uint_as_float(urb & 0xFFFF0000u);
+  const uint32_t ula = __float_as_uint(ra - ma), ulb = __float_as_uint(rb - mb);
+  p0 = __byte_perm(ua, ub, 0x7632);  // upper halves: a in the low word, b in the high word
+  p1 = __byte_perm(ura, urb, 0x7632);
+  p2 = __byte_perm(ula, ulb, 0x7632);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+
+template <typename Tin>
+__device__ __forceinline__ float ld_tok(const void *p, size_t i) {
+  return to_f32<Tin>(static_cast<const Tin *>(p)[i]);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1)
+    compose_tc_kernel(const __grid_constant__ CUtensorMap mapT, const __grid_constant__ CUtensorMap mapS,
+                      ComposeTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_t, bar_s, bar_m;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ float red[2][D];  // partial column dot products of the two row halves
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  float *sS0 = reinterpret_cast<float *>(sm + OFF_S0);
+  const int tid = threadIdx.x, warp = tid / 32;
+  const int H = a.H;
+  int b, h;
+  bool isT = false;  // scan: the T half (starts at I, no addend)
+  if (a.scan) {
+    isT = (blockIdx.x & 1) == 0;
+    h = blockIdx.x >> 1;
+    b = 0;
+  } else if (a.B_major) {
+    h = blockIdx.x % H;
+    b = blockIdx.x / H;
+  } else {
+    b = blockIdx.x % a.B;
+    h = blockIdx.x / a.B;
+  }
+  const int j = tid & (D - 1);   // the state column (= TMEM lane) this thread serves
+  const int half = tid >> 7;     // which 64 rows of it
+  const int i0 = half * R;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const bool addend = !isT;
+
+  auto entry = [&](int step) -> int64_t {
+    int64_t p = a.idx ? (int64_t)a.idx[(size_t)b * a.n + step] : (int64_t)step;
+    if (p < 0 || p >= a.pool_size) {
+      set_error(a.err, HYPIC_EDEVICE);
+      p = 0;
+    }
+    return p;
+  };
+  auto issue_T = [&](int step) {
+    const int row = (int)((entry(step) * H + h) * D);
+    mbar_arrive_expect_tx(&bar_t, 65536);
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) tma_load_2d(sm + OFF_TST + kb * 16384, &mapT, &bar_t, kb * 32, row);
+  };
+  auto issue_S = [&](int step) {
+    const int row = (int)((entry(step) * H + h) * D);
+    mbar_arrive_expect_tx(&bar_s, 65536);
+    tma_load_2d(sm + OFF_S0, &mapS, &bar_s, 0, row);
+  };
+
+  if (tid == 0) {
+    mbar_init(&bar_t, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_m, 1);
+    mbar_fence_init();
+    abort_flag = 0;
+    prefetch_tmap(&mapT);
+    prefetch_tmap(&mapS);
+    if (a.n > 0) {
+      issue_T(0);
+      if (addend) issue_S(0);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+
+  // Initial rows i0 .. i0 + 63 of column j.
+  float x[R];
+  const size_t base_bh = ((size_t)b * H + h) * D * D;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = i0 + r;
+    if (a.scan) x[r] = (isT && i == j) ? 1.f : 0.f;
+    else x[r] = a.S_init ? a.S_init[base_bh + (size_t)i * D + j] : 0.f;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // A pieces of S^T: lane j, rows i0.. as 32 columns (two rows per column) of each piece.
+  auto write_pieces = [&]() {
+#pragma unroll
+    for (int c0 = 0; c0 < R; c0 += 16) {
+      float p0[8], p1[8], p2[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint32_t w0, w1, w2;
+        split3_pair(x[c0 + 2 * q], x[c0 + 2 * q + 1], w0, w1, w2);
+        p0[q] = __uint_as_float(w0);
+        p1[q] = __uint_as_float(w1);
+        p2[q] = __uint_as_float(w2);
+      }
+      const uint32_t col = TM_A + (uint32_t)(i0 + c0) / 2;
+      tmem_st8(tmem + lane_base + col + 0 * 64, p0);
+      tmem_st8(tmem + lane_base + col + 1 * 64, p1);
+      tmem_st8(tmem + lane_base + col + 2 * 64, p2);
+    }
+    tmem_st_wait();
+  };
+  if (a.n > 0) write_pieces();
+
+  const uint32_t idesc = idesc_f32acc(1, 1, 0, 0, 128, 128);
+  const Tin *SK = static_cast<const Tin *>(a.seam_k);
+  const Tin *SV = static_cast<const Tin *>(a.seam_v);
+  const Tin *SQ = static_cast<const Tin *>(a.seam_q);
+  uint32_t ph = 0;
+
+  for (int step = 0; step < a.n; ++step) {
+    // (1) T of this step: fp32 staging -> three bf16 B pieces [128 i][128 k], K-major, swizzled.
+    // Thread (row i, half) converts k in [64 half, 64 half + 64).
+    if (tid == 0 && !mbar_wait_cycles(&bar_t, ph, a.err)) abort_flag = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag) break;
+    {
+      const uint32_t i = (uint32_t)j;
+#pragma unroll
+      for (int kq = 0; kq < 2; ++kq) {
+        const int kb = half * 2 + kq;  // 32-wide staging box
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {  // 8 consecutive k = 32 kb + 8 cp
+          const float4 u = *reinterpret_cast<const float4 *>(sm + OFF_TST + kb * 16384 + sw128_offset(i, 2 * cp));
+          const float4 w4 =
+              *reinterpret_cast<const float4 *>(sm + OFF_TST + kb * 16384 + sw128_offset(i, 2 * cp + 1));
+          uint32_t q0[4], q1[4], q2[4];
+          split3_pair(u.x, u.y, q0[0], q1[0], q2[0]);
+          split3_pair(u.z, u.w, q0[1], q1[1], q2[1]);
+          split3_pair(w4.x, w4.y, q0[2], q1[2], q2[2]);
+          split3_pair(w4.z, w4.w, q0[3], q1[3], q2[3]);
+          const uint32_t chunk = ((uint32_t)(kb & 1) << 2) + (uint32_t)cp;
+          const uint32_t off = (uint32_t)half * 16384 + sw128_offset(i, chunk);
+          *reinterpret_cast<uint4 *>(sm + OFF_TB + 0 * 32768 + off) = make_uint4(q0[0], q0[1], q0[2], q0[3]);
+          *reinterpret_cast<uint4 *>(sm + OFF_TB + 1 * 32768 + off) = make_uint4(q1[0], q1[1], q1[2], q1[3]);
+          *reinterpret_cast<uint4 *>(sm + OFF_TB + 2 * 32768 + off) = make_uint4(q2[0], q2[1], q2[2], q2[3]);
+        }
+      }
+    }
+    fence_proxy_async();  // B pieces are read by the MMA; the staging buffer is refilled by TMA
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      if (step + 1 < a.n) issue_T(step + 1);  // the staging buffer is consumed
+      // (2) D = S^T T^T with six split products (A piece, B piece), smallest first:
+      // (2,0) (1,1) (0,2) (1,0) (0,1) (0,0).
+      const int pa[6] = {2, 1, 0, 1, 0, 0}, pb[6] = {0, 1, 2, 0, 1, 0};
+#pragma unroll
+      for (int pr = 0; pr < 6; ++pr) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t bo = OFF_TB + pb[pr] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16_tmem_a(tmem + TM_D, tmem + TM_A + pa[pr] * 64 + kk * 8, sdesc_sw128(sb + bo, 16, 1024), idesc,
+                         (pr | kk) != 0);
+        }
+      }
+      mma_commit(&bar_m);
+      if (!mbar_wait_cycles(&bar_m, ph, a.err)) abort_flag = 1;
+      if (addend && !mbar_wait_cycles(&bar_s, ph, a.err)) abort_flag = 1;
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (abort_flag) break;
+
+    // (3) Epilogue: rows i0.. of column j of S_new = D row j (+ S_{C|0}).
+#pragma unroll
+    for (int c0 = 0; c0 < R; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + TM_D + i0 + c0, v);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) x[c0 + q] = v[q];
+    }
+    tmem_ld_wait();
+    if (addend) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) x[r] += sS0[(i0 + r) * D + j];
+    }
+    if (a.scan) {
+      float *rec = (isT ? a.T_rec : a.S_rec) + ((size_t)step * H + h) * D * D;
+#pragma unroll
+      for (int r = 0; r < R; ++r) rec[(size_t)(i0 + r) * D + j] = x[r];
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();  // S0 staging is consumed
+    if (step + 1 < a.n) {
+      // (4) Seam tokens of the next segment, token by token on the register column.
+      if (a.w > 0) {
+        float *sk = sS0, *sq = sS0 + D;
+        for (int t = 0; t < a.w; ++t) {
+          const size_t tok = ((size_t)b * (a.n - 1) + step) * a.w + t;
+          const size_t g = (tok * H + h) * D;
+          if (half == 0) sk[j] = ld_tok<Tin>(SK, g + j);
+          else if (a.o_out) sq[j] = ld_tok<Tin>(SQ, g + j);
+          const float at = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
+          const float bt = a.seam_beta[tok * H + h];
+          const float vj = ld_tok<Tin>(SV, g + j);
+          __syncthreads();
+          float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+          for (int r = 0; r < R; r += 4) {
+            c0 = fmaf(sk[i0 + r], x[r], c0);
+            c1 = fmaf(sk[i0 + r + 1], x[r + 1], c1);
+            c2 = fmaf(sk[i0 + r + 2], x[r + 2], c2);
+            c3 = fmaf(sk[i0 + r + 3], x[r + 3], c3);
+          }
+          red[half][j] = (c0 + c1) + (c2 + c3);
+          __syncthreads();
+          const float kx = red[0][j] + red[1][j];
+          const float coef = bt * (vj - at * kx);
+#pragma unroll
+          for (int r = 0; r < R; ++r) x[r] = fmaf(coef, sk[i0 + r], at * x[r]);
+          if (a.o_out) {
+            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; r += 4) {
+              o0 = fmaf(sq[i0 + r], x[r], o0);
+              o1 = fmaf(sq[i0 + r + 1], x[r + 1], o1);
+              o2 = fmaf(sq[i0 + r + 2], x[r + 2], o2);
+              o3 = fmaf(sq[i0 + r + 3], x[r + 3], o3);
+            }
+            __syncthreads();  // everyone has read red
+            red[half][j] = (o0 + o1) + (o2 + o3);
+            __syncthreads();
+            if (half == 0) a.o_out[g + j] = red[0][j] + red[1][j];
+          }
+          fence_proxy_async();  // the buffer is refilled by TMA next
+          __syncthreads();
+        }
+      }
+      if (tid == 0 && addend) issue_S(step + 1);
+      write_pieces();
+    }
+    ph ^= 1u;
+  }
+
+  if (!abort_flag && !a.scan) {
+    float *out = a.S_out + base_bh;
+#pragma unroll
+    for (int r = 0; r < R; ++r) out[(size_t)(i0 + r) * D + j] = x[r];
+  }
+  if (abort_flag && tid == 0) {
+    mbar_wait_cycles(&bar_m, ph, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_t, ph, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_s, ph, nullptr, 200000000LL);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+}  // namespace
+
+bool compose_tc_supported(int D_, int fam) {
+  return D_ == D && (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
+}
+
+cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
+  const uint64_t rows = (uint64_t)c.pool_size * c.H * D;
+  if (rows >= ((uint64_t)1 << 31)) return cudaErrorInvalidValue;
+  CUtensorMap mT, mS;
+  if (!make_tmap_f32_2d(&mT, c.pool_T, rows, D, D, 32, 128)) return cudaErrorInvalidValue;
+  {
+    auto fn = tma_encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(c.pool_S), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  ComposeTcArgs a{};
+  a.H = c.H;
+  a.B = c.B;
+  a.n = c.n;
+  a.w = c.w;
+  a.B_major = 0;
+  a.idx = c.idx;
+  a.pool_size = c.pool_size;
+  a.S_init = c.S_init;
+  a.S_out = c.S_out;
+  a.scan = c.scan;
+  a.T_rec = c.T_rec;
+  a.S_rec = c.S_rec;
+  a.fam = c.fam;
+  a.seam_bf16 = c.seam.in_dtype == HYPIC_BF16;
+  a.seam_k = c.seam.k;
+  a.seam_v = c.seam.v;
+  a.seam_q = c.seam.q;
+  a.seam_alpha = c.seam.alpha;
+  a.seam_beta = c.seam.beta;
+  a.o_out = c.o_out;
+  a.err = c.err;
+  const long long blocks = c.scan ? (long long)c.H * 2 : (long long)c.B * c.H;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e;
+  if (a.seam_bf16) {
+    e = cudaFuncSetAttribute(compose_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    compose_tc_kernel<__nv_bfloat16><<<(unsigned)blocks, NT, SMEM_BYTES, st>>>(mT, mS, a);
+  } else {
+    e = cudaFuncSetAttribute(compose_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    compose_tc_kernel<float><<<(unsigned)blocks, NT, SMEM_BYTES, st>>>(mT, mS, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace hypic

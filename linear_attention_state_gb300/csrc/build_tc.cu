@@ -21,7 +21,7 @@
 //     forward substitution; A diag(b gamma) and A diag(b) split into bf16 hi + lo
 //     and stored to the workspace as ready-made 128-byte-swizzled operand tiles,
 //     with the per-token scales exp(G_C - G_t) and gamma_C.
-//   chain_tc_kernel (one CTA per segment, head and column half of X): the state-
+//   chain_tc_kernel (one 256-thread CTA per segment, head and column half of X): the state-
 //     dependent chain.  Each CTA keeps its 128 x 128 fp32 half of X in tensor
 //     memory for the whole segment (the T half has no writes, the S half does;
 //     they evolve independently).  Per chunk: TMA brings K, V and the chunk's
@@ -81,6 +81,15 @@ __device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, i
   return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * WS_REC;
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+
 // hi = bf16(v), lo = bf16(v - hi) for 8 values, packed for one 16-byte store each.
 __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
   uint32_t h[4], l[4];
@@ -98,11 +107,11 @@ __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
 
 // ------------------------------------------------------------------------------------------------
 // Kernel 1: per (segment, chunk, head) -- gates, Gram, L, A = (I + L)^{-1}, operand tiles.
-constexpr uint32_t P_OFF_K = 0;                    // 16 KB K chunk, two [64 t][64 i] boxes
-constexpr uint32_t P_OFF_L = 16384;                // fp32 [64][64]
-constexpr uint32_t P_OFF_A = P_OFF_L + 16384;      // fp32 [64][64]
-constexpr uint32_t P_OFF_T = P_OFF_A + 16384;      // fp32 [32][32]
-constexpr uint32_t P_SMEM = P_OFF_T + 4096 + 1024;  // + alignment slack
+constexpr int LS = 68;                             // row stride of L (floats): conflict-light, 16-byte rows
+constexpr uint32_t P_OFF_K = 0;                    // 16 KB K chunk, two [64 t][64 i] boxes; later A
+constexpr uint32_t P_OFF_A = 0;                    // fp32 [64][64], over the consumed K chunk
+constexpr uint32_t P_OFF_L = 16384;                // fp32 [64][LS]; T = L21 A11 lives in its unused upper-right block
+constexpr uint32_t P_SMEM = P_OFF_L + 64 * LS * 4 + 1024;  // + alignment slack
 
 __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -113,7 +122,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *sL = reinterpret_cast<float *>(sm + P_OFF_L);
   float *sA = reinterpret_cast<float *>(sm + P_OFF_A);
-  float *sT = reinterpret_cast<float *>(sm + P_OFF_T);
+  float *sT = sL + 32;  // [32][32] with row stride LS: rows 0..31, columns 32..63 of L (never read as L)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int hh = blockIdx.x % a.Hb;
   const int c = (blockIdx.x / a.Hb) % a.max_chunks;
@@ -172,25 +181,42 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
       if (!mbar_wait_cycles(&bar_mma, 0, a.err)) ok_flag = 0;
     }
   }
+  // Decay factors: 2^(G_t - G_s) = e_t f_s with e_t = 2^(G_t - G_m), f_s = 2^(G_m - G_s) around the
+  // middle token m, exact in fp32 while the chunk's total log2-decay stays within 100 (gates
+  // averaging above 0.33 per token); otherwise every factor is taken as one exponential.
+  __shared__ float sE[C], sF[C];
   __syncthreads();
   tc_fence_after();
-  if (tid < C) sBG[tid] = sBv[tid] * exp2f(sG[tid]);
+  const bool separable = (sG[0] - sG[C - 1]) < 100.f;
+  if (tid < C) {
+    sBG[tid] = sBv[tid] * exp2f(sG[tid]);
+    sE[tid] = exp2f(sG[tid] - sG[C / 2]);
+    sF[tid] = exp2f(sG[C / 2] - sG[tid]);
+  }
+  __syncthreads();
   if (ok_flag) {
     // L_ts = b_t 2^(G_t - G_s) Gram_ts (s < t); Gram row t sits in lane 32(t/16) + t%16.
     const int t = warp * 16 + lane;
     const float Gt = lane < 16 ? sG[t] : 0.f;
     const float bt = lane < 16 ? sBv[t] : 0.f;
+    const float be = lane < 16 ? bt * sE[t] : 0.f;
+    float v[64];
+    tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16), v);
+    if (lane < 16) {
+      if (separable) {
 #pragma unroll
-    for (int c0 = 0; c0 < C; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-      tmem_ld_wait();
-      if (lane < 16) {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int sc = c0 + q;
-          sL[t * C + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[q] : 0.f;
+        for (int sc = 0; sc < C; sc += 4) {
+          const float4 f4 = *reinterpret_cast<const float4 *>(sF + sc);
+          float4 o;
+          o.x = (sc + 0 < t) ? be * f4.x * v[sc + 0] : 0.f;
+          o.y = (sc + 1 < t) ? be * f4.y * v[sc + 1] : 0.f;
+          o.z = (sc + 2 < t) ? be * f4.z * v[sc + 2] : 0.f;
+          o.w = (sc + 3 < t) ? be * f4.w * v[sc + 3] : 0.f;
+          *reinterpret_cast<float4 *>(sL + t * LS + sc) = o;
         }
+      } else {
+#pragma unroll
+        for (int sc = 0; sc < C; ++sc) sL[t * LS + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[sc] : 0.f;
       }
     }
   }
@@ -207,7 +233,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
     for (int r = 0; r < 32; ++r) x[r] = (r == cl) ? 1.f : 0.f;
 #pragma unroll
     for (int r = 1; r < 32; ++r) {
-      const float *Lr = sL + (base + r) * C + base;
+      const float *Lr = sL + (base + r) * LS + base;
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
       for (int q = 0; q + 3 < r; q += 4) {
@@ -229,22 +255,43 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
     }
   }
   __syncthreads();
-  // T = L21 A11 (32 x 32).
-  for (int e = tid; e < 1024; e += NT) {
-    const int r = e >> 5, cc = e & 31;
-    float acc = 0.f;
+  // T = L21 A11 and A21 = -A22 T (32 x 32 each): each thread owns a 2 x 4 output tile
+  // (rows 2 (tid / 8) + {0, 1}, columns 4 (tid % 8) + {0..3}).
+  {
+    const int r0 = 2 * (tid >> 3), c0 = 4 * (tid & 7);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 8
-    for (int k = 0; k < 32; ++k) acc = fmaf(sL[(32 + r) * C + k], sA[k * C + cc], acc);
-    sT[r * 32 + cc] = acc;
-  }
-  __syncthreads();
-  // A21 = -A22 T.
-  for (int e = tid; e < 1024; e += NT) {
-    const int r = e >> 5, cc = e & 31;
-    float acc = 0.f;
+    for (int k = 0; k < 32; ++k) {
+      const float a0 = sL[(32 + r0) * LS + k], a1 = sL[(33 + r0) * LS + k];
+      const float4 b4 = *reinterpret_cast<const float4 *>(sA + k * C + c0);
+      acc[0][0] = fmaf(a0, b4.x, acc[0][0]);
+      acc[0][1] = fmaf(a0, b4.y, acc[0][1]);
+      acc[0][2] = fmaf(a0, b4.z, acc[0][2]);
+      acc[0][3] = fmaf(a0, b4.w, acc[0][3]);
+      acc[1][0] = fmaf(a1, b4.x, acc[1][0]);
+      acc[1][1] = fmaf(a1, b4.y, acc[1][1]);
+      acc[1][2] = fmaf(a1, b4.z, acc[1][2]);
+      acc[1][3] = fmaf(a1, b4.w, acc[1][3]);
+    }
+    *reinterpret_cast<float4 *>(sT + r0 * LS + c0) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    *reinterpret_cast<float4 *>(sT + (r0 + 1) * LS + c0) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+    __syncthreads();
+    float bcc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 8
-    for (int k = 0; k < 32; ++k) acc = fmaf(sA[(32 + r) * C + 32 + k], sT[k * 32 + cc], acc);
-    sA[(32 + r) * C + cc] = -acc;
+    for (int k = 0; k < 32; ++k) {
+      const float a0 = sA[(32 + r0) * C + 32 + k], a1 = sA[(33 + r0) * C + 32 + k];
+      const float4 b4 = *reinterpret_cast<const float4 *>(sT + k * LS + c0);
+      bcc[0][0] = fmaf(a0, b4.x, bcc[0][0]);
+      bcc[0][1] = fmaf(a0, b4.y, bcc[0][1]);
+      bcc[0][2] = fmaf(a0, b4.z, bcc[0][2]);
+      bcc[0][3] = fmaf(a0, b4.w, bcc[0][3]);
+      bcc[1][0] = fmaf(a1, b4.x, bcc[1][0]);
+      bcc[1][1] = fmaf(a1, b4.y, bcc[1][1]);
+      bcc[1][2] = fmaf(a1, b4.z, bcc[1][2]);
+      bcc[1][3] = fmaf(a1, b4.w, bcc[1][3]);
+    }
+    *reinterpret_cast<float4 *>(sA + (32 + r0) * C + c0) = make_float4(-bcc[0][0], -bcc[0][1], -bcc[0][2], -bcc[0][3]);
+    *reinterpret_cast<float4 *>(sA + (33 + r0) * C + c0) = make_float4(-bcc[1][0], -bcc[1][1], -bcc[1][2], -bcc[1][3]);
   }
   __syncthreads();
 
@@ -253,11 +300,13 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
   for (int e = tid; e < C * 8; e += NT) {
     const int t = e >> 3, q = e & 7;
     float vb[8], vv[8];
+    const float4 a0 = *reinterpret_cast<const float4 *>(sA + t * C + 8 * q);
+    const float4 a1 = *reinterpret_cast<const float4 *>(sA + t * C + 8 * q + 4);
+    const float av8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float av = sA[t * C + 8 * q + j];
-      vb[j] = av * sBG[8 * q + j];
-      vv[j] = av * sBv[8 * q + j];
+      vb[j] = av8[j] * sBG[8 * q + j];
+      vv[j] = av8[j] * sBv[8 * q + j];
     }
     uint4 hi, lo;
     const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)q);
@@ -275,28 +324,43 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
 
 // ------------------------------------------------------------------------------------------------
 // Kernel 2: per (segment, head, column half) -- the chunk chain on tensor memory.
+//
+// The state is kept transposed, X^T (lanes = the 128 columns n of this half, TMEM columns =
+// rows i), so that both state-dependent products take their A operand straight from tensor
+// memory and read only their B operand from shared memory:
+//   P^T  = X^T Wk^T      A = bf16 hi/lo pieces of X^T (TMEM), B = Wk^T [i][t] (MN-major smem)
+//   X^T  = gamma_C X^T + R^T K
+//                        A = bf16 hi/lo pieces of R^T (TMEM), B = K [t][i] (MN-major, the TMA tile)
+// Wk^T = K^T (A diag(b gamma))^T and U^T = V^T (A diag(b))^T depend on the chunk's inputs only;
+// the MMAs of chunk c + 1 are issued right behind the update of chunk c so they overlap the
+// next chunk's split work.
 constexpr uint32_t OFF_KV = 0;                          // 2 stages x (K 16 KB + V 16 KB)
 constexpr uint32_t OFF_WS = 65536;                      // 2 stages x 33 KB workspace records
 constexpr uint32_t WS_STAGE = 33792;                    // record rounded up to 1024
-constexpr uint32_t OFF_XR = OFF_WS + 2 * WS_STAGE;      // 64 KB: X^T hi|lo, later R^T hi|lo
-constexpr uint32_t SMEM_BYTES = OFF_XR + 65536 + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_WS + 2 * WS_STAGE + 1024;  // + alignment slack
 
-constexpr uint32_t TM_X = 0;    // 128 cols: X half, lanes = rows i
-constexpr uint32_t TM_P = 128;  // 64 cols: P^T, lanes = columns n of the half
-constexpr uint32_t TM_W = 192;  // 64 cols: Wk^T, lanes = i
-constexpr uint32_t TM_U = 256;  // 64 cols: U^T, lanes = j
+constexpr uint32_t TM_X = 0;     // 128 cols: X^T accumulator, lanes n, columns i
+constexpr uint32_t TM_XP = 128;  // 2 x 64 cols: X^T hi, lo (bf16, two i per column)
+constexpr uint32_t TM_P = 256;   // 64 cols: P^T, lanes n, columns t
+constexpr uint32_t TM_RP = 320;  // 2 x 32 cols: R^T hi, lo (bf16, two t per column)
+constexpr uint32_t TM_W = 384;   // 64 cols: Wk^T, lanes i, columns t
+constexpr uint32_t TM_U = 448;   // 64 cols: U^T, lanes j, columns t
 constexpr uint32_t TM_COLS = 512;
 
-__global__ void __launch_bounds__(NT, 1)
+constexpr int NT2 = 256;  // two threads per TMEM lane, each with half of that lane's columns
+
+__global__ void __launch_bounds__(NT2, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_tma[2], bar_mma;
+  __shared__ uint64_t bar_tma[2], bar_x, bar_w;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid / 32;
+  const int row = tid & 127;  // TMEM lane this thread serves
+  const int part = tid >> 7;  // which half of that lane's columns
   const int half = blockIdx.x & 1;  // 0: T columns, 1: S columns
   const int hh = (blockIdx.x >> 1) % a.Hb;
   const int s = (blockIdx.x >> 1) / a.Hb;
@@ -313,7 +377,8 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     mbar_init(&bar_tma[0], 1);
     mbar_init(&bar_tma[1], 1);
-    mbar_init(&bar_mma, 1);
+    mbar_init(&bar_x, 1);
+    mbar_init(&bar_w, 1);
     mbar_fence_init();
     abort_flag = 0;
     prefetch_tmap(&mapK);
@@ -326,36 +391,60 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  auto issue = [&](int c) {
+  auto issue_tma = [&](int c) {
     const int st = c & 1;
-    const int row = (int)(beg + (int64_t)c * C);
+    const int rowt = (int)(beg + (int64_t)c * C);
     uint8_t *kv = sm + OFF_KV + st * 32768;
     uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
     const uint8_t *rec = ws_rec(a, s, c, hh);
     mbar_arrive_expect_tx(&bar_tma[st], isS ? 32768u + WS_REC : 16384u + 16384u + 512u);
-    tma_load_2d(kv, &mapK, &bar_tma[st], h * D, row);
-    tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, row);
+    tma_load_2d(kv, &mapK, &bar_tma[st], h * D, rowt);
+    tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, rowt);
     if (isS) {
-      tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, row);
-      tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, row);
+      tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, rowt);
+      tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, rowt);
       bulk_load(wsd, rec, WS_REC, &bar_tma[st]);
     } else {
       bulk_load(wsd, rec, 16384, &bar_tma[st]);
       bulk_load(wsd + WS_SC, rec + WS_SC, 512, &bar_tma[st]);
     }
   };
-  if (tid == 0) {
-    if (nchunks > 0) issue(0);
-    if (nchunks > 1) issue(1);
+  // Wk^T and U^T of chunk c: M = 128, N = 64, K = 64 (issued by thread 0, then committed).
+  const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);  // A = K^T or V^T (MN-major), B K-major
+  auto issue_wu = [&](int c) {
+    const int st = c & 1;
+    const uint32_t kb = sb + OFF_KV + st * 32768, wb = sb + OFF_WS + st * WS_STAGE;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ak = sdesc_sw128(kb + kk * 2048, 8192, 1024);
+      mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
+      mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
+      if (isS) {
+        const uint64_t av = sdesc_sw128(kb + 16384 + kk * 2048, 8192, 1024);
+        mma_f16(tmem + TM_U, av, sdesc_sw128(wb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
+        mma_f16(tmem + TM_U, av, sdesc_sw128(wb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
+      }
+    }
+    mma_commit(&bar_w);
+  };
+
+  if (tid == 0 && nchunks > 0) {
+    issue_tma(0);
+    if (nchunks > 1) issue_tma(1);
+    if (!mbar_wait_cycles(&bar_tma[0], 0, a.err)) abort_flag = 1;
+    else {
+      tc_fence_after();
+      issue_wu(0);
+    }
   }
 
-  // X starts at [I | 0]: this CTA's half is I (T) or 0 (S).
-  for (int c0 = 0; c0 < D; c0 += 16) {
+  // X^T starts at [I | 0]^T restricted to this half: I (T half) or 0 (S half).
+  for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
     float v[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == tid) ? 1.f : 0.f;
+    for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == row) ? 1.f : 0.f;
     tmem_st16(tmem + lane_base + TM_X + c0, v);
   }
   tmem_st_wait();
@@ -363,81 +452,63 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
 
-  uint32_t mph = 0;
-  const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);  // A = K^T or V^T (MN-major), B K-major
-  const uint32_t id_p = idesc_f32acc(1, 1, 1, 1, 128, 64);   // A = X^T (MN-major), B = Wk^T (MN-major)
-  const uint32_t id_x = idesc_f32acc(1, 1, 1, 0, 128, 128);  // A = K^T (MN-major), B = R K-major
-
-  auto wait_mma = [&]() -> bool {
-    if (tid == 0 && !mbar_wait_cycles(&bar_mma, mph, a.err)) abort_flag = 1;
-    mph ^= 1u;
-    __syncthreads();
-    tc_fence_after();
-    return abort_flag == 0;
-  };
+  const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces (TMEM), B = Wk^T (MN-major)
+  const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces (TMEM), B = K (MN-major)
+  uint32_t ph_x = 0, ph_w = 0;
 
   for (int c = 0; c < nchunks; ++c) {
     const int st = c & 1;
-    const uint32_t kbase = sb + OFF_KV + st * 32768;
-    const uint32_t vbase = kbase + 16384;
     uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+    const uint32_t kbase = sb + OFF_KV + st * 32768;
     const uint32_t wsb = sb + OFF_WS + st * WS_STAGE;
-    if (tid == 0 && !mbar_wait_cycles(&bar_tma[st], (c >> 1) & 1, a.err)) abort_flag = 1;
-    __syncthreads();
     if (abort_flag) break;
     const float *sR = reinterpret_cast<const float *>(wsd + WS_SC);
     const float gamma_C = sR[C];
 
-    // Wk^T = K^T (A diag(b gamma))^T and U^T = V^T (A diag(b))^T: M = 128, N = 64, K = 64.
-    if (tid == 0) {
-      tc_fence_after();
+    // (1) X^T -> bf16 hi/lo pieces in TMEM (lane n, this thread's 64 rows i), and gamma_C X^T
+    // back into the accumulator.
+    {
+      float xv[64];
+      tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ak = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
-        mma_f16(tmem + TM_W, ak, sdesc_sw128(wsb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
-        mma_f16(tmem + TM_W, ak, sdesc_sw128(wsb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
-        if (isS) {
-          const uint64_t av = sdesc_sw128(vbase + kk * 2048, 8192, 1024);
-          mma_f16(tmem + TM_U, av, sdesc_sw128(wsb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
-          mma_f16(tmem + TM_U, av, sdesc_sw128(wsb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float ph[8], pl[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const __nv_bfloat162 hp = __floats2bfloat162_rn(xv[c0 + 2 * q], xv[c0 + 2 * q + 1]);
+          const float2 hf = __bfloat1622float2(hp);
+          const __nv_bfloat162 lp = __floats2bfloat162_rn(xv[c0 + 2 * q] - hf.x, xv[c0 + 2 * q + 1] - hf.y);
+          ph[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
+          pl[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
         }
-      }
-      mma_commit(&bar_mma);
-    }
-
-    // X -> X^T hi/lo (MN-major A, two 64-column blocks); gamma_C X back into TMEM.
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + TM_X + c0, v);
-      tmem_ld_wait();
-      const uint32_t blk = (uint32_t)c0 >> 6;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint4 hi, lo;
-        split8(v + 8 * hf, hi, lo);
-        const uint32_t off = blk * 16384 + sw128_offset((uint32_t)tid, ((uint32_t)(c0 & 63) >> 3) + hf);
-        *reinterpret_cast<uint4 *>(sm + OFF_XR + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + OFF_XR + 32768 + off) = lo;
+        const uint32_t col = (uint32_t)(64 * part + c0) / 2;
+        tmem_st8(tmem + lane_base + TM_XP + col, ph);
+        tmem_st8(tmem + lane_base + TM_XP + 64 + col, pl);
       }
 #pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] *= gamma_C;
-      tmem_st16(tmem + lane_base + TM_X + c0, v);
-    }
-    tmem_st_wait();
-    if (!wait_mma()) break;  // Wk^T, U^T ready; the A tiles in the stage are consumed
-
-    // Wk^T (lanes i, columns t) -> MN-major B tile [i][t] hi/lo, over the consumed A tiles.
-#pragma unroll 1
-    for (int c0 = 0; c0 < C; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + TM_W + c0, v);
-      tmem_ld_wait();
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float sv[16];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+        for (int q = 0; q < 16; ++q) sv[q] = xv[c0 + q] * gamma_C;
+        tmem_st16(tmem + lane_base + TM_X + 64 * part + c0, sv);
+      }
+      tmem_st_wait();
+    }
+    // (2) Wk^T of this chunk (issued one chunk ahead) -> MN-major B tile [i][t] hi/lo over the
+    // consumed A tiles of the stage; this thread converts t in [32 part, 32 part + 32).
+    if (tid == 0 && !mbar_wait_cycles(&bar_w, ph_w, a.err)) abort_flag = 1;
+    ph_w ^= 1u;
+    __syncthreads();
+    tc_fence_after();
+    if (abort_flag) break;
+    {
+      float wv[32];
+      tmem_ld32(tmem + lane_base + TM_W + 32 * part, wv);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
         uint4 hi, lo;
-        split8(v + 8 * hf, hi, lo);
-        const uint32_t off = sw128_offset((uint32_t)tid, ((uint32_t)c0 >> 3) + hf);
+        split8(wv + 8 * q4, hi, lo);
+        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(4 * part + q4));
         *reinterpret_cast<uint4 *>(wsd + off) = hi;
         *reinterpret_cast<uint4 *>(wsd + 16384 + off) = lo;
       }
@@ -446,75 +517,84 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // P^T = X^T Wk^T: M = 128 (n), N = 64 (t), K = 128 (i); hi.hi + hi.lo + lo.hi.
+    // (3) P^T = X^T Wk^T: M = 128 (n), N = 64 (t), K = 128 (i); hi.hi + hi.lo + lo.hi.
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t xh = sdesc_sw128(sb + OFF_XR + kk * 2048, 16384, 1024);
-        const uint64_t xl = sdesc_sw128(sb + OFF_XR + 32768 + kk * 2048, 16384, 1024);
         const uint64_t wh = sdesc_sw128(wsb + kk * 2048, 16384, 1024);
         const uint64_t wl = sdesc_sw128(wsb + 16384 + kk * 2048, 16384, 1024);
-        mma_f16(tmem + TM_P, xh, wh, id_p, kk > 0);
-        mma_f16(tmem + TM_P, xh, wl, id_p, 1);
-        mma_f16(tmem + TM_P, xl, wh, id_p, 1);
+        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wh, id_p, kk > 0);
+        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wl, id_p, 1);
+        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + 64 + kk * 8, wh, id_p, 1);
       }
-      mma_commit(&bar_mma);
+      mma_commit(&bar_x);
+      if (!mbar_wait_cycles(&bar_x, ph_x, a.err)) abort_flag = 1;
     }
-    if (!wait_mma()) break;
+    ph_x ^= 1u;
+    __syncthreads();
+    tc_fence_after();
+    if (abort_flag) break;
 
-    // R^T[n][t] = (U^T - P^T)[n][t] exp(G_C - G_t) -> K-major B tile [n][t] hi/lo.
-#pragma unroll 1
-    for (int c0 = 0; c0 < C; c0 += 16) {
-      float p[16], u[16];
-      tmem_ld16(tmem + lane_base + TM_P + c0, p);
-      if (isS) tmem_ld16(tmem + lane_base + TM_U + c0, u);
-      tmem_ld_wait();
+    // (4) R^T[n][t] = (U^T - P^T)[n][t] exp(G_C - G_t) -> bf16 hi/lo pieces in TMEM (lane n);
+    // this thread handles t in [32 part, 32 part + 32).
+    {
+      float pv[32], uv[32];
+      tmem_ld32(tmem + lane_base + TM_P + 32 * part, pv);
+      if (isS) tmem_ld32(tmem + lane_base + TM_U + 32 * part, uv);
+      float ph[16], pl[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) p[q] = ((isS ? u[q] : 0.f) - p[q]) * sR[c0 + q];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint4 hi, lo;
-        split8(p + 8 * hf, hi, lo);
-        const uint32_t off = sw128_offset((uint32_t)tid, ((uint32_t)c0 >> 3) + hf);
-        *reinterpret_cast<uint4 *>(sm + OFF_XR + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + OFF_XR + 16384 + off) = lo;
+      for (int q = 0; q < 16; ++q) {
+        const int t = 32 * part + 2 * q;
+        const float r0 = ((isS ? uv[2 * q] : 0.f) - pv[2 * q]) * sR[t];
+        const float r1 = ((isS ? uv[2 * q + 1] : 0.f) - pv[2 * q + 1]) * sR[t + 1];
+        const __nv_bfloat162 hp = __floats2bfloat162_rn(r0, r1);
+        const float2 hf = __bfloat1622float2(hp);
+        const __nv_bfloat162 lp = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
+        ph[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
+        pl[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
       }
+      tmem_st16(tmem + lane_base + TM_RP + 16 * part, ph);
+      tmem_st16(tmem + lane_base + TM_RP + 32 + 16 * part, pl);
+      tmem_st_wait();
     }
-    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
-    // X += K^T R: M = 128 (i), N = 128 (n), K = 64 (t).
+    // (5) X^T += R^T K: M = 128 (n), N = 128 (i), K = 64 (t); then the next chunk's Wk^T, U^T.
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ak = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
-        mma_f16(tmem + TM_X, ak, sdesc_sw128(sb + OFF_XR + kk * 32, 16, 1024), id_x, 1);
-        mma_f16(tmem + TM_X, ak, sdesc_sw128(sb + OFF_XR + 16384 + kk * 32, 16, 1024), id_x, 1);
+        const uint64_t bk = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
+        mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + kk * 8, bk, id_x, 1);
+        mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + 32 + kk * 8, bk, id_x, 1);
       }
-      mma_commit(&bar_mma);
+      mma_commit(&bar_x);
+      if (c + 1 < nchunks) {
+        if (!mbar_wait_cycles(&bar_tma[(c + 1) & 1], ((c + 1) >> 1) & 1, a.err)) abort_flag = 1;
+        else issue_wu(c + 1);
+      }
+      if (!mbar_wait_cycles(&bar_x, ph_x, a.err)) abort_flag = 1;
+      // This stage (K, V, records and the Wk tile) is consumed: prefetch chunk c + 2 into it.
+      if (!abort_flag && c + 2 < nchunks) issue_tma(c + 2);
     }
-    if (!wait_mma()) break;
-    // This stage is consumed: prefetch chunk c + 2 into it.
-    if (tid == 0 && c + 2 < nchunks) issue(c + 2);
+    ph_x ^= 1u;
+    __syncthreads();
+    tc_fence_after();
   }
 
   if (!abort_flag) {
-    float *out = (isS ? a.S_out : a.T_out) + (((size_t)s * a.H + h) * D + tid) * D;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + TM_X + c0, v);
-      tmem_ld_wait();
+    // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
+    float *out = (isS ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
+    float xv[64];
+    tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
 #pragma unroll
-      for (int q = 0; q < 16; q += 4)
-        *reinterpret_cast<float4 *>(out + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-    }
+    for (int q = 0; q < 64; ++q) out[(size_t)(64 * part + q) * D + row] = xv[q];
   } else if (tid == 0) {
     // Let any copy or MMA still in flight land before the memory is released.
-    mbar_wait_cycles(&bar_mma, mph, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_x, ph_x, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_w, ph_w, nullptr, 200000000LL);
     mbar_wait_cycles(&bar_tma[0], 0, nullptr, 200000000LL);
     mbar_wait_cycles(&bar_tma[1], 0, nullptr, 200000000LL);
   }
@@ -584,7 +664,7 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     const long long g2 = (long long)r.n_seg * a.Hb * 2;
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     wy_prep_kernel<<<(unsigned)g1, NT, P_SMEM, st>>>(mk, a);
-    chain_tc_kernel<<<(unsigned)g2, NT, SMEM_BYTES, st>>>(mk, mv, a);
+    chain_tc_kernel<<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

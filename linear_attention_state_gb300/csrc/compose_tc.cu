@@ -258,14 +258,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (abort_flag) break;
 
     // (3) Epilogue: rows i0.. of column j of S_new = D row j (+ S_{C|0}).
-#pragma unroll
-    for (int c0 = 0; c0 < R; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + TM_D + i0 + c0, v);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) x[c0 + q] = v[q];
-    }
-    tmem_ld_wait();
+    tmem_ld64(tmem + lane_base + TM_D + i0, x);
     if (addend) {
 #pragma unroll
       for (int r = 0; r < R; ++r) x[r] += sS0[(i0 + r) * D + j];

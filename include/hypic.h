@@ -219,6 +219,17 @@ hypic_status hypic_assemble(const hypic_shape *shape, int32_t B, int32_t n, int3
  */
 hypic_status hypic_stream_status(hypic_stream_t stream);
 
+/*
+ * Self-test of failure detection (no counterpart in the paper).  Every wait inside
+ * the library's kernels is bounded: when it runs out, the kernel records
+ * HYPIC_ETIMEOUT in the status word and returns instead of hanging.  This call
+ * enqueues a one-thread kernel whose wait can never be satisfied, bounded by
+ * limit_cycles SM clock cycles (0 .. 4e9; a million cycles is about half a
+ * millisecond), so a caller or a test can check that the timeout is reported by
+ * hypic_stream_status() and that the device stays usable afterwards.
+ */
+hypic_status hypic_selftest_bounded_wait(int64_t limit_cycles, hypic_stream_t stream);
+
 /* Static, never NULL. */
 const char *hypic_strerror(hypic_status status);
 

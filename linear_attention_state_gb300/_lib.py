@@ -42,6 +42,7 @@ SIGNATURES = {
     "hypic_assemble": (_i32, [_SP, _i32, _i32, _i32, _i32p, _i64, _fp, _fp, _vp, _vp, _vp, _fp, _fp, _fp,
                               _fp, _fp, _vp]),
     "hypic_stream_status": (_i32, [_vp]),
+    "hypic_selftest_bounded_wait": (_i32, [_i64, _vp]),
 }
 
 _lock = threading.Lock()

@@ -286,6 +286,13 @@ hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T,
   return from_cuda(launch_chain(a, (cudaStream_t)stream));
 }
 
+hypic_status hypic_selftest_bounded_wait(int64_t limit_cycles, hypic_stream_t stream) {
+  if (limit_cycles < 0 || limit_cycles > 4000000000LL) return HYPIC_EINVAL;
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  return from_cuda(launch_bounded_wait_selftest(limit_cycles, err, (cudaStream_t)stream));
+}
+
 hypic_status hypic_stream_status(hypic_stream_t stream) {
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaStreamSynchronize(st) != cudaSuccess) return HYPIC_ECUDA;

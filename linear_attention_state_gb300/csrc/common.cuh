@@ -83,4 +83,7 @@ cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st);
 bool compose_tc_supported(int D, int fam);
 cudaError_t launch_compose_tc(const ChainArgs &a, cudaStream_t st);
 
+// Bounded-wait self-test (see hypic_selftest_bounded_wait).
+cudaError_t launch_bounded_wait_selftest(long long limit_cycles, int *err, cudaStream_t st);
+
 }  // namespace hypic

@@ -34,9 +34,9 @@ FLOP_PER_CHUNK_WY = 3 * 2 * 64 * 64 * D + 2 * 2 * 64 * D * (2 * D)  # G, U, W; W
 FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
-# dram__bytes_read.sum + dram__bytes_write.sum of one build_tc_kernel launch on this workload,
-# from the committed ncu capture (None until taken for the current kernel).
-BUILD_TC_TRAFFIC = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
+# this workload, from the ncu capture summarised in profiles/build_tc_32h_d128_8x4096.md.
+BUILD_TC_TRAFFIC = 277_319_000 + 482_150_912 + 1_082_203_000 + 33_041_920
 
 
 def load_peaks():

@@ -18,7 +18,7 @@
 //   wy_prep_kernel  (one CTA per chunk and head, all chunks in parallel): the
 //     state-independent part.  TMA loads K; gates and their log-cumsum; Gram =
 //     K K^T on tcgen05 (M = 64); L; A = (I + L)^{-1} in fp32 by 2 x 2 blocked
-//     forward substitution; A diag(b gamma) and A diag(b) split into bf16 hi + lo
+//     forward substitution; A diag(b gamma) and -A diag(b) split into bf16 hi + lo
 //     and stored to the workspace as ready-made 128-byte-swizzled operand tiles,
 //     with the per-token scales exp(G_C - G_t) and gamma_C.
 //   chain_tc_kernel (one 256-thread CTA per segment, head and column half of X): the state-
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       vb[j] = av8[j] * sBG[8 * q + j];
-      vv[j] = av8[j] * sBv[8 * q + j];
+      vv[j] = -av8[j] * sBv[8 * q + j];  // negated: the chain accumulates -U under P
     }
     uint4 hi, lo;
     const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)q);
@@ -328,12 +328,13 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
 // The state is kept transposed, X^T (lanes = the 128 columns n of this half, TMEM columns =
 // rows i), so that both state-dependent products take their A operand straight from tensor
 // memory and read only their B operand from shared memory:
-//   P^T  = X^T Wk^T      A = bf16 hi/lo pieces of X^T (TMEM), B = Wk^T [i][t] (MN-major smem)
-//   X^T  = gamma_C X^T + R^T K
-//                        A = bf16 hi/lo pieces of R^T (TMEM), B = K [t][i] (MN-major, the TMA tile)
-// Wk^T = K^T (A diag(b gamma))^T and U^T = V^T (A diag(b))^T depend on the chunk's inputs only;
-// the MMAs of chunk c + 1 are issued right behind the update of chunk c so they overlap the
-// next chunk's split work.
+//   P^T - U^T = X^T Wk^T - U^T   A = bf16 hi/lo pieces of X^T (TMEM), B = Wk^T [i][t] (MN-major)
+//   X^T = gamma_C X^T + R^T K    A = bf16 hi/lo pieces of R^T (TMEM), B = K [t][i] (MN-major TMA tile)
+// Wk^T = K^T (A diag(b gamma))^T and -U^T = V^T (-A diag(b))^T depend on the chunk's inputs only;
+// -U^T is written into the P^T accumulator, which the P MMAs then add onto.  Warp 8 issues
+// every TMA copy and MMA; warps 0-7 (two threads per TMEM lane) do the conversions.  The two
+// sides hand over through mbarriers: MMA completions arrive through tcgen05.commit, the
+// conversion warps arrive after their TMEM and shared-memory writes are fenced.
 constexpr uint32_t OFF_KV = 0;                          // 2 stages x (K 16 KB + V 16 KB)
 constexpr uint32_t OFF_WS = 65536;                      // 2 stages x 33 KB workspace records
 constexpr uint32_t WS_STAGE = 33792;                    // record rounded up to 1024
@@ -341,26 +342,37 @@ constexpr uint32_t SMEM_BYTES = OFF_WS + 2 * WS_STAGE + 1024;  // + alignment sl
 
 constexpr uint32_t TM_X = 0;     // 128 cols: X^T accumulator, lanes n, columns i
 constexpr uint32_t TM_XP = 128;  // 2 x 64 cols: X^T hi, lo (bf16, two i per column)
-constexpr uint32_t TM_P = 256;   // 64 cols: P^T, lanes n, columns t
+constexpr uint32_t TM_P = 256;   // 64 cols: P^T - U^T, lanes n, columns t
 constexpr uint32_t TM_RP = 320;  // 2 x 32 cols: R^T hi, lo (bf16, two t per column)
 constexpr uint32_t TM_W = 384;   // 64 cols: Wk^T, lanes i, columns t
-constexpr uint32_t TM_U = 448;   // 64 cols: U^T, lanes j, columns t
 constexpr uint32_t TM_COLS = 512;
 
-constexpr int NT2 = 256;  // two threads per TMEM lane, each with half of that lane's columns
+constexpr int NCONV = 256;        // conversion threads: two per TMEM lane
+constexpr int NT2 = NCONV + 32;   // + the issuing warp
+
+// hi = truncation of x to bf16, lo = bf16 rounding of the exact remainder, for two values;
+// returns the packed hi pair and lo pair (first value in the low half).
+__device__ __forceinline__ void split2_pair(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const float ra = a - __uint_as_float(ua & 0xFFFF0000u), rb = b - __uint_as_float(ub & 0xFFFF0000u);
+  hi = __byte_perm(ua, ub, 0x7632);
+  const __nv_bfloat162 lp = __floats2bfloat162_rn(ra, rb);
+  lo = *reinterpret_cast<const uint32_t *>(&lp);
+}
 
 __global__ void __launch_bounds__(NT2, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_tma[2], bar_x, bar_w;
+  __shared__ uint64_t bar_tma[2], bar_w, bar_p, bar_x, bar_r1, bar_r2;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
-  const int tid = threadIdx.x, warp = tid / 32;
-  const int row = tid & 127;  // TMEM lane this thread serves
-  const int part = tid >> 7;  // which half of that lane's columns
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const bool issuer = warp == NCONV / 32;
+  const int row = tid & 127;  // TMEM lane a conversion thread serves
+  const int part = (tid >> 7) & 1;  // which half of that lane's columns
   const int half = blockIdx.x & 1;  // 0: T columns, 1: S columns
   const int hh = (blockIdx.x >> 1) % a.Hb;
   const int s = (blockIdx.x >> 1) / a.Hb;
@@ -377,12 +389,13 @@ __global__ void __launch_bounds__(NT2, 1)
   if (tid == 0) {
     mbar_init(&bar_tma[0], 1);
     mbar_init(&bar_tma[1], 1);
-    mbar_init(&bar_x, 1);
     mbar_init(&bar_w, 1);
+    mbar_init(&bar_p, 1);
+    mbar_init(&bar_x, 1);
+    mbar_init(&bar_r1, NCONV);
+    mbar_init(&bar_r2, NCONV);
     mbar_fence_init();
     abort_flag = 0;
-    prefetch_tmap(&mapK);
-    if (isS) prefetch_tmap(&mapV);
   }
   if (warp == 0) {
     tmem_alloc(&tmem_slot, TM_COLS);
@@ -393,210 +406,211 @@ __global__ void __launch_bounds__(NT2, 1)
   const uint32_t tmem = tmem_slot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  auto issue_tma = [&](int c) {
-    const int st = c & 1;
-    const int rowt = (int)(beg + (int64_t)c * C);
-    uint8_t *kv = sm + OFF_KV + st * 32768;
-    uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
-    const uint8_t *rec = ws_rec(a, s, c, hh);
-    mbar_arrive_expect_tx(&bar_tma[st], isS ? 32768u + WS_REC : 16384u + 16384u + 512u);
-    tma_load_2d(kv, &mapK, &bar_tma[st], h * D, rowt);
-    tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, rowt);
-    if (isS) {
-      tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, rowt);
-      tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, rowt);
-      bulk_load(wsd, rec, WS_REC, &bar_tma[st]);
-    } else {
-      bulk_load(wsd, rec, 16384, &bar_tma[st]);
-      bulk_load(wsd + WS_SC, rec + WS_SC, 512, &bar_tma[st]);
-    }
-  };
-  // Wk^T and U^T of chunk c: M = 128, N = 64, K = 64 (issued by thread 0, then committed).
-  const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);  // A = K^T or V^T (MN-major), B K-major
-  auto issue_wu = [&](int c) {
-    const int st = c & 1;
-    const uint32_t kb = sb + OFF_KV + st * 32768, wb = sb + OFF_WS + st * WS_STAGE;
+  if (issuer) {
+    // ----------------------------------------------------------------------------- issuing warp
+    if (lane == 0) {
+      prefetch_tmap(&mapK);
+      if (isS) prefetch_tmap(&mapV);
+      auto issue_tma = [&](int c) {
+        const int st = c & 1;
+        const int rowt = (int)(beg + (int64_t)c * C);
+        uint8_t *kv = sm + OFF_KV + st * 32768;
+        uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+        const uint8_t *rec = ws_rec(a, s, c, hh);
+        mbar_arrive_expect_tx(&bar_tma[st], isS ? 32768u + WS_REC : 16384u + 16384u + 512u);
+        tma_load_2d(kv, &mapK, &bar_tma[st], h * D, rowt);
+        tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, rowt);
+        if (isS) {
+          tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, rowt);
+          tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, rowt);
+          bulk_load(wsd, rec, WS_REC, &bar_tma[st]);
+        } else {
+          bulk_load(wsd, rec, 16384, &bar_tma[st]);
+          bulk_load(wsd + WS_SC, rec + WS_SC, 512, &bar_tma[st]);
+        }
+      };
+      const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = K^T or V^T (MN-major), B K-major
+      const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);    // A = X^T pieces (TMEM), B = Wk^T
+      const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);   // A = R^T pieces (TMEM), B = K
+      // Wk^T -> TM_W and -U^T -> TM_P for chunk c (M = 128, N = 64, K = 64).
+      auto issue_wu = [&](int c) {
+        const int st = c & 1;
+        const uint32_t kb = sb + OFF_KV + st * 32768, wb = sb + OFF_WS + st * WS_STAGE;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ak = sdesc_sw128(kb + kk * 2048, 8192, 1024);
-      mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
-      mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
-      if (isS) {
-        const uint64_t av = sdesc_sw128(kb + 16384 + kk * 2048, 8192, 1024);
-        mma_f16(tmem + TM_U, av, sdesc_sw128(wb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
-        mma_f16(tmem + TM_U, av, sdesc_sw128(wb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ak = sdesc_sw128(kb + kk * 2048, 8192, 1024);
+          mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
+          mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
+          if (isS) {
+            const uint64_t av = sdesc_sw128(kb + 16384 + kk * 2048, 8192, 1024);
+            mma_f16(tmem + TM_P, av, sdesc_sw128(wb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
+            mma_f16(tmem + TM_P, av, sdesc_sw128(wb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
+          }
+        }
+        mma_commit(&bar_w);
+      };
+      bool ok = true;
+      if (nchunks > 0) {
+        issue_tma(0);
+        if (nchunks > 1) issue_tma(1);
+        ok = mbar_wait_cycles(&bar_tma[0], 0, a.err);
+        if (ok) {
+          tc_fence_after();
+          issue_wu(0);
+        }
       }
-    }
-    mma_commit(&bar_w);
-  };
-
-  if (tid == 0 && nchunks > 0) {
-    issue_tma(0);
-    if (nchunks > 1) issue_tma(1);
-    if (!mbar_wait_cycles(&bar_tma[0], 0, a.err)) abort_flag = 1;
-    else {
-      tc_fence_after();
-      issue_wu(0);
-    }
-  }
-
-  // X^T starts at [I | 0]^T restricted to this half: I (T half) or 0 (S half).
-  for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
-    float v[16];
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c & 1;
+        const uint32_t kbase = sb + OFF_KV + st * 32768;
+        const uint32_t wsb = sb + OFF_WS + st * WS_STAGE;
+        const uint32_t par = (uint32_t)c & 1u;
+        // P^T (onto -U^T for the S half): M = 128 (n), N = 64 (t), K = 128 (i).
+        if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
+        tc_fence_after();
 #pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == row) ? 1.f : 0.f;
-    tmem_st16(tmem + lane_base + TM_X + c0, v);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t wh = sdesc_sw128(wsb + kk * 2048, 16384, 1024);
+          const uint64_t wl = sdesc_sw128(wsb + 16384 + kk * 2048, 16384, 1024);
+          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wh, id_p, (isS || kk > 0) ? 1u : 0u);
+          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wl, id_p, 1);
+          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + 64 + kk * 8, wh, id_p, 1);
+        }
+        mma_commit(&bar_p);
+        // X^T += R^T K: M = 128 (n), N = 128 (i), K = 64 (t).
+        if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bk = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
+          mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + kk * 8, bk, id_x, 1);
+          mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + 32 + kk * 8, bk, id_x, 1);
+        }
+        mma_commit(&bar_x);
+        if (c + 1 < nchunks) {
+          if (!(ok = mbar_wait_cycles(&bar_tma[(c + 1) & 1], ((uint32_t)(c + 1) >> 1) & 1u, a.err))) break;
+          tc_fence_after();
+          issue_wu(c + 1);
+        }
+        if (c + 2 < nchunks) {
+          // The stage of chunk c is consumed once its update has run: refill it with chunk c + 2.
+          if (!(ok = mbar_wait_cycles(&bar_x, par, a.err))) break;
+          issue_tma(c + 2);
+        }
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------------- conversion warps
+    // X^T starts at [I | 0]^T restricted to this half: I (T half) or 0 (S half).
+    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == row) ? 1.f : 0.f;
+      tmem_st16(tmem + lane_base + TM_X + c0, v);
+    }
+    tmem_st_wait();
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c & 1;
+      uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+      const uint32_t par = (uint32_t)c & 1u;
+      if (c > 0 && !(ok = mbar_wait_cycles(&bar_x, par ^ 1u, a.err))) break;  // the previous update is done
+      if (!(ok = mbar_wait_cycles(&bar_tma[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
+      tc_fence_after();
+      const float *sR = reinterpret_cast<const float *>(wsd + WS_SC);
+      const float gamma_C = sR[C];
+      // (1) X^T -> bf16 hi/lo pieces (this thread's 64 rows i), and gamma_C X^T back.
+      {
+        float xv[64];
+        tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float ph[8], pl[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t hi, lo;
+            split2_pair(xv[c0 + 2 * q], xv[c0 + 2 * q + 1], hi, lo);
+            ph[q] = __uint_as_float(hi);
+            pl[q] = __uint_as_float(lo);
+          }
+          const uint32_t col = (uint32_t)(64 * part + c0) / 2;
+          tmem_st8(tmem + lane_base + TM_XP + col, ph);
+          tmem_st8(tmem + lane_base + TM_XP + 64 + col, pl);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float sv[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) sv[q] = xv[c0 + q] * gamma_C;
+          tmem_st16(tmem + lane_base + TM_X + 64 * part + c0, sv);
+        }
+      }
+      // (2) Wk^T -> MN-major B tile [i][t] hi/lo over the consumed A tiles of the stage
+      // (this thread: t in [32 part, 32 part + 32)).
+      if (!(ok = mbar_wait_cycles(&bar_w, par, a.err))) break;
+      tc_fence_after();
+      {
+        float wv[32];
+        tmem_ld32(tmem + lane_base + TM_W + 32 * part, wv);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2_pair(wv[8 * q4 + 2 * e], wv[8 * q4 + 2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(4 * part + q4));
+          *reinterpret_cast<uint4 *>(wsd + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(wsd + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&bar_r1);
+      // (3) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in TMEM.
+      if (!(ok = mbar_wait_cycles(&bar_p, par, a.err))) break;
+      tc_fence_after();
+      {
+        float pv[32];
+        tmem_ld32(tmem + lane_base + TM_P + 32 * part, pv);
+        float ph[16], pl[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int t = 32 * part + 2 * q;
+          uint32_t hi, lo;
+          split2_pair(-pv[2 * q] * sR[t], -pv[2 * q + 1] * sR[t + 1], hi, lo);
+          ph[q] = __uint_as_float(hi);
+          pl[q] = __uint_as_float(lo);
+        }
+        tmem_st16(tmem + lane_base + TM_RP + 16 * part, ph);
+        tmem_st16(tmem + lane_base + TM_RP + 32 + 16 * part, pl);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_r2);
+    }
+    if (ok && nchunks > 0) ok = mbar_wait_cycles(&bar_x, (uint32_t)(nchunks - 1) & 1u, a.err);
+    if (!ok) abort_flag = 1;
   }
-  tmem_st_wait();
-  tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
-  const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces (TMEM), B = Wk^T (MN-major)
-  const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces (TMEM), B = K (MN-major)
-  uint32_t ph_x = 0, ph_w = 0;
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int st = c & 1;
-    uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
-    const uint32_t kbase = sb + OFF_KV + st * 32768;
-    const uint32_t wsb = sb + OFF_WS + st * WS_STAGE;
-    if (abort_flag) break;
-    const float *sR = reinterpret_cast<const float *>(wsd + WS_SC);
-    const float gamma_C = sR[C];
-
-    // (1) X^T -> bf16 hi/lo pieces in TMEM (lane n, this thread's 64 rows i), and gamma_C X^T
-    // back into the accumulator.
-    {
-      float xv[64];
-      tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        float ph[8], pl[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const __nv_bfloat162 hp = __floats2bfloat162_rn(xv[c0 + 2 * q], xv[c0 + 2 * q + 1]);
-          const float2 hf = __bfloat1622float2(hp);
-          const __nv_bfloat162 lp = __floats2bfloat162_rn(xv[c0 + 2 * q] - hf.x, xv[c0 + 2 * q + 1] - hf.y);
-          ph[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
-          pl[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
-        }
-        const uint32_t col = (uint32_t)(64 * part + c0) / 2;
-        tmem_st8(tmem + lane_base + TM_XP + col, ph);
-        tmem_st8(tmem + lane_base + TM_XP + 64 + col, pl);
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        float sv[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) sv[q] = xv[c0 + q] * gamma_C;
-        tmem_st16(tmem + lane_base + TM_X + 64 * part + c0, sv);
-      }
-      tmem_st_wait();
+  if (abort_flag && tid == 0) {
+    // Let any copy or MMA still in flight land before the tensor memory is released.
+    for (int k = 0; k < 2; ++k) {
+      mbar_wait_cycles(&bar_x, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_w, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_p, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_tma[0], (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_tma[1], (uint32_t)k, nullptr, 100000000LL);
     }
-    // (2) Wk^T of this chunk (issued one chunk ahead) -> MN-major B tile [i][t] hi/lo over the
-    // consumed A tiles of the stage; this thread converts t in [32 part, 32 part + 32).
-    if (tid == 0 && !mbar_wait_cycles(&bar_w, ph_w, a.err)) abort_flag = 1;
-    ph_w ^= 1u;
-    __syncthreads();
-    tc_fence_after();
-    if (abort_flag) break;
-    {
-      float wv[32];
-      tmem_ld32(tmem + lane_base + TM_W + 32 * part, wv);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 hi, lo;
-        split8(wv + 8 * q4, hi, lo);
-        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(4 * part + q4));
-        *reinterpret_cast<uint4 *>(wsd + off) = hi;
-        *reinterpret_cast<uint4 *>(wsd + 16384 + off) = lo;
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // (3) P^T = X^T Wk^T: M = 128 (n), N = 64 (t), K = 128 (i); hi.hi + hi.lo + lo.hi.
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t wh = sdesc_sw128(wsb + kk * 2048, 16384, 1024);
-        const uint64_t wl = sdesc_sw128(wsb + 16384 + kk * 2048, 16384, 1024);
-        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wh, id_p, kk > 0);
-        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wl, id_p, 1);
-        mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + 64 + kk * 8, wh, id_p, 1);
-      }
-      mma_commit(&bar_x);
-      if (!mbar_wait_cycles(&bar_x, ph_x, a.err)) abort_flag = 1;
-    }
-    ph_x ^= 1u;
-    __syncthreads();
-    tc_fence_after();
-    if (abort_flag) break;
-
-    // (4) R^T[n][t] = (U^T - P^T)[n][t] exp(G_C - G_t) -> bf16 hi/lo pieces in TMEM (lane n);
-    // this thread handles t in [32 part, 32 part + 32).
-    {
-      float pv[32], uv[32];
-      tmem_ld32(tmem + lane_base + TM_P + 32 * part, pv);
-      if (isS) tmem_ld32(tmem + lane_base + TM_U + 32 * part, uv);
-      float ph[16], pl[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int t = 32 * part + 2 * q;
-        const float r0 = ((isS ? uv[2 * q] : 0.f) - pv[2 * q]) * sR[t];
-        const float r1 = ((isS ? uv[2 * q + 1] : 0.f) - pv[2 * q + 1]) * sR[t + 1];
-        const __nv_bfloat162 hp = __floats2bfloat162_rn(r0, r1);
-        const float2 hf = __bfloat1622float2(hp);
-        const __nv_bfloat162 lp = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
-        ph[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
-        pl[q] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
-      }
-      tmem_st16(tmem + lane_base + TM_RP + 16 * part, ph);
-      tmem_st16(tmem + lane_base + TM_RP + 32 + 16 * part, pl);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // (5) X^T += R^T K: M = 128 (n), N = 128 (i), K = 64 (t); then the next chunk's Wk^T, U^T.
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bk = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
-        mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + kk * 8, bk, id_x, 1);
-        mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + 32 + kk * 8, bk, id_x, 1);
-      }
-      mma_commit(&bar_x);
-      if (c + 1 < nchunks) {
-        if (!mbar_wait_cycles(&bar_tma[(c + 1) & 1], ((c + 1) >> 1) & 1, a.err)) abort_flag = 1;
-        else issue_wu(c + 1);
-      }
-      if (!mbar_wait_cycles(&bar_x, ph_x, a.err)) abort_flag = 1;
-      // This stage (K, V, records and the Wk tile) is consumed: prefetch chunk c + 2 into it.
-      if (!abort_flag && c + 2 < nchunks) issue_tma(c + 2);
-    }
-    ph_x ^= 1u;
-    __syncthreads();
-    tc_fence_after();
   }
-
-  if (!abort_flag) {
+  if (!abort_flag && !issuer) {
     // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
     float *out = (isS ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
     float xv[64];
     tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
 #pragma unroll
     for (int q = 0; q < 64; ++q) out[(size_t)(64 * part + q) * D + row] = xv[q];
-  } else if (tid == 0) {
-    // Let any copy or MMA still in flight land before the memory is released.
-    mbar_wait_cycles(&bar_x, ph_x, nullptr, 200000000LL);
-    mbar_wait_cycles(&bar_w, ph_w, nullptr, 200000000LL);
-    mbar_wait_cycles(&bar_tma[0], 0, nullptr, 200000000LL);
-    mbar_wait_cycles(&bar_tma[1], 0, nullptr, 200000000LL);
   }
   tc_fence_before();
   __syncthreads();

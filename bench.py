@@ -227,6 +227,89 @@ def cpu_baseline(w, n_heads, threads):
     return tokens_equiv / dt, dt
 
 
+def decay_build_measure(steps, warmup, dev, peaks):
+    """Decay-family builds (64 segments x 512 tokens, 32 heads, bf16) and the 64-step compose of each.
+
+    Roofline of the scalar and diagonal builds: HBM, algorithmic bytes per head-token = k and v
+    (bf16, 2 x 256 B) + the gates (4 B per head-token scalar, 512 B diagonal).  The gated-delta
+    build is reported against the bf16 tensor peak with the chunked count.
+    """
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import workloads as W
+    out = {}
+    for fam, w in W.DECAY_FAMILIES.items():
+        tok = w.draw_request(dev, need_q=False)
+        bounds = torch.tensor(w.body_bounds(), device=dev)
+        ws_bytes = hy.build_workspace_bytes(w.H, w.d, w.n_seg, w.seg_len, family=fam, in_dtype=w.in_dtype)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+        T = torch.empty((w.n_seg, w.H, hy.t_size(fam, w.d)), device=dev)
+        S = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
+        idx = torch.arange(w.n_seg, dtype=torch.int32, device=dev)[None]
+        S_out = torch.empty((1, w.H, w.d, w.d), device=dev)
+
+        def fn(ev):
+            if ev is not None:
+                ev[0].record()
+            hy.segment_build_batched(tok["k"], tok["v"], bounds, tok["alpha"], tok["beta"], family=fam,
+                                     max_len=w.seg_len, out=(T, S), ws=ws)
+            if ev is not None:
+                ev[1].record()
+            hy.compose(T, S, idx, family=fam, out=S_out)
+            if ev is not None:
+                ev[2].record()
+
+        _, kb, kc = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+        tb, tc = sum(kb) / len(kb) / 1e3, sum(kc) / len(kc) / 1e3
+        ht = w.n_seg * w.seg_len * w.H
+        entry = {"build_head_tokens_per_s": ht / tb, "build_ms": tb * 1e3,
+                 "compose_ms": tc * 1e3, "compositions_per_s": w.n_seg * w.H / tc}
+        if fam == "gated_delta":
+            fl = FLOP_PER_HEAD_TOKEN_WY * ht
+            entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"]}
+        else:
+            per = 2 * w.d * 2 + (4 if fam != "diag" else 4 * w.d)
+            by = per * ht + w.n_seg * w.H * w.d * w.d * 4
+            entry["roofline"] = {"bound": "hbm", "achieved": by / tb / 1e9, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": by / tb / 1e9 / peaks["hbm_gbs"],
+                                 "bytes_per_head_token": per}
+        entry["status"] = hy.stream_status()
+        out[fam] = entry
+        del tok, T, S, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def scan_measure(steps, warmup, dev, peaks):
+    """Affine scan of 64 pairs per head over 960 heads (d = 128, fp32): prefix pairs/s."""
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import workloads as W
+    n, H, d = 64, 960, 128
+    T, S = W.random_pairs(n, H, d, dev, key=11)
+
+    def fn(ev):
+        if ev is not None:
+            ev[0].record()
+        hy.affine_scan(T, S, family="gated_delta")
+        if ev is not None:
+            ev[1].record()
+            ev[2].record()
+
+    total, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+    t = sum(k1) / len(k1) / 1e3
+    by = n * H * (2 * d * d * 4) * 2  # read T and S, write both prefixes
+    res = {"workload": f"scan_{n}x{H}heads_d{d}_fp32", "prefix_pairs_per_s": n * H / t, "ms": t * 1e3,
+           "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": by / t / 1e9 / peaks["hbm_gbs"]}, "status": hy.stream_status()}
+    del T, S
+    torch.cuda.empty_cache()
+    return res
+
+
 def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False):
     """Warm-cache composition: 30 layers x 32 heads, pool of 256 fp32 pairs, 64 requests x 16 segments."""
     import dataclasses
@@ -382,6 +465,10 @@ def main():
     e2e_ms, _, _ = run_timed(e2e_step, args.steps, min(args.warmup, 3), sync_all, kernel_events=False)
     e2e_value = req.tokens * world / (e2e_ms / 1e3 / args.steps)
 
+    decay = scan = None
+    if not args.no_compose:
+        decay = decay_build_measure(args.steps, args.warmup, dev, peaks)
+        scan = scan_measure(args.steps, args.warmup, dev, peaks)
     compose = None
     if not args.no_compose:
         del host
@@ -412,6 +499,8 @@ def main():
                          "seam_head_tokens_per_s": req.seam_head_tokens / avg_asm_s, "ms": avg_asm_s * 1e3},
             "roofline": roof,
             "compose_pool": compose,
+            "decay_builds": decay,
+            "affine_scan": scan,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": req.launches_per_step * args.steps,

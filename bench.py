@@ -231,7 +231,8 @@ def decay_build_measure(steps, warmup, dev, peaks):
     """Decay-family builds (64 segments x 512 tokens, 32 heads, bf16) and the 64-step compose of each.
 
     Roofline of the scalar and diagonal builds: HBM, algorithmic bytes per head-token = k and v
-    (bf16, 2 x 256 B) + the gates (4 B per head-token scalar, 512 B diagonal).  The gated-delta
+    (bf16, 2 x 256 B) + the gates (none for a constant gate, 4 B scalar, 512 B diagonal), plus
+    the pairs written.  The gated-delta
     build is reported against the bf16 tensor peak with the chunked count.
     """
     import torch
@@ -270,7 +271,7 @@ def decay_build_measure(steps, warmup, dev, peaks):
             entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"]}
         else:
-            per = 2 * w.d * 2 + (4 if fam != "diag" else 4 * w.d)
+            per = 2 * w.d * 2 + {"scalar_const": 0, "scalar": 4, "diag": 4 * w.d}[fam]
             by = per * ht + w.n_seg * w.H * w.d * w.d * 4
             entry["roofline"] = {"bound": "hbm", "achieved": by / tb / 1e9, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": by / tb / 1e9 / peaks["hbm_gbs"],

@@ -82,6 +82,8 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
   }
   const bool tc = tokens && build_tc_supported(sh->d_k, sh->family, sh->in_dtype, o_out != nullptr) &&
                   !force_recurrent();
+  const bool dtc = tokens && build_decay_tc_supported(sh->d_k, sh->family, sh->in_dtype, o_out != nullptr) &&
+                   !force_recurrent();
   if (tc && (ws_bytes < build_tc_min_workspace(n_seg, seg.max_len) || !ok_ptr(ws))) return HYPIC_ENOSPACE;
   int *err = nullptr;
   cudaError_t e = status_word(&err);
@@ -99,6 +101,7 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
   a.o_out = o_out;
   a.err = err;
   if (tc) return from_cuda(launch_build_tc(a, ws, ws_bytes, st));
+  if (dtc) return from_cuda(launch_build_decay_tc(a, st));
   return from_cuda(launch_recurrent(a, st));
 }
 

@@ -67,6 +67,24 @@ __device__ __forceinline__ bool mbar_wait_cycles(uint64_t *bar, uint32_t phase, 
   return true;
 }
 
+// Named barriers for a subset of the block (whole warps; `n` threads, a multiple of 32).
+__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Same, returning the OR of `v` over the participating threads (one decision for all).
+__device__ __forceinline__ bool bar_or_named(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // ---- TMA -----------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
   asm volatile(

@@ -55,4 +55,20 @@ inline bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map without swizzle: box = box_cols x box_rows, box_cols <= 256 (rows of
+// box_cols * 4 bytes land back to back in shared memory).  Out-of-range elements read as zero.
+inline bool make_tmap_f32_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                               uint32_t box_cols, uint32_t box_rows) {
+  auto fn = tma_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace hypic

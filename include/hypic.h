@@ -120,9 +120,9 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
 /*
  * Workspace bytes the build prefers for n_seg bodies of at most max_len tokens
  * (0 when the shape runs without one).  The d = 128 bf16 delta-family build
- * keeps one 33,280-byte operand record per (64-token chunk, head) in it; it
+ * keeps one 49,664-byte operand record per (64-token chunk, head) in it; it
  * processes the heads in blocks that fit the workspace it is given, so any size
- * that holds one head's records (n_seg * ceil(max_len / 64) * 33,280 bytes)
+ * that holds one head's records (n_seg * ceil(max_len / 64) * 49,664 bytes)
  * works, and less gives HYPIC_ENOSPACE.  The preferred size covers all heads up
  * to about 1 GiB.  The workspace is caller-owned device memory, 16-byte aligned,
  * and must not be used by anything else until the stream reaches the end of the call.
@@ -141,8 +141,8 @@ size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int6
  * scratch array of HYPIC_NOALLOC_SCRATCH_BYTES that lives in the library, so
  * every GPU that loads the library holds that memory until the process exits.
  * Limit: one head's operand records must fit the scratch, i.e.
- * n_seg * ceil(max_len / 64) * 33,280 <= HYPIC_NOALLOC_SCRATCH_BYTES
- * (n_seg * ceil(max_len / 64) <= 2016); larger requests return HYPIC_ENOSPACE
+ * n_seg * ceil(max_len / 64) * 49,664 <= HYPIC_NOALLOC_SCRATCH_BYTES
+ * (n_seg * ceil(max_len / 64) <= 1351); larger requests return HYPIC_ENOSPACE
  * before anything is enqueued.  More heads are processed in blocks that fit.
  * The first call on a device looks up the scratch array's device address
  * (once per device, with that device current); make that first call before

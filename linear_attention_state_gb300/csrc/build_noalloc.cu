@@ -16,7 +16,7 @@ namespace hypic {
 namespace {
 
 constexpr size_t kScratchBytes = HYPIC_NOALLOC_SCRATCH_BYTES;  // per device
-constexpr size_t kRecordBytes = 33280;  // operand record of one (64-token chunk, head)
+constexpr size_t kRecordBytes = 49664;  // operand record of one (64-token chunk, head)
 
 static __device__ __align__(256) unsigned char g_build_scratch[kScratchBytes];
 

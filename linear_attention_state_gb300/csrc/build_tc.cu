@@ -18,18 +18,19 @@
 //   wy_prep_kernel  (one CTA per chunk and head, all chunks in parallel): the
 //     state-independent part.  TMA loads K; gates and their log-cumsum; Gram =
 //     K K^T on tcgen05 (M = 64); L; A = (I + L)^{-1} in fp32 by 2 x 2 blocked
-//     forward substitution; A diag(b gamma) and -A diag(b) split into bf16 hi + lo
-//     and stored to the workspace as ready-made 128-byte-swizzled operand tiles,
-//     with the per-token scales exp(G_C - G_t) and gamma_C.
-//   chain_tc_kernel (one 256-thread CTA per segment, head and column half of X): the state-
-//     dependent chain.  Each CTA keeps its 128 x 128 fp32 half of X in tensor
-//     memory for the whole segment (the T half has no writes, the S half does;
-//     they evolve independently).  Per chunk: TMA brings K, V and the chunk's
-//     workspace tiles (double buffered); tcgen05 forms Wk^T = K^T (A diag(b g))^T
-//     and U^T = V^T (A diag(b))^T (hi + lo); X is split hi + lo into shared memory
-//     and gamma_C X written back as the accumulator; P^T = X^T Wk^T (hi.hi +
-//     hi.lo + lo.hi); R^T = (U^T - P^T) diag(exp(G_C - G_t)) split hi + lo;
-//     X += K^T R.
+//     forward substitution; Wk^T = K^T (A diag(b gamma))^T on tcgen05 (K exact in
+//     bf16, A diag(b gamma) split hi + lo).  Stored to the workspace as ready-made
+//     128-byte-swizzled operand tiles: Wk^T hi + lo, -A diag(b) hi + lo, and the
+//     per-token scales exp(G_C - G_t) and gamma_C.
+//   chain_tc_kernel (one CTA per segment and head): the state-dependent chain.  The
+//     CTA keeps both 128 x 128 fp32 column halves of X (T and S, which evolve
+//     independently) in tensor memory for the whole segment, transposed.  Per chunk:
+//     TMA brings K, V and the chunk's record (double buffered); -U^T = V^T (-A diag(b))^T
+//     goes into the S half's P accumulator; each half splits X^T into bf16 hi (tensor
+//     memory) + lo (shared memory) and writes gamma_C X^T back; P^T = X^T Wk^T
+//     (hi.hi + hi.lo + lo.hi); R^T = (U^T - P^T) diag(exp(G_C - G_t)) split hi + lo in
+//     place; X^T += R^T K.  The two halves run a half-step apart, so one half's
+//     conversions overlap the other half's MMAs.
 // Operands are fp32-accurate to about 2^-16 relative (bf16 hi + lo; K and V are
 // exact in bf16) and every product accumulates in fp32 in TMEM.  Padded tokens of
 // a ragged last chunk get b = 0 and a = 1, which makes them exact identity steps.
@@ -47,9 +48,13 @@ constexpr int C = 64;    // tokens per chunk
 constexpr int D = 128;   // d_k = d_v
 constexpr int NT = 128;  // threads per CTA
 
-// Workspace record of one (chunk, head): four 8 KB K-major [64 t][64 s] tiles and the scales.
-constexpr uint32_t WS_ABH = 0, WS_ABL = 8192, WS_AVH = 16384, WS_AVL = 24576, WS_SC = 32768;
-constexpr uint32_t WS_REC = 33280;  // bytes per (chunk, head)
+// Workspace record of one (chunk, head): Wk^T hi and lo as MN-major [128 i][64 t] tiles
+// (16 KB each), -A diag(b) hi and lo as K-major [64 t][64 s] tiles (8 KB each), then the
+// 65 scales (exp(G_C - G_t) for t < 64, gamma_C), padded.
+constexpr uint32_t WS_WH = 0, WS_WL = 16384, WS_AVH = 32768, WS_AVL = 40960, WS_SC = 49152;
+constexpr uint32_t WS_TILES = 49152;  // the four tiles, contiguous
+constexpr uint32_t WS_SC_BYTES = 272;  // 65 floats rounded up to 16 bytes
+constexpr uint32_t WS_REC = 49664;  // bytes per (chunk, head)
 constexpr size_t WS_CAP = (size_t)1 << 30;  // preferred workspace size bound
 
 struct BuildTcArgs {
@@ -81,15 +86,6 @@ __device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, i
   return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * WS_REC;
 }
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
-      : "memory");
-}
-
 // hi = bf16(v), lo = bf16(v - hi) for 8 values, packed for one 16-byte store each.
 __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
   uint32_t h[4], l[4];
@@ -108,12 +104,14 @@ __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
 // ------------------------------------------------------------------------------------------------
 // Kernel 1: per (segment, chunk, head) -- gates, Gram, L, A = (I + L)^{-1}, operand tiles.
 constexpr int LS = 68;                             // row stride of L (floats): conflict-light, 16-byte rows
-constexpr uint32_t P_OFF_K = 0;                    // 16 KB K chunk, two [64 t][64 i] boxes; later A
-constexpr uint32_t P_OFF_A = 0;                    // fp32 [64][64], over the consumed K chunk
-constexpr uint32_t P_OFF_L = 16384;                // fp32 [64][LS]; T = L21 A11 lives in its unused upper-right block
+constexpr uint32_t P_OFF_K = 0;       // 16 KB K chunk, two [64 t][64 i] boxes
+constexpr uint32_t P_OFF_L = 16384;   // fp32 [64][LS]: L, then A in place (lower triangle); T = L21 A11
+                                      // in its upper-right block; later the A diag(b gamma) hi, lo tiles
+constexpr uint32_t P_OFF_AB = P_OFF_L;  // K-major [64 t][64 s] bf16 tiles, 8 KB each
+constexpr uint32_t P_OFF_WT = 0;      // Wk^T hi, lo staged for the store, over K and L once both are consumed
 constexpr uint32_t P_SMEM = P_OFF_L + 64 * LS * 4 + 1024;  // + alignment slack
 
-__global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, BuildTcArgs a) {
+__global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
@@ -121,7 +119,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
   __shared__ int ok_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *sL = reinterpret_cast<float *>(sm + P_OFF_L);
-  float *sA = reinterpret_cast<float *>(sm + P_OFF_A);
+  float *sA = sL;  // A = (I + L)^{-1} replaces L in place, row stride LS
   float *sT = sL + 32;  // [32][32] with row stride LS: rows 0..31, columns 32..63 of L (never read as L)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int hh = blockIdx.x % a.Hb;
@@ -200,35 +198,45 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
     const float Gt = lane < 16 ? sG[t] : 0.f;
     const float bt = lane < 16 ? sBv[t] : 0.f;
     const float be = lane < 16 ? bt * sE[t] : 0.f;
-    float v[64];
-    tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16), v);
-    if (lane < 16) {
-      if (separable) {
+#pragma unroll 1
+    for (int hb = 0; hb < C; hb += 32) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + hb, v);
+      if (lane < 16) {
+        if (separable) {
 #pragma unroll
-        for (int sc = 0; sc < C; sc += 4) {
-          const float4 f4 = *reinterpret_cast<const float4 *>(sF + sc);
-          float4 o;
-          o.x = (sc + 0 < t) ? be * f4.x * v[sc + 0] : 0.f;
-          o.y = (sc + 1 < t) ? be * f4.y * v[sc + 1] : 0.f;
-          o.z = (sc + 2 < t) ? be * f4.z * v[sc + 2] : 0.f;
-          o.w = (sc + 3 < t) ? be * f4.w * v[sc + 3] : 0.f;
-          *reinterpret_cast<float4 *>(sL + t * LS + sc) = o;
+          for (int q = 0; q < 32; q += 4) {
+            const int sc = hb + q;
+            const float4 f4 = *reinterpret_cast<const float4 *>(sF + sc);
+            float4 o;
+            o.x = (sc + 0 < t) ? be * f4.x * v[q + 0] : 0.f;
+            o.y = (sc + 1 < t) ? be * f4.y * v[q + 1] : 0.f;
+            o.z = (sc + 2 < t) ? be * f4.z * v[q + 2] : 0.f;
+            o.w = (sc + 3 < t) ? be * f4.w * v[q + 3] : 0.f;
+            *reinterpret_cast<float4 *>(sL + t * LS + sc) = o;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int sc = hb + q;
+            sL[t * LS + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[q] : 0.f;
+          }
         }
-      } else {
-#pragma unroll
-        for (int sc = 0; sc < C; ++sc) sL[t * LS + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[sc] : 0.f;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
-  if (!ok_flag) return;
+  if (!ok_flag) {
+    if (warp == 0) tmem_dealloc(tmem, 64);
+    return;
+  }
 
-  // Diagonal 32 x 32 blocks of A by column-wise forward substitution (threads 0..63).
+  // Diagonal 32 x 32 blocks of A by column-wise forward substitution (threads 0..63), written
+  // over the blocks of L they came from once every thread has read them.
+  float x[32];
+  const int base = (tid >> 5) * 32, cl = tid & 31;
   if (tid < C) {
-    const int base = (tid >> 5) * 32, cl = tid & 31;
-    float x[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r) x[r] = (r == cl) ? 1.f : 0.f;
 #pragma unroll
@@ -247,12 +255,11 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
       for (int q = (r / 4) * 4; q < r; ++q) a0 = fmaf(Lr[q], x[q], a0);
       if (r > cl) x[r] = -((a0 + a1) + (a2 + a3));
     }
+  }
+  __syncthreads();
+  if (tid < C) {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) sA[(base + r) * C + base + cl] = x[r];
-    if (base == 0) {
-#pragma unroll
-      for (int r = 0; r < 32; ++r) sA[r * C + 32 + cl] = 0.f;
-    }
+    for (int r = 0; r < 32; ++r) sA[(base + r) * LS + base + cl] = x[r];
   }
   __syncthreads();
   // T = L21 A11 and A21 = -A22 T (32 x 32 each): each thread owns a 2 x 4 output tile
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
 #pragma unroll 8
     for (int k = 0; k < 32; ++k) {
       const float a0 = sL[(32 + r0) * LS + k], a1 = sL[(33 + r0) * LS + k];
-      const float4 b4 = *reinterpret_cast<const float4 *>(sA + k * C + c0);
+      const float4 b4 = *reinterpret_cast<const float4 *>(sA + k * LS + c0);
       acc[0][0] = fmaf(a0, b4.x, acc[0][0]);
       acc[0][1] = fmaf(a0, b4.y, acc[0][1]);
       acc[0][2] = fmaf(a0, b4.z, acc[0][2]);
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
     float bcc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 8
     for (int k = 0; k < 32; ++k) {
-      const float a0 = sA[(32 + r0) * C + 32 + k], a1 = sA[(33 + r0) * C + 32 + k];
+      const float a0 = sA[(32 + r0) * LS + 32 + k], a1 = sA[(33 + r0) * LS + 32 + k];
       const float4 b4 = *reinterpret_cast<const float4 *>(sT + k * LS + c0);
       bcc[0][0] = fmaf(a0, b4.x, bcc[0][0]);
       bcc[0][1] = fmaf(a0, b4.y, bcc[0][1]);
@@ -290,65 +297,121 @@ __global__ void __launch_bounds__(NT) wy_prep_kernel(const __grid_constant__ CUt
       bcc[1][2] = fmaf(a1, b4.z, bcc[1][2]);
       bcc[1][3] = fmaf(a1, b4.w, bcc[1][3]);
     }
-    *reinterpret_cast<float4 *>(sA + (32 + r0) * C + c0) = make_float4(-bcc[0][0], -bcc[0][1], -bcc[0][2], -bcc[0][3]);
-    *reinterpret_cast<float4 *>(sA + (33 + r0) * C + c0) = make_float4(-bcc[1][0], -bcc[1][1], -bcc[1][2], -bcc[1][3]);
+    *reinterpret_cast<float4 *>(sA + (32 + r0) * LS + c0) = make_float4(-bcc[0][0], -bcc[0][1], -bcc[0][2], -bcc[0][3]);
+    *reinterpret_cast<float4 *>(sA + (33 + r0) * LS + c0) = make_float4(-bcc[1][0], -bcc[1][1], -bcc[1][2], -bcc[1][3]);
   }
   __syncthreads();
 
-  // Operand tiles: A diag(b gamma) and A diag(b), split hi + lo, 128-byte-swizzled K-major.
+  // Operand tiles, split hi + lo, 128-byte-swizzled K-major [64 t][64 s]: -A diag(b) straight to
+  // the workspace record; A diag(b gamma) into shared memory (over A, once all of A is read) for
+  // the Wk^T product.  Entries above the diagonal of A are zero (the upper-right block holds T).
   uint8_t *rec = ws_rec(a, s, c, hh);
-  for (int e = tid; e < C * 8; e += NT) {
+  uint4 abh[4], abl[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + j * NT;
     const int t = e >> 3, q = e & 7;
     float vb[8], vv[8];
-    const float4 a0 = *reinterpret_cast<const float4 *>(sA + t * C + 8 * q);
-    const float4 a1 = *reinterpret_cast<const float4 *>(sA + t * C + 8 * q + 4);
+    const float4 a0 = *reinterpret_cast<const float4 *>(sA + t * LS + 8 * q);
+    const float4 a1 = *reinterpret_cast<const float4 *>(sA + t * LS + 8 * q + 4);
     const float av8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      vb[j] = av8[j] * sBG[8 * q + j];
-      vv[j] = -av8[j] * sBv[8 * q + j];  // negated: the chain accumulates -U under P
+    for (int i = 0; i < 8; ++i) {
+      const float av = (8 * q + i <= t) ? av8[i] : 0.f;
+      vb[i] = av * sBG[8 * q + i];
+      vv[i] = -av * sBv[8 * q + i];  // negated: the chain accumulates -U under P
     }
     uint4 hi, lo;
     const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)q);
-    split8(vb, hi, lo);
-    *reinterpret_cast<uint4 *>(rec + WS_ABH + off) = hi;
-    *reinterpret_cast<uint4 *>(rec + WS_ABL + off) = lo;
+    split8(vb, abh[j], abl[j]);
     split8(vv, hi, lo);
     *reinterpret_cast<uint4 *>(rec + WS_AVH + off) = hi;
     *reinterpret_cast<uint4 *>(rec + WS_AVL + off) = lo;
   }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + j * NT;
+    const uint32_t off = sw128_offset((uint32_t)(e >> 3), (uint32_t)(e & 7));
+    *reinterpret_cast<uint4 *>(sm + P_OFF_AB + off) = abh[j];
+    *reinterpret_cast<uint4 *>(sm + P_OFF_AB + 8192 + off) = abl[j];
+  }
   float *sc = reinterpret_cast<float *>(rec + WS_SC);
   if (tid < C) sc[tid] = exp2f(sG[C - 1] - sG[tid]);
   if (tid == 0) sc[C] = exp2f(sG[C - 1]);
+  fence_proxy_async();
+  __syncthreads();
+
+  // Wk^T = K^T (A diag(b gamma))^T: M = 128 (i), N = 64 (t), K = 64 (s), into the Gram's columns.
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t kb = smem_u32(sm + P_OFF_K), ab = smem_u32(sm + P_OFF_AB);
+    const uint32_t id = idesc_f32acc(1, 1, 1, 0, 128, 64);  // A = K^T (MN-major), B K-major
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ak = sdesc_sw128(kb + kk * 2048, 8192, 1024);
+      mma_f16(tmem, ak, sdesc_sw128(ab + kk * 32, 16, 1024), id, kk > 0);
+      mma_f16(tmem, ak, sdesc_sw128(ab + 8192 + kk * 32, 16, 1024), id, 1);
+    }
+    mma_commit(&bar_mma);
+    if (!mbar_wait_cycles(&bar_mma, 1, a.err)) ok_flag = 0;
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (ok_flag) {
+    // lane i = tid holds Wk^T row i: split into the MN-major [128 i][64 t] hi and lo tiles.
+#pragma unroll 1
+    for (int hb = 0; hb < C; hb += 32) {
+      float wv[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + hb, wv);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 hi, lo;
+        split8(wv + 8 * q, hi, lo);
+        const uint32_t off = sw128_offset((uint32_t)tid, (uint32_t)(hb / 8 + q));
+        *reinterpret_cast<uint4 *>(sm + P_OFF_WT + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + P_OFF_WT + 16384 + off) = lo;
+      }
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (ok_flag && tid == 0) {
+    bulk_store(rec + WS_WH, sm + P_OFF_WT, 32768);
+    bulk_store_commit();
+    bulk_store_wait_all();
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel 2: per (segment, head, column half) -- the chunk chain on tensor memory.
+// Kernel 2: per (segment, head) -- the chunk chain of both column halves on tensor memory.
 //
-// The state is kept transposed, X^T (lanes = the 128 columns n of this half, TMEM columns =
-// rows i), so that both state-dependent products take their A operand straight from tensor
-// memory and read only their B operand from shared memory:
-//   P^T - U^T = X^T Wk^T - U^T   A = bf16 hi/lo pieces of X^T (TMEM), B = Wk^T [i][t] (MN-major)
-//   X^T = gamma_C X^T + R^T K    A = bf16 hi/lo pieces of R^T (TMEM), B = K [t][i] (MN-major TMA tile)
-// Wk^T = K^T (A diag(b gamma))^T and -U^T = V^T (-A diag(b))^T depend on the chunk's inputs only;
-// -U^T is written into the P^T accumulator, which the P MMAs then add onto.  Warp 8 issues
-// every TMA copy and MMA; warps 0-7 (two threads per TMEM lane) do the conversions.  The two
-// sides hand over through mbarriers: MMA completions arrive through tcgen05.commit, the
-// conversion warps arrive after their TMEM and shared-memory writes are fenced.
-constexpr uint32_t OFF_KV = 0;                          // 2 stages x (K 16 KB + V 16 KB)
-constexpr uint32_t OFF_WS = 65536;                      // 2 stages x 33 KB workspace records
-constexpr uint32_t WS_STAGE = 33792;                    // record rounded up to 1024
-constexpr uint32_t SMEM_BYTES = OFF_WS + 2 * WS_STAGE + 1024;  // + alignment slack
+// Each half's state is kept transposed, X^T (lanes = the 128 columns n of the half, TMEM columns
+// = rows i), so that both state-dependent products take their A operand from tensor or shared
+// memory and read only their B operand from the chunk's tiles:
+//   P^T - U^T = X^T Wk^T - U^T   A = X^T hi (TMEM) / lo (shared), B = Wk^T [i][t] (MN-major)
+//   X^T = gamma_C X^T + R^T K    A = R^T hi/lo pieces (TMEM, in place over P^T), B = K [t][i]
+// -U^T = V^T (-A diag(b))^T is written into the S half's P accumulator first.  Warp 16 issues
+// every TMA copy and MMA; warps 0-7 convert for the T half and warps 8-15 for the S half (two
+// threads per TMEM lane each).  MMA completions reach the converters through tcgen05.commit;
+// the converters arrive after their TMEM and shared-memory writes are fenced.
+constexpr uint32_t STAGE_K = 0, STAGE_V = 16384, STAGE_REC = 32768;  // within a stage
+constexpr uint32_t STAGE_BYTES = STAGE_REC + WS_TILES;               // 81,920 (1024-aligned)
+constexpr uint32_t OFF_XLO = 2 * STAGE_BYTES;                        // X^T lo tiles, 32 KB per half
+constexpr uint32_t OFF_SC = OFF_XLO + 65536;                         // scales, 512 B per stage
+constexpr uint32_t SMEM_BYTES = OFF_SC + 1024 + 1024;                // + alignment slack
 
-constexpr uint32_t TM_X = 0;     // 128 cols: X^T accumulator, lanes n, columns i
-constexpr uint32_t TM_XP = 128;  // 2 x 64 cols: X^T hi, lo (bf16, two i per column)
-constexpr uint32_t TM_P = 256;   // 64 cols: P^T - U^T, lanes n, columns t
-constexpr uint32_t TM_RP = 320;  // 2 x 32 cols: R^T hi, lo (bf16, two t per column)
-constexpr uint32_t TM_W = 384;   // 64 cols: Wk^T, lanes i, columns t
+// Tensor memory (512 columns): per half h, X^T at 128 h, X^T hi pieces at 256 + 64 h, P^T (then
+// the R^T pieces) at 384 + 64 h.
+__device__ __forceinline__ uint32_t tm_x(int h) { return 128u * h; }
+__device__ __forceinline__ uint32_t tm_xp(int h) { return 256u + 64u * h; }
+__device__ __forceinline__ uint32_t tm_p(int h) { return 384u + 64u * h; }
 constexpr uint32_t TM_COLS = 512;
 
-constexpr int NCONV = 256;        // conversion threads: two per TMEM lane
-constexpr int NT2 = NCONV + 32;   // + the issuing warp
+constexpr int NCONV = 512;       // conversion threads: two per TMEM lane and half
+constexpr int NT2 = NCONV + 32;  // + the issuing warp
 
 // hi = truncation of x to bf16, lo = bf16 rounding of the exact remainder, for two values;
 // returns the packed hi pair and lo pair (first value in the low half).
@@ -364,36 +427,36 @@ __global__ void __launch_bounds__(NT2, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_tma[2], bar_w, bar_p, bar_x, bar_r1, bar_r2;
+  // per half: r1 (X pieces ready), r2 (R pieces ready), p (P^T done), x (update done)
+  __shared__ uint64_t bar_full[2], bar_r1[2], bar_r2[2], bar_p[2], bar_x[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const bool issuer = warp == NCONV / 32;
-  const int row = tid & 127;  // TMEM lane a conversion thread serves
+  const int row = tid & 127;        // TMEM lane a conversion thread serves
   const int part = (tid >> 7) & 1;  // which half of that lane's columns
-  const int half = blockIdx.x & 1;  // 0: T columns, 1: S columns
-  const int hh = (blockIdx.x >> 1) % a.Hb;
-  const int s = (blockIdx.x >> 1) / a.Hb;
+  const int half = (tid >> 8) & 1;  // 0: T columns, 1: S columns
+  const int hh = blockIdx.x % a.Hb;
+  const int s = blockIdx.x / a.Hb;
   const int h = a.h0 + hh;
-  const bool isS = half == 1;
 
   int64_t beg, end;
   if (!seg_bounds(a, s, beg, end)) {
-    if (tid == 0 && !isS) set_error(a.err, HYPIC_EDEVICE);
+    if (tid == 0) set_error(a.err, HYPIC_EDEVICE);
     return;
   }
   const int nchunks = (int)((end - beg + C - 1) / C);
 
   if (tid == 0) {
-    mbar_init(&bar_tma[0], 1);
-    mbar_init(&bar_tma[1], 1);
-    mbar_init(&bar_w, 1);
-    mbar_init(&bar_p, 1);
-    mbar_init(&bar_x, 1);
-    mbar_init(&bar_r1, NCONV);
-    mbar_init(&bar_r2, NCONV);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_r1[i], 256);
+      mbar_init(&bar_r2[i], 256);
+      mbar_init(&bar_p[i], 1);
+      mbar_init(&bar_x[i], 1);
+    }
     mbar_fence_init();
     abort_flag = 0;
   }
@@ -410,91 +473,72 @@ __global__ void __launch_bounds__(NT2, 1)
     // ----------------------------------------------------------------------------- issuing warp
     if (lane == 0) {
       prefetch_tmap(&mapK);
-      if (isS) prefetch_tmap(&mapV);
+      prefetch_tmap(&mapV);
       auto issue_tma = [&](int c) {
         const int st = c & 1;
         const int rowt = (int)(beg + (int64_t)c * C);
-        uint8_t *kv = sm + OFF_KV + st * 32768;
-        uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
+        uint8_t *stg = sm + st * STAGE_BYTES;
         const uint8_t *rec = ws_rec(a, s, c, hh);
-        mbar_arrive_expect_tx(&bar_tma[st], isS ? 32768u + WS_REC : 16384u + 16384u + 512u);
-        tma_load_2d(kv, &mapK, &bar_tma[st], h * D, rowt);
-        tma_load_2d(kv + 8192, &mapK, &bar_tma[st], h * D + 64, rowt);
-        if (isS) {
-          tma_load_2d(kv + 16384, &mapV, &bar_tma[st], h * D, rowt);
-          tma_load_2d(kv + 24576, &mapV, &bar_tma[st], h * D + 64, rowt);
-          bulk_load(wsd, rec, WS_REC, &bar_tma[st]);
-        } else {
-          bulk_load(wsd, rec, 16384, &bar_tma[st]);
-          bulk_load(wsd + WS_SC, rec + WS_SC, 512, &bar_tma[st]);
-        }
+        mbar_arrive_expect_tx(&bar_full[st], 32768u + WS_TILES + WS_SC_BYTES);
+        tma_load_2d(stg + STAGE_K, &mapK, &bar_full[st], h * D, rowt);
+        tma_load_2d(stg + STAGE_K + 8192, &mapK, &bar_full[st], h * D + 64, rowt);
+        tma_load_2d(stg + STAGE_V, &mapV, &bar_full[st], h * D, rowt);
+        tma_load_2d(stg + STAGE_V + 8192, &mapV, &bar_full[st], h * D + 64, rowt);
+        bulk_load(stg + STAGE_REC, rec, WS_TILES, &bar_full[st]);
+        bulk_load(sm + OFF_SC + st * 512, rec + WS_SC, WS_SC_BYTES, &bar_full[st]);
       };
-      const uint32_t id_wu = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = K^T or V^T (MN-major), B K-major
-      const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);    // A = X^T pieces (TMEM), B = Wk^T
-      const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);   // A = R^T pieces (TMEM), B = K
-      // Wk^T -> TM_W and -U^T -> TM_P for chunk c (M = 128, N = 64, K = 64).
-      auto issue_wu = [&](int c) {
-        const int st = c & 1;
-        const uint32_t kb = sb + OFF_KV + st * 32768, wb = sb + OFF_WS + st * WS_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ak = sdesc_sw128(kb + kk * 2048, 8192, 1024);
-          mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABH + kk * 32, 16, 1024), id_wu, kk > 0);
-          mma_f16(tmem + TM_W, ak, sdesc_sw128(wb + WS_ABL + kk * 32, 16, 1024), id_wu, 1);
-          if (isS) {
-            const uint64_t av = sdesc_sw128(kb + 16384 + kk * 2048, 8192, 1024);
-            mma_f16(tmem + TM_P, av, sdesc_sw128(wb + WS_AVH + kk * 32, 16, 1024), id_wu, kk > 0);
-            mma_f16(tmem + TM_P, av, sdesc_sw128(wb + WS_AVL + kk * 32, 16, 1024), id_wu, 1);
-          }
-        }
-        mma_commit(&bar_w);
-      };
+      const uint32_t id_u = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = V^T (MN-major), B K-major
+      const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces, B = Wk^T (MN-major)
+      const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces (TMEM), B = K
       bool ok = true;
-      if (nchunks > 0) {
-        issue_tma(0);
-        if (nchunks > 1) issue_tma(1);
-        ok = mbar_wait_cycles(&bar_tma[0], 0, a.err);
-        if (ok) {
-          tc_fence_after();
-          issue_wu(0);
-        }
-      }
+      if (nchunks > 0) issue_tma(0);
+      if (nchunks > 1) issue_tma(1);
       for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c & 1;
-        const uint32_t kbase = sb + OFF_KV + st * 32768;
-        const uint32_t wsb = sb + OFF_WS + st * WS_STAGE;
         const uint32_t par = (uint32_t)c & 1u;
-        // P^T (onto -U^T for the S half): M = 128 (n), N = 64 (t), K = 128 (i).
-        if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
+        const uint32_t stg = sb + st * STAGE_BYTES;
+        if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t wh = sdesc_sw128(wsb + kk * 2048, 16384, 1024);
-          const uint64_t wl = sdesc_sw128(wsb + 16384 + kk * 2048, 16384, 1024);
-          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wh, id_p, (isS || kk > 0) ? 1u : 0u);
-          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + kk * 8, wl, id_p, 1);
-          mma_f16_tmem_a(tmem + TM_P, tmem + TM_XP + 64 + kk * 8, wh, id_p, 1);
-        }
-        mma_commit(&bar_p);
-        // X^T += R^T K: M = 128 (n), N = 128 (i), K = 64 (t).
-        if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
-        tc_fence_after();
+        // -U^T into the S half's P^T (M = 128 j, N = 64 t, K = 64 s).
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bk = sdesc_sw128(kbase + kk * 2048, 8192, 1024);
-          mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + kk * 8, bk, id_x, 1);
-          mma_f16_tmem_a(tmem + TM_X, tmem + TM_RP + 32 + kk * 8, bk, id_x, 1);
+          const uint64_t av = sdesc_sw128(stg + STAGE_V + kk * 2048, 8192, 1024);
+          mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVH + kk * 32, 16, 1024), id_u, kk > 0);
+          mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVL + kk * 32, 16, 1024), id_u, 1);
         }
-        mma_commit(&bar_x);
-        if (c + 1 < nchunks) {
-          if (!(ok = mbar_wait_cycles(&bar_tma[(c + 1) & 1], ((uint32_t)(c + 1) >> 1) & 1u, a.err))) break;
+        // The stage of chunk c - 1 is free once that chunk's S update has run: refill it.
+        if (c >= 1 && c + 1 < nchunks) {
+          if (!(ok = mbar_wait_cycles(&bar_x[1], par ^ 1u, a.err))) break;
+          issue_tma(c + 1);
+        }
+        // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
           tc_fence_after();
-          issue_wu(c + 1);
+          const uint32_t xlo = sb + OFF_XLO + hf * 32768;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t wh = sdesc_sw128(stg + STAGE_REC + WS_WH + kk * 2048, 16384, 1024);
+            const uint64_t wl = sdesc_sw128(stg + STAGE_REC + WS_WL + kk * 2048, 16384, 1024);
+            const uint64_t al = sdesc_sw128(xlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            mma_f16_tmem_a(tmem + tm_p(hf), tmem + tm_xp(hf) + kk * 8, wh, id_p, (hf == 1 || kk > 0) ? 1u : 0u);
+            mma_f16_tmem_a(tmem + tm_p(hf), tmem + tm_xp(hf) + kk * 8, wl, id_p, 1);
+            mma_f16(tmem + tm_p(hf), al, wh, id_p, 1);
+          }
+          mma_commit(&bar_p[hf]);
         }
-        if (c + 2 < nchunks) {
-          // The stage of chunk c is consumed once its update has run: refill it with chunk c + 2.
-          if (!(ok = mbar_wait_cycles(&bar_x, par, a.err))) break;
-          issue_tma(c + 2);
+        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          if (!(ok = mbar_wait_cycles(&bar_r2[hf], par, a.err))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bk = sdesc_sw128(stg + STAGE_K + kk * 2048, 8192, 1024);
+            const uint32_t pc = tmem + tm_p(hf) + 32 * (kk >> 1) + 8 * (kk & 1);
+            mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
+            mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);
+          }
+          mma_commit(&bar_x[hf]);
         }
       }
       if (!ok) abort_flag = 1;
@@ -503,76 +547,59 @@ __global__ void __launch_bounds__(NT2, 1)
   } else {
     // ------------------------------------------------------------------------- conversion warps
     // X^T starts at [I | 0]^T restricted to this half: I (T half) or 0 (S half).
+    const uint32_t tx = tmem + lane_base + tm_x(half), txp = tmem + lane_base + tm_xp(half);
+    const uint32_t tp = tmem + lane_base + tm_p(half);
+    uint8_t *xlo = sm + OFF_XLO + half * 32768 + part * 16384;
     for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
       float v[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = (!isS && c0 + q == row) ? 1.f : 0.f;
-      tmem_st16(tmem + lane_base + TM_X + c0, v);
+      for (int q = 0; q < 16; ++q) v[q] = (half == 0 && c0 + q == row) ? 1.f : 0.f;
+      tmem_st16(tx + c0, v);
     }
     tmem_st_wait();
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int st = c & 1;
-      uint8_t *wsd = sm + OFF_WS + st * WS_STAGE;
       const uint32_t par = (uint32_t)c & 1u;
-      if (c > 0 && !(ok = mbar_wait_cycles(&bar_x, par ^ 1u, a.err))) break;  // the previous update is done
-      if (!(ok = mbar_wait_cycles(&bar_tma[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
+      if (c > 0 && !(ok = mbar_wait_cycles(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
+      if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
       tc_fence_after();
-      const float *sR = reinterpret_cast<const float *>(wsd + WS_SC);
+      const float *sR = reinterpret_cast<const float *>(sm + OFF_SC + st * 512);
       const float gamma_C = sR[C];
-      // (1) X^T -> bf16 hi/lo pieces (this thread's 64 rows i), and gamma_C X^T back.
-      {
-        float xv[64];
-        tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
+      // (1) this thread's 64 rows i of X^T: hi pieces to TMEM, lo pieces to the shared A tile,
+      // gamma_C X^T back into the accumulator.
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          float ph[8], pl[8];
+      for (int cb = 0; cb < 64; cb += 32) {
+        float xv[32];
+        tmem_ld32(tx + 64 * part + cb, xv);
+        float ph[16];
+        uint32_t pl[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t hi, lo;
-            split2_pair(xv[c0 + 2 * q], xv[c0 + 2 * q + 1], hi, lo);
-            ph[q] = __uint_as_float(hi);
-            pl[q] = __uint_as_float(lo);
-          }
-          const uint32_t col = (uint32_t)(64 * part + c0) / 2;
-          tmem_st8(tmem + lane_base + TM_XP + col, ph);
-          tmem_st8(tmem + lane_base + TM_XP + 64 + col, pl);
+        for (int q = 0; q < 16; ++q) {
+          uint32_t hi;
+          split2_pair(xv[2 * q], xv[2 * q + 1], hi, pl[q]);
+          ph[q] = __uint_as_float(hi);
         }
+        tmem_st16(txp + (64 * part + cb) / 2, ph);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          float sv[16];
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
+              make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) sv[q] = xv[c0 + q] * gamma_C;
-          tmem_st16(tmem + lane_base + TM_X + 64 * part + c0, sv);
-        }
-      }
-      // (2) Wk^T -> MN-major B tile [i][t] hi/lo over the consumed A tiles of the stage
-      // (this thread: t in [32 part, 32 part + 32)).
-      if (!(ok = mbar_wait_cycles(&bar_w, par, a.err))) break;
-      tc_fence_after();
-      {
-        float wv[32];
-        tmem_ld32(tmem + lane_base + TM_W + 32 * part, wv);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split2_pair(wv[8 * q4 + 2 * e], wv[8 * q4 + 2 * e + 1], hi[e], lo[e]);
-          const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(4 * part + q4));
-          *reinterpret_cast<uint4 *>(wsd + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4 *>(wsd + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+        for (int q = 0; q < 32; ++q) xv[q] *= gamma_C;
+        tmem_st32(tx + 64 * part + cb, xv);
       }
       tmem_st_wait();
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(&bar_r1);
-      // (3) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in TMEM.
-      if (!(ok = mbar_wait_cycles(&bar_p, par, a.err))) break;
+      mbar_arrive(&bar_r1[half]);
+      // (2) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in place: this thread's
+      // columns t in [32 part, 32 part + 32) become 16 hi columns then 16 lo columns.
+      if (!(ok = mbar_wait_cycles(&bar_p[half], par, a.err))) break;
       tc_fence_after();
       {
         float pv[32];
-        tmem_ld32(tmem + lane_base + TM_P + 32 * part, pv);
+        tmem_ld32(tp + 32 * part, pv);
         float ph[16], pl[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -582,35 +609,38 @@ __global__ void __launch_bounds__(NT2, 1)
           ph[q] = __uint_as_float(hi);
           pl[q] = __uint_as_float(lo);
         }
-        tmem_st16(tmem + lane_base + TM_RP + 16 * part, ph);
-        tmem_st16(tmem + lane_base + TM_RP + 32 + 16 * part, pl);
+        tmem_st16(tp + 32 * part, ph);
+        tmem_st16(tp + 32 * part + 16, pl);
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&bar_r2);
+      mbar_arrive(&bar_r2[half]);
     }
-    if (ok && nchunks > 0) ok = mbar_wait_cycles(&bar_x, (uint32_t)(nchunks - 1) & 1u, a.err);
+    if (ok && nchunks > 0) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)(nchunks - 1) & 1u, a.err);
     if (!ok) abort_flag = 1;
   }
   __syncthreads();
   tc_fence_after();
   if (abort_flag && tid == 0) {
     // Let any copy or MMA still in flight land before the tensor memory is released.
-    for (int k = 0; k < 2; ++k) {
-      mbar_wait_cycles(&bar_x, (uint32_t)k, nullptr, 100000000LL);
-      mbar_wait_cycles(&bar_w, (uint32_t)k, nullptr, 100000000LL);
-      mbar_wait_cycles(&bar_p, (uint32_t)k, nullptr, 100000000LL);
-      mbar_wait_cycles(&bar_tma[0], (uint32_t)k, nullptr, 100000000LL);
-      mbar_wait_cycles(&bar_tma[1], (uint32_t)k, nullptr, 100000000LL);
-    }
+    for (int k = 0; k < 2; ++k)
+      for (int i = 0; i < 2; ++i) {
+        mbar_wait_cycles(&bar_x[i], (uint32_t)k, nullptr, 100000000LL);
+        mbar_wait_cycles(&bar_p[i], (uint32_t)k, nullptr, 100000000LL);
+        mbar_wait_cycles(&bar_full[i], (uint32_t)k, nullptr, 100000000LL);
+      }
   }
   if (!abort_flag && !issuer) {
     // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
-    float *out = (isS ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
-    float xv[64];
-    tmem_ld64(tmem + lane_base + TM_X + 64 * part, xv);
+    float *out = (half ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
+    const uint32_t tx = tmem + lane_base + tm_x(half);
 #pragma unroll
-    for (int q = 0; q < 64; ++q) out[(size_t)(64 * part + q) * D + row] = xv[q];
+    for (int cb = 0; cb < 64; cb += 32) {
+      float xv[32];
+      tmem_ld32(tx + 64 * part + cb, xv);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) out[(size_t)(64 * part + cb + q) * D + row] = xv[q];
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -675,7 +705,7 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     a.h0 = h0;
     a.Hb = (r.H - h0) < Hb ? (r.H - h0) : Hb;
     const long long g1 = (long long)r.n_seg * a.max_chunks * a.Hb;
-    const long long g2 = (long long)r.n_seg * a.Hb * 2;
+    const long long g2 = (long long)r.n_seg * a.Hb;
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     wy_prep_kernel<<<(unsigned)g1, NT, P_SMEM, st>>>(mk, a);
     chain_tc_kernel<<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);

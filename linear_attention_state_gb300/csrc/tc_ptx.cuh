@@ -108,6 +108,15 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// Plain bulk copy shared -> global (bulk-group completion); same alignment rules.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of this thread has completed (writes visible).
+__device__ __forceinline__ void bulk_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -258,6 +267,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+#define HYPIC_U(i) "r"(__float_as_uint(v[i]))
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      HYPIC_U(0), HYPIC_U(1), HYPIC_U(2), HYPIC_U(3), HYPIC_U(4), HYPIC_U(5), HYPIC_U(6), HYPIC_U(7), HYPIC_U(8),
+      HYPIC_U(9), HYPIC_U(10), HYPIC_U(11), HYPIC_U(12), HYPIC_U(13), HYPIC_U(14), HYPIC_U(15), HYPIC_U(16),
+      HYPIC_U(17), HYPIC_U(18), HYPIC_U(19), HYPIC_U(20), HYPIC_U(21), HYPIC_U(22), HYPIC_U(23), HYPIC_U(24),
+      HYPIC_U(25), HYPIC_U(26), HYPIC_U(27), HYPIC_U(28), HYPIC_U(29), HYPIC_U(30), HYPIC_U(31)
+      : "memory");
+#undef HYPIC_U
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled

@@ -155,7 +155,7 @@ def test_binding_refuses_cpu_tensors():
 
 def test_build_workspace_contract(lib):
     sh = L.shape(32, 128, "gated_delta", "bf16")
-    per_head = 8 * 64 * 33280
+    per_head = 8 * 64 * 49664
     assert lib.hypic_build_workspace_bytes(ctypes.byref(sh), 8, 4096) == 32 * per_head
     # shapes that run without a workspace
     for fam, dt in (("scalar", "bf16"), ("gated_delta", "f32")):

@@ -19,7 +19,7 @@ from linear_attention_state_gb300 import _lib as L
 from refs import TOL_BF16, np64, relerr
 
 SCRATCH = 64 << 20
-RECORD = 33280
+RECORD = 49664
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +58,7 @@ def test_noalloc_build_matches_the_workspace_build_twice(lib):
         off += L_ + gap
     b_dev = torch.tensor(bounds, dtype=torch.int64, device=dev)
     max_len = max(lens)
-    # per head: 4 bodies x 16 chunks x 33,280 B = 2.1 MB, so 40 heads take two blocks of the scratch
+    # per head: 4 bodies x 16 chunks x 49,664 B = 3.2 MB, so 40 heads take two blocks of the scratch
     assert len(lens) * ((max_len + 63) // 64) * RECORD * H > SCRATCH
 
     T_ref, S_ref = hy.segment_build_batched(tok["k"], tok["v"], b_dev, tok["alpha"], tok["beta"],

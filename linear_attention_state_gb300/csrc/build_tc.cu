@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ 
 //   P^T - U^T = X^T Wk^T - U^T   A = X^T hi (TMEM) / lo (shared), B = Wk^T [i][t] (MN-major)
 //   X^T = gamma_C X^T + R^T K    A = R^T hi/lo pieces (TMEM, in place over P^T), B = K [t][i]
 // -U^T = V^T (-A diag(b))^T is written into the S half's P accumulator first.  Warp 16 issues
-// every TMA copy and MMA; warps 0-7 convert for the T half and warps 8-15 for the S half (two
-// threads per TMEM lane each).  MMA completions reach the converters through tcgen05.commit;
+// every MMA, warp 17 every TMA copy; warps 0-7 convert for the T half and warps 8-15 for the S
+// half (two threads per TMEM lane each).  MMA completions reach the converters through tcgen05.commit;
 // the converters arrive after their TMEM and shared-memory writes are fenced.
 constexpr uint32_t STAGE_K = 0, STAGE_V = 16384, STAGE_REC = 32768;  // within a stage
 constexpr uint32_t STAGE_BYTES = STAGE_REC + WS_TILES;               // 81,920 (1024-aligned)
@@ -411,7 +411,7 @@ __device__ __forceinline__ uint32_t tm_p(int h) { return 384u + 64u * h; }
 constexpr uint32_t TM_COLS = 512;
 
 constexpr int NCONV = 512;       // conversion threads: two per TMEM lane and half
-constexpr int NT2 = NCONV + 32;  // + the issuing warp
+constexpr int NT2 = NCONV + 64;  // + the MMA warp and the TMA warp
 
 // hi = truncation of x to bf16, lo = bf16 rounding of the exact remainder, for two values;
 // returns the packed hi pair and lo pair (first value in the low half).
@@ -428,13 +428,14 @@ __global__ void __launch_bounds__(NT2, 1)
                     BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // per half: r1 (X pieces ready), r2 (R pieces ready), p (P^T done), x (update done)
-  __shared__ uint64_t bar_full[2], bar_r1[2], bar_r2[2], bar_p[2], bar_x[2];
+  // per stage: full (copies landed), empty (the chunk's last MMAs done)
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1[2], bar_r2[2], bar_p[2], bar_x[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const bool issuer = warp == NCONV / 32;
+  const bool issuer = warp == NCONV / 32, producer = warp == NCONV / 32 + 1;
   const int row = tid & 127;        // TMEM lane a conversion thread serves
   const int part = (tid >> 7) & 1;  // which half of that lane's columns
   const int half = (tid >> 8) & 1;  // 0: T columns, 1: S columns
@@ -452,6 +453,7 @@ __global__ void __launch_bounds__(NT2, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
       mbar_init(&bar_r1[i], 256);
       mbar_init(&bar_r2[i], 256);
       mbar_init(&bar_p[i], 1);
@@ -469,13 +471,17 @@ __global__ void __launch_bounds__(NT2, 1)
   const uint32_t tmem = tmem_slot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (issuer) {
-    // ----------------------------------------------------------------------------- issuing warp
+  if (producer) {
+    // ------------------------------------------------------------------------------- TMA warp
+    // Chunk c goes into stage c & 1 once chunk c - 2, the stage's previous user, has run its last
+    // MMAs (the converters are done with the stage before those are issued).
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      auto issue_tma = [&](int c) {
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c & 1;
+        if (c >= 2 && !(ok = mbar_wait_cycles(&bar_empty[st], (uint32_t)((c >> 1) - 1) & 1u, a.err))) break;
         const int rowt = (int)(beg + (int64_t)c * C);
         uint8_t *stg = sm + st * STAGE_BYTES;
         const uint8_t *rec = ws_rec(a, s, c, hh);
@@ -486,31 +492,35 @@ __global__ void __launch_bounds__(NT2, 1)
         tma_load_2d(stg + STAGE_V + 8192, &mapV, &bar_full[st], h * D + 64, rowt);
         bulk_load(stg + STAGE_REC, rec, WS_TILES, &bar_full[st]);
         bulk_load(sm + OFF_SC + st * 512, rec + WS_SC, WS_SC_BYTES, &bar_full[st]);
-      };
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (issuer) {
+    // ------------------------------------------------------------------------------- MMA warp
+    if (lane == 0) {
       const uint32_t id_u = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = V^T (MN-major), B K-major
       const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces, B = Wk^T (MN-major)
       const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces (TMEM), B = K
-      bool ok = true;
-      if (nchunks > 0) issue_tma(0);
-      if (nchunks > 1) issue_tma(1);
-      for (int c = 0; c < nchunks && ok; ++c) {
+      // -U^T of chunk c into the S half's P^T (M = 128 j, N = 64 t, K = 64 s).  It follows the
+      // previous chunk's S update in the pipe, which has read the R^T pieces stored there.
+      auto issue_u = [&](int c) -> bool {
         const int st = c & 1;
-        const uint32_t par = (uint32_t)c & 1u;
         const uint32_t stg = sb + st * STAGE_BYTES;
-        if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
+        if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err)) return false;
         tc_fence_after();
-        // -U^T into the S half's P^T (M = 128 j, N = 64 t, K = 64 s).
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t av = sdesc_sw128(stg + STAGE_V + kk * 2048, 8192, 1024);
           mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVH + kk * 32, 16, 1024), id_u, kk > 0);
           mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVL + kk * 32, 16, 1024), id_u, 1);
         }
-        // The stage of chunk c - 1 is free once that chunk's S update has run: refill it.
-        if (c >= 1 && c + 1 < nchunks) {
-          if (!(ok = mbar_wait_cycles(&bar_x[1], par ^ 1u, a.err))) break;
-          issue_tma(c + 1);
-        }
+        return true;
+      };
+      bool ok = nchunks == 0 || issue_u(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const uint32_t par = (uint32_t)c & 1u;
+        const uint32_t stg = sb + (c & 1) * STAGE_BYTES;
         // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
         for (int hf = 0; hf < 2 && ok; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
@@ -540,6 +550,8 @@ __global__ void __launch_bounds__(NT2, 1)
           }
           mma_commit(&bar_x[hf]);
         }
+        if (ok) mma_commit(&bar_empty[c & 1]);
+        if (ok && c + 1 < nchunks) ok = issue_u(c + 1);
       }
       if (!ok) abort_flag = 1;
     }
@@ -628,9 +640,10 @@ __global__ void __launch_bounds__(NT2, 1)
         mbar_wait_cycles(&bar_x[i], (uint32_t)k, nullptr, 100000000LL);
         mbar_wait_cycles(&bar_p[i], (uint32_t)k, nullptr, 100000000LL);
         mbar_wait_cycles(&bar_full[i], (uint32_t)k, nullptr, 100000000LL);
+        mbar_wait_cycles(&bar_empty[i], (uint32_t)k, nullptr, 100000000LL);
       }
   }
-  if (!abort_flag && !issuer) {
+  if (!abort_flag && !issuer && !producer) {
     // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
     float *out = (half ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
     const uint32_t tx = tmem + lane_base + tm_x(half);

@@ -537,7 +537,9 @@ __global__ void __launch_bounds__(NT2, 1)
           }
           mma_commit(&bar_p[hf]);
         }
-        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).
+        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next chunk's -U^T
+        // is queued right behind the S update, before its commit, so the pipe does not wait
+        // for the commits; the S half's update barrier then also covers it.
         for (int hf = 0; hf < 2 && ok; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r2[hf], par, a.err))) break;
           tc_fence_after();
@@ -548,10 +550,11 @@ __global__ void __launch_bounds__(NT2, 1)
             mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);
           }
+          if (hf == 1 && c + 1 < nchunks) ok = issue_u(c + 1);
+          if (!ok) break;
           mma_commit(&bar_x[hf]);
         }
         if (ok) mma_commit(&bar_empty[c & 1]);
-        if (ok && c + 1 < nchunks) ok = issue_u(c + 1);
       }
       if (!ok) abort_flag = 1;
     }
@@ -573,8 +576,8 @@ __global__ void __launch_bounds__(NT2, 1)
     for (int c = 0; c < nchunks && ok; ++c) {
       const int st = c & 1;
       const uint32_t par = (uint32_t)c & 1u;
-      if (c > 0 && !(ok = mbar_wait_cycles(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
-      if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
+      if (c > 0 && !(ok = mbar_wait_sleep(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
+      if (!(ok = mbar_wait_sleep(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
       tc_fence_after();
       const float *sR = reinterpret_cast<const float *>(sm + OFF_SC + st * 512);
       const float gamma_C = sR[C];
@@ -607,7 +610,7 @@ __global__ void __launch_bounds__(NT2, 1)
       mbar_arrive(&bar_r1[half]);
       // (2) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in place: this thread's
       // columns t in [32 part, 32 part + 32) become 16 hi columns then 16 lo columns.
-      if (!(ok = mbar_wait_cycles(&bar_p[half], par, a.err))) break;
+      if (!(ok = mbar_wait_sleep(&bar_p[half], par, a.err))) break;
       tc_fence_after();
       {
         float pv[32];

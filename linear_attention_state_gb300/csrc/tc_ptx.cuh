@@ -53,6 +53,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase, int *er
   return false;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps until it
+// completes or about `hint_ns` nanoseconds pass, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t phase, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for waiters that expect to wait long: sleeps in try_wait rather than spinning,
+// so it takes no issue slots from the warps doing the work.  Gives up after `limit` cycles.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t phase, int *err,
+                                                long long limit = 2000000000LL) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, phase, 20000u)) {
+    if (clock64() - t0 > limit) {
+      set_error(err, HYPIC_ETIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Same, bounded by elapsed SM clock cycles instead of polls (about a second at 2 GHz
 // for the default limit).
 __device__ __forceinline__ bool mbar_wait_cycles(uint64_t *bar, uint32_t phase, int *err,

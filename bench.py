@@ -35,9 +35,11 @@ FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 # dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
-# this workload, from the ncu capture summarised in profiles/build_tc_32h_d128_8x4096.md; None
-# until the current kernels have been captured.
-BUILD_TC_TRAFFIC = None
+# this workload, from the ncu capture summarised in profiles/build_tc_32h_d128_8x4096.md.
+BUILD_TC_TRAFFIC = 277_341_000 + 749_664_256 + 1_349_144_000 + 27_557_632
+# The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from the capture
+# summarised in profiles/build_decay_tc_32h_d128_64x512.md.
+DECAY_TC_TRAFFIC = {"scalar_const": 536_935_000 + 112_331_264, "diag": 1_073_959_000 + 122_754_304}
 
 
 def load_peaks():
@@ -276,7 +278,8 @@ def decay_build_measure(steps, warmup, dev, peaks):
             by = per * ht + w.n_seg * w.H * w.d * w.d * 4
             entry["roofline"] = {"bound": "hbm", "achieved": by / tb / 1e9, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": by / tb / 1e9 / peaks["hbm_gbs"],
-                                 "bytes_per_head_token": per}
+                                 "bytes_per_head_token": per, "traffic": DECAY_TC_TRAFFIC.get(fam),
+                                 "kernel": "build_decay_tc_kernel"}
         entry["status"] = hy.stream_status()
         out[fam] = entry
         del tok, T, S, ws
@@ -378,6 +381,10 @@ def main():
     ap.add_argument("--compose-pool", type=int, default=None, help="pool entries per head (default 256)")
     ap.add_argument("--compose-n", type=int, default=None, help="segments per request (default 16)")
     ap.add_argument("--compose-random", action="store_true", help="generator-drawn pairs instead of built ones")
+    ap.add_argument("--decay-only", action="store_true",
+                    help="time only the decay-family builds (profiling aid; prints its own line)")
+    ap.add_argument("--scan-only", action="store_true",
+                    help="time only the affine scan (profiling aid; prints its own line)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -416,6 +423,12 @@ def main():
             print(json.dumps({"metric": "compositions/s", "value": res["compositions_per_s"] * world,
                               "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
                               "warmup": args.warmup, "compose_pool": res}))
+        return
+    if args.decay_only or args.scan_only:
+        res = (decay_build_measure if args.decay_only else scan_measure)(args.steps, args.warmup, dev, peaks)
+        if rank == 0:
+            print(json.dumps({"metric": "decay-family builds" if args.decay_only else "affine scan",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "result": res}))
         return
     req = RequestStep(w, dev)
     status0 = hy.stream_status()

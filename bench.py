@@ -315,8 +315,12 @@ def scan_measure(steps, warmup, dev, peaks):
     return res
 
 
-def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False):
-    """Warm-cache composition: 30 layers x 32 heads, pool of 256 fp32 pairs, 64 requests x 16 segments."""
+def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False, storage="both"):
+    """Warm-cache composition: 30 layers x 32 heads, pool of 256 pairs, 64 requests x 16 segments.
+
+    storage "f32": fp32 pairs (128 KiB per composition); "bf16": the same pairs rounded to bf16
+    (64 KiB per composition, 16-bit cache storage); "both": fp32 first, then bf16 as "bf16_pool".
+    """
     import dataclasses
 
     import torch
@@ -342,27 +346,44 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
             del tok, T, S
     idx = pw.request_indices(dev)
     out = torch.empty((pw.B, H, d, d), device=dev)
-    torch.cuda.synchronize()
-
-    def fn(ev):
-        if ev is not None:
-            ev[0].record()
-        hy.compose(pool_T, pool_S, idx, family="gated_delta", out=out)
-        if ev is not None:
-            ev[1].record()
-            ev[2].record()
-
-    total_ms, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
     comps = pw.B * pw.n * H
-    avg = sum(k1) / len(k1) / 1e3
-    bytes_ = comps * BYTES_PER_COMPOSITION
-    st = hy.stream_status()
-    res = {"workload": pw.name, "compositions_per_s": comps / (total_ms / 1e3 / steps), "ms_per_step": total_ms / steps,
-           "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"], "traffic": None,
-                        "peak_source": peaks["source"]},
-           "status": st}
-    del pool_T, pool_S
+
+    def timed(pT, pS, bytes_per_comp, name):
+        torch.cuda.synchronize()
+
+        def fn(ev):
+            if ev is not None:
+                ev[0].record()
+            hy.compose(pT, pS, idx, family="gated_delta", out=out)
+            if ev is not None:
+                ev[1].record()
+                ev[2].record()
+
+        total_ms, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+        avg = sum(k1) / len(k1) / 1e3
+        bytes_ = comps * bytes_per_comp
+        return {"workload": name, "compositions_per_s": comps / (total_ms / 1e3 / steps),
+                "ms_per_step": total_ms / steps,
+                "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                             "bytes_per_composition": bytes_per_comp, "peak_source": peaks["source"]},
+                "status": hy.stream_status()}
+
+    res = None
+    if storage in ("f32", "both"):
+        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION, pw.name)
+    if storage in ("bf16", "both"):
+        T_lp, S_lp = hy.pairs_to_bf16(pool_T, pool_S, family="gated_delta")
+        del pool_T, pool_S
+        torch.cuda.empty_cache()
+        lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2, pw.name + "_bf16pairs")
+        del T_lp, S_lp
+        if res is None:
+            res = lp
+        else:
+            res["bf16_pool"] = lp
+    else:
+        del pool_T, pool_S
     torch.cuda.empty_cache()
     return res
 
@@ -381,6 +402,8 @@ def main():
     ap.add_argument("--compose-pool", type=int, default=None, help="pool entries per head (default 256)")
     ap.add_argument("--compose-n", type=int, default=None, help="segments per request (default 16)")
     ap.add_argument("--compose-random", action="store_true", help="generator-drawn pairs instead of built ones")
+    ap.add_argument("--compose-storage", default="both", choices=["both", "f32", "bf16"],
+                    help="pair storage of the composition measurement (fp32, bf16 or both)")
     ap.add_argument("--decay-only", action="store_true",
                     help="time only the decay-family builds (profiling aid; prints its own line)")
     ap.add_argument("--scan-only", action="store_true",
@@ -418,7 +441,7 @@ def main():
 
     if args.compose_only:
         res = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
-                                   args.compose_random)
+                                   args.compose_random, args.compose_storage)
         if rank == 0:
             print(json.dumps({"metric": "compositions/s", "value": res["compositions_per_s"] * world,
                               "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
@@ -488,7 +511,7 @@ def main():
     if not args.no_compose:
         del host
         compose = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
-                                       args.compose_random)
+                                       args.compose_random, args.compose_storage)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

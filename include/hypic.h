@@ -213,6 +213,39 @@ hypic_status hypic_assemble(const hypic_shape *shape, int32_t B, int32_t n, int3
                             const float *S_init, float *S_out, float *o_out, hypic_stream_t stream);
 
 /*
+ * 16-bit storage of cached pairs (HYPIC notes, Method 3, Table 3: the cache sizes there
+ * assume 16-bit T_C and S).  Rounds n_pairs fp32 pairs to bf16, round to nearest even:
+ *   T [n_pairs, H, t_size] fp32 -> T_lp, same layout, bf16
+ *   S [n_pairs, H, d_k, d_v] fp32 -> S_lp, same layout, bf16
+ * Device pointers, 16-byte aligned; the outputs must not overlap the inputs.  bf16 keeps
+ * fp32's exponent range, so a T_C that has decayed far stays representable; each stored
+ * value carries a relative rounding error of at most 2^-9.
+ * Errors: HYPIC_EINVAL (null or misaligned pointer, n_pairs < 0), HYPIC_EUNSUPPORTED (shape),
+ * HYPIC_ECUDA.
+ */
+hypic_status hypic_pairs_to_bf16(const hypic_shape *shape, int64_t n_pairs, const float *T, const float *S,
+                                 void *T_lp, void *S_lp, hypic_stream_t stream);
+
+/*
+ * hypic_compose and hypic_assemble over a pool stored in bf16 (as written by
+ * hypic_pairs_to_bf16; same layouts, half the bytes).  The running state, S_init, S_out and
+ * o_out stay fp32; each step computes S <- T S + S0 with the stored bf16 values taken
+ * exactly (no further rounding of T or S0), so the result matches a float64 composition of
+ * the same stored values to fp32 accuracy.  Supported for every family at d_k = d_v = 128 and
+ * for the scalar and diagonal families at every size; the delta families at d < 128 return
+ * HYPIC_EUNSUPPORTED before anything is enqueued.  Other arguments and errors as in
+ * hypic_compose / hypic_assemble.
+ */
+hypic_status hypic_compose_bf16(const hypic_shape *shape, int32_t B, int32_t n, const int32_t *idx,
+                                int64_t pool_size, const void *pool_T, const void *pool_S,
+                                const float *S_init, float *S_out, hypic_stream_t stream);
+hypic_status hypic_assemble_bf16(const hypic_shape *shape, int32_t B, int32_t n, int32_t w,
+                                 const int32_t *idx, int64_t pool_size, const void *pool_T,
+                                 const void *pool_S, const void *seam_q, const void *seam_k,
+                                 const void *seam_v, const float *seam_alpha, const float *seam_beta,
+                                 const float *S_init, float *S_out, float *o_out, hypic_stream_t stream);
+
+/*
  * Waits for `stream`, then returns and clears the status word of the current
  * device: HYPIC_OK, HYPIC_EDEVICE or HYPIC_ETIMEOUT (first error recorded by
  * any kernel since the last call), or HYPIC_ECUDA if the stream itself failed.

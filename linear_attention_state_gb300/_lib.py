@@ -41,6 +41,10 @@ SIGNATURES = {
     "hypic_seam_advance": (_i32, [_SP, _i32, _fp, _vp, _vp, _vp, _fp, _fp, _i32, _fp, _vp]),
     "hypic_assemble": (_i32, [_SP, _i32, _i32, _i32, _i32p, _i64, _fp, _fp, _vp, _vp, _vp, _fp, _fp, _fp,
                               _fp, _fp, _vp]),
+    "hypic_pairs_to_bf16": (_i32, [_SP, _i64, _fp, _fp, _vp, _vp, _vp]),
+    "hypic_compose_bf16": (_i32, [_SP, _i32, _i32, _i32p, _i64, _vp, _vp, _fp, _fp, _vp]),
+    "hypic_assemble_bf16": (_i32, [_SP, _i32, _i32, _i32, _i32p, _i64, _vp, _vp, _vp, _vp, _vp, _fp, _fp, _fp,
+                                   _fp, _fp, _vp]),
     "hypic_stream_status": (_i32, [_vp]),
     "hypic_selftest_bounded_wait": (_i32, [_i64, _vp]),
 }

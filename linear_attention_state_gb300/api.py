@@ -125,10 +125,34 @@ def segment_build_batched(k, v, bounds, alpha=None, beta=None, q=None, family="g
     return (T, S, o) if want_o else (T, S)
 
 
-def compose(pool_T, pool_S, idx, S_init=None, family="gated_delta", out=None, stream=None):
-    """S_out [B, H, d, d]: each request b composes pool entries idx[b, 0..n-1] in order."""
+def _pool_dtype(pool_T, pool_S):
+    """fp32 pools, or bf16 pools (16-bit pair storage, see pairs_to_bf16); both the same."""
+    dt = pool_S.dtype if isinstance(pool_S, torch.Tensor) else None
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("pool_S must be a float32 or bfloat16 CUDA tensor")
+    _cuda(pool_S, "pool_S", dt), _cuda(pool_T, "pool_T", dt)
+    return dt == torch.bfloat16
+
+
+def pairs_to_bf16(T, S, family="gated_delta", stream=None):
+    """Round fp32 pairs T [n, H, ...], S [n, H, d, d] to bf16 storage (nearest even)."""
     lib = L.load()
-    _cuda(pool_S, "pool_S", torch.float32), _cuda(pool_T, "pool_T", torch.float32)
+    _cuda(T, "T", torch.float32), _cuda(S, "S", torch.float32)
+    n, H, d, _ = S.shape
+    T_lp = torch.empty(T.shape, device=S.device, dtype=torch.bfloat16)
+    S_lp = torch.empty(S.shape, device=S.device, dtype=torch.bfloat16)
+    sh = L.shape(H, d, family, "f32")
+    st = lib.hypic_pairs_to_bf16(ctypes.byref(sh), n, _p(T), _p(S), _p(T_lp), _p(S_lp), _stream(stream))
+    L.check(st, "hypic_pairs_to_bf16")
+    return T_lp, S_lp
+
+
+def compose(pool_T, pool_S, idx, S_init=None, family="gated_delta", out=None, stream=None):
+    """S_out [B, H, d, d]: each request b composes pool entries idx[b, 0..n-1] in order.
+
+    The pools are fp32, or bf16 as written by pairs_to_bf16 (hypic_compose_bf16)."""
+    lib = L.load()
+    lp = _pool_dtype(pool_T, pool_S)
     _cuda(idx, "idx", torch.int32)
     P, H, d, _ = pool_S.shape
     B, n = idx.shape
@@ -136,9 +160,9 @@ def compose(pool_T, pool_S, idx, S_init=None, family="gated_delta", out=None, st
         _cuda(S_init, "S_init", torch.float32)
     S_out = out if out is not None else torch.empty((B, H, d, d), device=pool_S.device, dtype=torch.float32)
     sh = L.shape(H, d, family, "f32")
-    st = lib.hypic_compose(ctypes.byref(sh), B, n, _p(idx), P, _p(pool_T), _p(pool_S), _p(S_init), _p(S_out),
-                           _stream(stream))
-    L.check(st, "hypic_compose")
+    fn, name = (lib.hypic_compose_bf16, "hypic_compose_bf16") if lp else (lib.hypic_compose, "hypic_compose")
+    st = fn(ctypes.byref(sh), B, n, _p(idx), P, _p(pool_T), _p(pool_S), _p(S_init), _p(S_out), _stream(stream))
+    L.check(st, name)
     return S_out
 
 
@@ -176,9 +200,11 @@ def seam_advance(S, k, v, alpha=None, beta=None, q=None, family="gated_delta", w
 
 def assemble(pool_T, pool_S, idx, seam_k, seam_v, seam_alpha=None, seam_beta=None, seam_q=None,
              S_init=None, family="gated_delta", want_o=True, out=None, o_out=None, stream=None):
-    """Fused seam advance + compose.  Seam tokens [B, n-1, w, H, d]; returns (S_out, o [B, n-1, w, H, d])."""
+    """Fused seam advance + compose.  Seam tokens [B, n-1, w, H, d]; returns (S_out, o [B, n-1, w, H, d]).
+
+    The pools are fp32, or bf16 as written by pairs_to_bf16 (hypic_assemble_bf16)."""
     lib = L.load()
-    _cuda(pool_S, "pool_S", torch.float32), _cuda(pool_T, "pool_T", torch.float32)
+    lp = _pool_dtype(pool_T, pool_S)
     _cuda(idx, "idx", torch.int32)
     P, H, d, _ = pool_S.shape
     B, n = idx.shape
@@ -199,10 +225,10 @@ def assemble(pool_T, pool_S, idx, seam_k, seam_v, seam_alpha=None, seam_beta=Non
         o = o_out if o_out is not None else torch.empty((B, n - 1, w, H, d), device=pool_S.device,
                                                         dtype=torch.float32)
     sh = L.shape(H, d, family, in_dtype)
-    st = lib.hypic_assemble(ctypes.byref(sh), B, n, w, _p(idx), P, _p(pool_T), _p(pool_S),
-                            _p(seam_q if o is not None else None), _p(seam_k), _p(seam_v), _p(seam_alpha),
-                            _p(seam_beta), _p(S_init), _p(S_out), _p(o), _stream(stream))
-    L.check(st, "hypic_assemble")
+    fn, name = (lib.hypic_assemble_bf16, "hypic_assemble_bf16") if lp else (lib.hypic_assemble, "hypic_assemble")
+    st = fn(ctypes.byref(sh), B, n, w, _p(idx), P, _p(pool_T), _p(pool_S), _p(seam_q if o is not None else None),
+            _p(seam_k), _p(seam_v), _p(seam_alpha), _p(seam_beta), _p(S_init), _p(S_out), _p(o), _stream(stream))
+    L.check(st, name)
     return S_out, o
 
 

@@ -201,12 +201,15 @@ hypic_status hypic_seam_advance(const hypic_shape *sh, int32_t B, float *S_inout
 }
 
 static hypic_status chain_common(const hypic_shape *sh, int32_t B, int32_t n, int32_t w, const int32_t *idx,
-                                 int64_t pool_size, const float *pool_T, const float *pool_S,
+                                 int64_t pool_size, const void *pool_T, const void *pool_S, bool pair_bf16,
                                  const void *seam_q, const void *seam_k, const void *seam_v,
                                  const float *seam_alpha, const float *seam_beta, const float *S_init,
                                  float *S_out, float *o_out, cudaStream_t st) {
   hypic_status r = check_shape(sh);
   if (r != HYPIC_OK) return r;
+  // bf16 pools: delta families only on the d = 128 tensor-core chain
+  const bool dense = sh->family == HYPIC_FAM_DELTA || sh->family == HYPIC_FAM_GATED_DELTA;
+  if (pair_bf16 && dense && sh->d_k != 128) return HYPIC_EUNSUPPORTED;
   if (B < 0 || n < 0 || w < 0 || pool_size < 0) return HYPIC_EINVAL;
   if (B == 0 || sh->H == 0) return HYPIC_OK;
   if (!ok_ptr(S_out) || !ok_opt(S_init) || !ok_opt(o_out)) return HYPIC_EINVAL;
@@ -230,6 +233,7 @@ static hypic_status chain_common(const hypic_shape *sh, int32_t B, int32_t n, in
   a.pool_size = pool_size;
   a.pool_T = pool_T;
   a.pool_S = pool_S;
+  a.pair_bf16 = pair_bf16 ? 1 : 0;
   a.S_init = S_init;
   a.S_out = S_out;
   a.scan = 0;
@@ -242,7 +246,14 @@ static hypic_status chain_common(const hypic_shape *sh, int32_t B, int32_t n, in
 hypic_status hypic_compose(const hypic_shape *sh, int32_t B, int32_t n, const int32_t *idx, int64_t pool_size,
                            const float *pool_T, const float *pool_S, const float *S_init, float *S_out,
                            hypic_stream_t stream) {
-  return chain_common(sh, B, n, 0, idx, pool_size, pool_T, pool_S, nullptr, nullptr, nullptr, nullptr,
+  return chain_common(sh, B, n, 0, idx, pool_size, pool_T, pool_S, false, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, S_init, S_out, nullptr, (cudaStream_t)stream);
+}
+
+hypic_status hypic_compose_bf16(const hypic_shape *sh, int32_t B, int32_t n, const int32_t *idx,
+                                int64_t pool_size, const void *pool_T, const void *pool_S, const float *S_init,
+                                float *S_out, hypic_stream_t stream) {
+  return chain_common(sh, B, n, 0, idx, pool_size, pool_T, pool_S, true, nullptr, nullptr, nullptr, nullptr,
                       nullptr, S_init, S_out, nullptr, (cudaStream_t)stream);
 }
 
@@ -251,8 +262,29 @@ hypic_status hypic_assemble(const hypic_shape *sh, int32_t B, int32_t n, int32_t
                             const void *seam_k, const void *seam_v, const float *seam_alpha,
                             const float *seam_beta, const float *S_init, float *S_out, float *o_out,
                             hypic_stream_t stream) {
-  return chain_common(sh, B, n, w, idx, pool_size, pool_T, pool_S, seam_q, seam_k, seam_v, seam_alpha,
+  return chain_common(sh, B, n, w, idx, pool_size, pool_T, pool_S, false, seam_q, seam_k, seam_v, seam_alpha,
                       seam_beta, S_init, S_out, o_out, (cudaStream_t)stream);
+}
+
+hypic_status hypic_assemble_bf16(const hypic_shape *sh, int32_t B, int32_t n, int32_t w, const int32_t *idx,
+                                 int64_t pool_size, const void *pool_T, const void *pool_S, const void *seam_q,
+                                 const void *seam_k, const void *seam_v, const float *seam_alpha,
+                                 const float *seam_beta, const float *S_init, float *S_out, float *o_out,
+                                 hypic_stream_t stream) {
+  return chain_common(sh, B, n, w, idx, pool_size, pool_T, pool_S, true, seam_q, seam_k, seam_v, seam_alpha,
+                      seam_beta, S_init, S_out, o_out, (cudaStream_t)stream);
+}
+
+hypic_status hypic_pairs_to_bf16(const hypic_shape *sh, int64_t n_pairs, const float *T, const float *S,
+                                 void *T_lp, void *S_lp, hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (n_pairs < 0) return HYPIC_EINVAL;
+  if (n_pairs == 0 || sh->H == 0) return HYPIC_OK;
+  if (!ok_ptr(T) || !ok_ptr(S) || !ok_ptr(T_lp) || !ok_ptr(S_lp)) return HYPIC_EINVAL;
+  const int64_t t_elems = n_pairs * sh->H * hypic_t_size(sh);
+  const int64_t s_elems = n_pairs * sh->H * (int64_t)sh->d_k * sh->d_v;
+  return from_cuda(launch_pairs_to_bf16(T, S, T_lp, S_lp, t_elems, s_elems, (cudaStream_t)stream));
 }
 
 hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T, const float *S,
@@ -278,6 +310,7 @@ hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T,
   a.pool_size = n;
   a.pool_T = T;
   a.pool_S = S;
+  a.pair_bf16 = 0;
   a.S_init = nullptr;
   a.S_out = nullptr;
   a.scan = 1;

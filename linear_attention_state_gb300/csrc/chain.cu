@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_dense_kernel(ChainArgs a) {
     else if (!a.scan && a.S_init) v0 = a.S_init[((size_t)b * H + h) * DD + e];
     S[e] = v0;
   }
-  if (a.n > 0) stage_T<D>(Tb, a.pool_T + ((size_t)pool_entry(a, b, 0) * H + h) * DD, tid);
+  const float *poolT = static_cast<const float *>(a.pool_T), *poolS = static_cast<const float *>(a.pool_S);
+  if (a.n > 0) stage_T<D>(Tb, poolT + ((size_t)pool_entry(a, b, 0) * H + h) * DD, tid);
   cp_async_commit();
 
   for (int j = 0; j < a.n; ++j) {
@@ -145,11 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_dense_kernel(ChainArgs a) {
     cp_async_wait_all();
     __syncthreads();
     if (j + 1 < a.n)
-      stage_T<D>(Tb + ((j + 1) & 1) * DD, a.pool_T + ((size_t)pool_entry(a, b, j + 1) * H + h) * DD, tid);
+      stage_T<D>(Tb + ((j + 1) & 1) * DD, poolT + ((size_t)pool_entry(a, b, j + 1) * H + h) * DD, tid);
     cp_async_commit();
 
     float add[TM][TM];
-    const float *S0 = a.pool_S + ((size_t)p * H + h) * DD;
+    const float *S0 = poolS + ((size_t)p * H + h) * DD;
 #pragma unroll
     for (int r = 0; r < TM; ++r) {
       if constexpr (TM % 4 == 0) {
@@ -235,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_dense_kernel(ChainArgs a) {
   }
 }
 
-// Scalar and diagonal families: column-per-thread chain, HBM-bound.
-template <int D, typename Tin>
+// Scalar and diagonal families: column-per-thread chain, HBM-bound.  Pairs are fp32 or bf16 (Tp).
+template <int D, typename Tin, typename Tp>
 __global__ void __launch_bounds__(D >= 64 ? 64 : D) chain_diag_kernel(ChainArgs a) {
   constexpr int TPC = D >= 64 ? 64 : D;
   constexpr int NCB = D / TPC;
@@ -288,12 +289,12 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) chain_diag_kernel(ChainArgs 
       }
     }
     __syncthreads();
-    const float *Tp = a.pool_T + ((size_t)p * H + h) * ts;
-    for (int i = tid; i < D; i += TPC) st[i] = diag ? Tp[i] : Tp[0];
+    const Tp *Tq = static_cast<const Tp *>(a.pool_T) + ((size_t)p * H + h) * ts;
+    for (int i = tid; i < D; i += TPC) st[i] = to_f32<Tp>(diag ? Tq[i] : Tq[0]);
     __syncthreads();
-    const float *S0 = a.pool_S + ((size_t)p * H + h) * DD;
+    const Tp *S0 = static_cast<const Tp *>(a.pool_S) + ((size_t)p * H + h) * DD;
 #pragma unroll
-    for (int i = 0; i < D; ++i) x[i] = fmaf(st[i], x[i], __ldg(S0 + (size_t)i * D + j));
+    for (int i = 0; i < D; ++i) x[i] = fmaf(st[i], x[i], to_f32<Tp>(S0[(size_t)i * D + j]));
     if (a.scan) {
       tp *= st[diag ? j : 0];
       float *rec = a.S_rec + ((size_t)jj * H + h) * DD;
@@ -313,6 +314,7 @@ template <int D, typename Tin>
 cudaError_t launch_d(const ChainArgs &a, cudaStream_t st) {
   const bool dense = a.fam == HYPIC_FAM_DELTA || a.fam == HYPIC_FAM_GATED_DELTA;
   if (dense) {
+    if (a.pair_bf16) return cudaErrorInvalidValue;  // rejected by the API before any launch
     const long long blocks = (long long)a.B * a.H * (a.scan ? 2 : 1);
     if (blocks <= 0) return cudaSuccess;
     const size_t smem = sizeof(float) * (3 * D * D + 3 * D + kThreads + 2);
@@ -324,7 +326,8 @@ cudaError_t launch_d(const ChainArgs &a, cudaStream_t st) {
     constexpr int TPC = D >= 64 ? 64 : D;
     const long long blocks = (long long)a.B * a.H * (D / TPC);
     if (blocks <= 0) return cudaSuccess;
-    chain_diag_kernel<D, Tin><<<(unsigned)blocks, TPC, 0, st>>>(a);
+    if (a.pair_bf16) chain_diag_kernel<D, Tin, __nv_bfloat16><<<(unsigned)blocks, TPC, 0, st>>>(a);
+    else chain_diag_kernel<D, Tin, float><<<(unsigned)blocks, TPC, 0, st>>>(a);
   }
   return cudaGetLastError();
 }

@@ -70,8 +70,9 @@ struct ChainArgs {
   int B, n, w;
   const int32_t *idx;  // [B, n] or null: step j of chain uses pool entry j
   int64_t pool_size;
-  const float *pool_T;  // [P, H, t_size]
-  const float *pool_S;  // [P, H, D, D]
+  const void *pool_T;  // [P, H, t_size]  fp32, or bf16 when pair_bf16
+  const void *pool_S;  // [P, H, D, D]     same element type
+  int pair_bf16;
   const float *S_init;  // [B, H, D, D] or null
   float *S_out;         // final [B, H, D, D]
   // scan mode: record every prefix; T half of the augmented state goes to T_rec
@@ -87,6 +88,10 @@ cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st);
 // tcgen05 composition chain (d = 128, delta families): compose, assemble and scan.
 bool compose_tc_supported(int D, int fam);
 cudaError_t launch_compose_tc(const ChainArgs &a, cudaStream_t st);
+
+// fp32 pairs -> bf16 storage, round to nearest even (element counts; 16-byte aligned pointers).
+cudaError_t launch_pairs_to_bf16(const float *T, const float *S, void *T_lp, void *S_lp, int64_t t_elems,
+                                 int64_t s_elems, cudaStream_t st);
 
 // Bounded-wait self-test (see hypic_selftest_bounded_wait).
 cudaError_t launch_bounded_wait_selftest(long long limit_cycles, int *err, cudaStream_t st);

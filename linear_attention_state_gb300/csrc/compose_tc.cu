@@ -19,6 +19,11 @@
 // column in registers (k . S_j, rank-1 update, q . S_j), and splits the column into the three
 // A pieces for the next step.  Grid order is head-major, so the requests that share a head's
 // pool entries run together and re-read them from L2.
+//
+// Pairs stored in bf16 (16-bit cache storage, Method 3 Table 3 sizes): T is then an exact bf16
+// B operand, so TMA lands it directly in the swizzled K-major layout the MMA reads (double
+// buffered: the next step's T loads while this step runs), only the three products
+// hi.T + mid.T + lo.T remain, and S_{C|0} is staged in bf16 and added in fp32.
 #include <cuda_bf16.h>
 
 #include "tc_ptx.cuh"
@@ -33,10 +38,15 @@ constexpr int D = 128;
 constexpr int NT = 256;
 constexpr int R = 64;  // rows of the column each thread owns
 
+// fp32 pairs
 constexpr uint32_t OFF_TST = 0;                 // T staging, fp32, 4 boxes [128 i][32 k] swizzled
 constexpr uint32_t OFF_TB = 65536;              // 3 pieces x 2 k-blocks x [128 i][64 k] bf16 (K-major B)
 constexpr uint32_t OFF_S0 = OFF_TB + 3 * 32768;  // S0 staging, fp32 [128 i][128 j], row-major
 constexpr uint32_t SMEM_BYTES = OFF_S0 + 65536 + 1024;
+// bf16 pairs
+constexpr uint32_t OFF_TB16 = 0;       // 2 buffers x 2 k-blocks x [128 i][64 k] bf16 (K-major B), by TMA
+constexpr uint32_t OFF_S016 = 65536;   // S0 staging, bf16 [128 i][128 j], row-major
+constexpr uint32_t SMEM_BYTES16 = OFF_S016 + 32768 + 1024;
 
 constexpr uint32_t TM_D = 0;    // accumulator D = S_new^T: lanes j, columns i
 constexpr uint32_t TM_A = 128;  // three A pieces of S^T, 64 columns each (two bf16 per column)
@@ -89,18 +99,18 @@ __device__ __forceinline__ float ld_tok(const void *p, size_t i) {
   return to_f32<Tin>(static_cast<const Tin *>(p)[i]);
 }
 
-template <typename Tin>
+template <typename Tin, bool PB>
 __global__ void __launch_bounds__(NT, 1)
     compose_tc_kernel(const __grid_constant__ CUtensorMap mapT, const __grid_constant__ CUtensorMap mapS,
                       ComposeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_t, bar_s, bar_m;
+  __shared__ uint64_t bar_t[2], bar_s, bar_m;  // bar_t[1]: second T buffer (bf16 pairs)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float red[2][D];  // partial column dot products of the two row halves
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
-  float *sS0 = reinterpret_cast<float *>(sm + OFF_S0);
+  float *sS0 = reinterpret_cast<float *>(sm + (PB ? OFF_S016 : OFF_S0));
   const int tid = threadIdx.x, warp = tid / 32;
   const int H = a.H;
   int b, h;
@@ -132,18 +142,27 @@ __global__ void __launch_bounds__(NT, 1)
   };
   auto issue_T = [&](int step) {
     const int row = (int)((entry(step) * H + h) * D);
-    mbar_arrive_expect_tx(&bar_t, 65536);
+    if (PB) {
+      const int buf = step & 1;
+      mbar_arrive_expect_tx(&bar_t[buf], 32768);
 #pragma unroll
-    for (int kb = 0; kb < 4; ++kb) tma_load_2d(sm + OFF_TST + kb * 16384, &mapT, &bar_t, kb * 32, row);
+      for (int kb = 0; kb < 2; ++kb)
+        tma_load_2d(sm + OFF_TB16 + buf * 32768 + kb * 16384, &mapT, &bar_t[buf], kb * 64, row);
+    } else {
+      mbar_arrive_expect_tx(&bar_t[0], 65536);
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) tma_load_2d(sm + OFF_TST + kb * 16384, &mapT, &bar_t[0], kb * 32, row);
+    }
   };
   auto issue_S = [&](int step) {
     const int row = (int)((entry(step) * H + h) * D);
-    mbar_arrive_expect_tx(&bar_s, 65536);
-    tma_load_2d(sm + OFF_S0, &mapS, &bar_s, 0, row);
+    mbar_arrive_expect_tx(&bar_s, PB ? 32768 : 65536);
+    tma_load_2d(sm + (PB ? OFF_S016 : OFF_S0), &mapS, &bar_s, 0, row);
   };
 
   if (tid == 0) {
-    mbar_init(&bar_t, 1);
+    mbar_init(&bar_t[0], 1);
+    mbar_init(&bar_t[1], 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_m, 1);
     mbar_fence_init();
@@ -203,12 +222,16 @@ __global__ void __launch_bounds__(NT, 1)
 
   for (int step = 0; step < a.n; ++step) {
     // (1) T of this step: fp32 staging -> three bf16 B pieces [128 i][128 k], K-major, swizzled.
-    // Thread (row i, half) converts k in [64 half, 64 half + 64).
-    if (tid == 0 && !mbar_wait_cycles(&bar_t, ph, a.err)) abort_flag = 1;
+    // Thread (row i, half) converts k in [64 half, 64 half + 64).  bf16 pairs: already in place.
+    if (tid == 0) {
+      const bool got = PB ? mbar_wait_cycles(&bar_t[step & 1], (uint32_t)(step >> 1) & 1u, a.err)
+                          : mbar_wait_cycles(&bar_t[0], ph, a.err);
+      if (!got) abort_flag = 1;
+    }
     tc_fence_before();
     __syncthreads();
     if (abort_flag) break;
-    {
+    if (!PB) {
       const uint32_t i = (uint32_t)j;
 #pragma unroll
       for (int kq = 0; kq < 2; ++kq) {
@@ -236,17 +259,31 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      if (step + 1 < a.n) issue_T(step + 1);  // the staging buffer is consumed
-      // (2) D = S^T T^T with six split products (A piece, B piece), smallest first:
-      // (2,0) (1,1) (0,2) (1,0) (0,1) (0,0).
-      const int pa[6] = {2, 1, 0, 1, 0, 0}, pb[6] = {0, 1, 2, 0, 1, 0};
+      // fp32: the staging buffer is consumed.  bf16: the other buffer's MMAs (step - 1) are done.
+      if (step + 1 < a.n) issue_T(step + 1);
+      if (PB) {
+        // (2) D = S^T T^T with three products (A piece, exact T), smallest first: lo, mid, hi.
 #pragma unroll
-      for (int pr = 0; pr < 6; ++pr) {
+        for (int pr = 0; pr < 3; ++pr) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t bo = OFF_TB + pb[pr] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_tmem_a(tmem + TM_D, tmem + TM_A + pa[pr] * 64 + kk * 8, sdesc_sw128(sb + bo, 16, 1024), idesc,
-                         (pr | kk) != 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t bo = OFF_TB16 + (step & 1) * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16_tmem_a(tmem + TM_D, tmem + TM_A + (2 - pr) * 64 + kk * 8, sdesc_sw128(sb + bo, 16, 1024),
+                           idesc, (pr | kk) != 0);
+          }
+        }
+      } else {
+        // (2) D = S^T T^T with six split products (A piece, B piece), smallest first:
+        // (2,0) (1,1) (0,2) (1,0) (0,1) (0,0).
+        const int pa[6] = {2, 1, 0, 1, 0, 0}, pb[6] = {0, 1, 2, 0, 1, 0};
+#pragma unroll
+        for (int pr = 0; pr < 6; ++pr) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t bo = OFF_TB + pb[pr] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16_tmem_a(tmem + TM_D, tmem + TM_A + pa[pr] * 64 + kk * 8, sdesc_sw128(sb + bo, 16, 1024),
+                           idesc, (pr | kk) != 0);
+          }
         }
       }
       mma_commit(&bar_m);
@@ -260,8 +297,14 @@ __global__ void __launch_bounds__(NT, 1)
     // (3) Epilogue: rows i0.. of column j of S_new = D row j (+ S_{C|0}).
     tmem_ld64(tmem + lane_base + TM_D + i0, x);
     if (addend) {
+      if (PB) {
+        const __nv_bfloat16 *s0b = reinterpret_cast<const __nv_bfloat16 *>(sS0);
 #pragma unroll
-      for (int r = 0; r < R; ++r) x[r] += sS0[(i0 + r) * D + j];
+        for (int r = 0; r < R; ++r) x[r] += __bfloat162float(s0b[(i0 + r) * D + j]);
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) x[r] += sS0[(i0 + r) * D + j];
+      }
     }
     if (a.scan) {
       float *rec = (isT ? a.T_rec : a.S_rec) + ((size_t)step * H + h) * D * D;
@@ -329,7 +372,12 @@ __global__ void __launch_bounds__(NT, 1)
   }
   if (abort_flag && tid == 0) {
     mbar_wait_cycles(&bar_m, ph, nullptr, 200000000LL);
-    mbar_wait_cycles(&bar_t, ph, nullptr, 200000000LL);
+    mbar_wait_cycles(&bar_t[0], PB ? 0u : ph, nullptr, 200000000LL);
+    if (PB) {
+      mbar_wait_cycles(&bar_t[0], 1u, nullptr, 200000000LL);
+      mbar_wait_cycles(&bar_t[1], 0u, nullptr, 200000000LL);
+      mbar_wait_cycles(&bar_t[1], 1u, nullptr, 200000000LL);
+    }
     mbar_wait_cycles(&bar_s, ph, nullptr, 200000000LL);
   }
   tc_fence_before();
@@ -343,20 +391,38 @@ bool compose_tc_supported(int D_, int fam) {
   return D_ == D && (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
 }
 
+template <typename Tin, bool PB>
+cudaError_t launch_one(const CUtensorMap &mT, const CUtensorMap &mS, const ComposeTcArgs &a, long long blocks,
+                       cudaStream_t st) {
+  const uint32_t smem = PB ? SMEM_BYTES16 : SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel<Tin, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  compose_tc_kernel<Tin, PB><<<(unsigned)blocks, NT, smem, st>>>(mT, mS, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
   const uint64_t rows = (uint64_t)c.pool_size * c.H * D;
   if (rows >= ((uint64_t)1 << 31)) return cudaErrorInvalidValue;
+  const bool pb = c.pair_bf16 != 0;
   CUtensorMap mT, mS;
-  if (!make_tmap_f32_2d(&mT, c.pool_T, rows, D, D, 32, 128)) return cudaErrorInvalidValue;
+  if (pb) {
+    if (!make_tmap_bf16_2d(&mT, c.pool_T, rows, D, D, 64, 128)) return cudaErrorInvalidValue;
+  } else if (!make_tmap_f32_2d(&mT, c.pool_T, rows, D, D, 32, 128)) {
+    return cudaErrorInvalidValue;
+  }
   {
+    // S_{C|0} as one [128][128] box, no swizzle, row-major in shared memory.
     auto fn = tma_encode_fn();
     if (!fn) return cudaErrorInvalidValue;
+    const uint32_t es = pb ? 2 : 4;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    cuuint64_t strides[1] = {(cuuint64_t)D * es};
     cuuint32_t box[2] = {128, 128};
     cuuint32_t estr[2] = {1, 1};
-    if (fn(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(c.pool_S), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (fn(&mS, pb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+           const_cast<void *>(c.pool_S), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -385,18 +451,11 @@ cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
   const long long blocks = c.scan ? (long long)c.H * 2 : (long long)c.B * c.H;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaError_t e;
   if (a.seam_bf16) {
-    e = cudaFuncSetAttribute(compose_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    compose_tc_kernel<__nv_bfloat16><<<(unsigned)blocks, NT, SMEM_BYTES, st>>>(mT, mS, a);
-  } else {
-    e = cudaFuncSetAttribute(compose_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    compose_tc_kernel<float><<<(unsigned)blocks, NT, SMEM_BYTES, st>>>(mT, mS, a);
+    return pb ? launch_one<__nv_bfloat16, true>(mT, mS, a, blocks, st)
+              : launch_one<__nv_bfloat16, false>(mT, mS, a, blocks, st);
   }
-  return cudaGetLastError();
+  return pb ? launch_one<float, true>(mT, mS, a, blocks, st) : launch_one<float, false>(mT, mS, a, blocks, st);
 }
 
 }  // namespace hypic

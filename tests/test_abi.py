@@ -168,3 +168,21 @@ def test_build_workspace_contract(lib):
     assert r == L.HYPIC_ENOSPACE
     r = lib.hypic_segment_build(ctypes.byref(sh), p, p, None, p, p, 4096, p, p, None, None, 0, None)
     assert r == L.HYPIC_ENOSPACE
+
+
+def test_bf16_pair_storage_validation(lib):
+    p = _fake()
+    mis = _fake(0x10004)
+    # the delta families take bf16 pools on the d = 128 tensor-core chain only: rejected on the host
+    sh64 = L.shape(2, 64, "gated_delta", "f32")
+    assert lib.hypic_compose_bf16(ctypes.byref(sh64), 1, 2, p, 4, p, p, None, p, None) == L.HYPIC_EUNSUPPORTED
+    assert lib.hypic_assemble_bf16(ctypes.byref(sh64), 1, 2, 0, p, 4, p, p, None, None, None, None, None, None, p,
+                                   None, None) == L.HYPIC_EUNSUPPORTED
+    sh = L.shape(2, 128, "gated_delta", "f32")
+    assert lib.hypic_compose_bf16(ctypes.byref(sh), 1, 2, None, 4, p, p, None, p, None) == L.HYPIC_EINVAL
+    assert lib.hypic_compose_bf16(ctypes.byref(sh), 0, 2, None, 0, None, None, None, None, None) == L.HYPIC_OK
+    # conversion: negative count, misaligned or missing pointers; zero pairs is a no-op
+    assert lib.hypic_pairs_to_bf16(ctypes.byref(sh), -1, p, p, p, p, None) == L.HYPIC_EINVAL
+    assert lib.hypic_pairs_to_bf16(ctypes.byref(sh), 3, p, mis, p, p, None) == L.HYPIC_EINVAL
+    assert lib.hypic_pairs_to_bf16(ctypes.byref(sh), 3, p, p, None, p, None) == L.HYPIC_EINVAL
+    assert lib.hypic_pairs_to_bf16(ctypes.byref(sh), 0, None, None, None, None, None) == L.HYPIC_OK

@@ -315,6 +315,42 @@ def scan_measure(steps, warmup, dev, peaks):
     return res
 
 
+def boundary_measure(steps, warmup, dev, peaks):
+    """Boundary patches, HBM-bound: RoPE shift of one 32k-token segment's keys (8 heads x 128
+    dims, bf16, out of place) and re-rotation of 2,048 scalar-family states (64 segments x 32
+    heads, 128 x 128 fp32, in place).  Bytes are one read and one write of each tensor."""
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    g = torch.Generator(device=dev)
+    g.manual_seed(881)
+    K = torch.randn((32768, 8, 128), device=dev, generator=g).to(torch.bfloat16)
+    K_out = torch.empty_like(K)
+    S = torch.randn((64, 32, 128, 128), device=dev, generator=g)
+    out = {}
+    for name, fn_call, nbytes in (
+            ("rope_shift_32768x8x128_bf16", lambda: hy.rope_shift(K, 70_001, base=1e6, out=K_out), 2 * K.numel() * 2),
+            ("state_rerotate_64x32_128x128_fp32", lambda: hy.state_rerotate(S, 70_001, base=1e6, family="scalar"),
+             2 * S.numel() * 4)):
+        def fn(ev, f=fn_call):
+            if ev is not None:
+                ev[0].record()
+            f()
+            if ev is not None:
+                ev[1].record()
+                ev[2].record()
+
+        _, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+        avg = sum(k1) / len(k1) / 1e3
+        out[name] = {"ms": avg * 1e3, "roofline": {"bound": "hbm", "achieved": nbytes / avg / 1e9,
+                                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                                    "frac": nbytes / avg / 1e9 / peaks["hbm_gbs"], "traffic": None}}
+    out["status"] = hy.stream_status()
+    del K, K_out, S
+    torch.cuda.empty_cache()
+    return out
+
+
 def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False, storage="both"):
     """Warm-cache composition: 30 layers x 32 heads, pool of 256 pairs, 64 requests x 16 segments.
 
@@ -408,6 +444,8 @@ def main():
                     help="time only the decay-family builds (profiling aid; prints its own line)")
     ap.add_argument("--scan-only", action="store_true",
                     help="time only the affine scan (profiling aid; prints its own line)")
+    ap.add_argument("--boundary-only", action="store_true",
+                    help="time only the boundary patches (profiling aid; prints its own line)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -447,11 +485,13 @@ def main():
                               "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
                               "warmup": args.warmup, "compose_pool": res}))
         return
-    if args.decay_only or args.scan_only:
-        res = (decay_build_measure if args.decay_only else scan_measure)(args.steps, args.warmup, dev, peaks)
+    if args.decay_only or args.scan_only or args.boundary_only:
+        fn, what = ((decay_build_measure, "decay-family builds") if args.decay_only else
+                    (scan_measure, "affine scan") if args.scan_only else (boundary_measure, "boundary patches"))
+        res = fn(args.steps, args.warmup, dev, peaks)
         if rank == 0:
-            print(json.dumps({"metric": "decay-family builds" if args.decay_only else "affine scan",
-                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "result": res}))
+            print(json.dumps({"metric": what, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "result": res}))
         return
     req = RequestStep(w, dev)
     status0 = hy.stream_status()
@@ -503,10 +543,11 @@ def main():
     e2e_ms, _, _ = run_timed(e2e_step, args.steps, min(args.warmup, 3), sync_all, kernel_events=False)
     e2e_value = req.tokens * world / (e2e_ms / 1e3 / args.steps)
 
-    decay = scan = None
+    decay = scan = bnd = None
     if not args.no_compose:
         decay = decay_build_measure(args.steps, args.warmup, dev, peaks)
         scan = scan_measure(args.steps, args.warmup, dev, peaks)
+        bnd = boundary_measure(args.steps, args.warmup, dev, peaks)
     compose = None
     if not args.no_compose:
         del host
@@ -539,6 +580,7 @@ def main():
             "compose_pool": compose,
             "decay_builds": decay,
             "affine_scan": scan,
+            "boundary_patches": bnd,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": req.launches_per_step * args.steps,

@@ -245,6 +245,57 @@ hypic_status hypic_assemble_bf16(const hypic_shape *shape, int32_t B, int32_t n,
                                  const void *seam_v, const float *seam_alpha, const float *seam_beta,
                                  const float *S_init, float *S_out, float *o_out, hypic_stream_t stream);
 
+/* ---- Boundary patches (HYPIC notes, Method 6: causal convolution and RoPE at segment
+ * boundaries; paper Sec. 4.2-4.3, Eqs. (7), (8)).  None allocates; all are asynchronous on
+ * `stream`; pointers are caller-owned device memory, 16-byte aligned. */
+
+typedef enum { HYPIC_ACT_IDENTITY = 0, HYPIC_ACT_SILU = 1 } hypic_activation;
+
+/*
+ * RoPE key shift, Eq. (8): K_b = R(b - a) K_a, for keys cached at one start position and reused
+ * at another (delta = b - a, any sign).  K_in, K_out [n_rows, d] (n_rows = tokens x heads),
+ * dtype HYPIC_F32 or HYPIC_BF16, K_out may equal K_in.  Rotate-half convention: dims i and
+ * i + rot_dim/2 (i < rot_dim/2) form a pair turned by delta * base^(-2i/rot_dim); dims >=
+ * rot_dim pass through.  2 <= rot_dim <= d <= 512, rot_dim even, base > 1.  The angle is
+ * reduced modulo 2 pi in double precision, the rotation applied in fp32 (bf16 outputs are
+ * rounded to nearest even).  Errors: HYPIC_EINVAL (pointers, sizes), HYPIC_ECUDA.
+ */
+hypic_status hypic_rope_shift(int64_t n_rows, int32_t d, int32_t rot_dim, double base, int64_t delta,
+                              hypic_dtype dtype, const void *K_in, void *K_out, hypic_stream_t stream);
+
+/*
+ * Linear-layer state re-rotation, Eq. (7): S_{C|b} = R(b - a) S_{C|a} applied to the key (row)
+ * index of S [n, H, d_k, d_v] fp32, in place; T_C is unchanged.  Exact only when the transition
+ * commutes with the rotation, so only the scalar families are accepted (HYPIC_FAM_SCALAR_CONST,
+ * HYPIC_FAM_SCALAR); others return HYPIC_EUNSUPPORTED.  Rotation as in hypic_rope_shift, with
+ * rot_dim <= d_k.
+ */
+hypic_status hypic_state_rerotate(const hypic_shape *shape, int64_t n, float *S_inout, int32_t rot_dim,
+                                  double base, int64_t delta, hypic_stream_t stream);
+
+/*
+ * Causal-convolution tail of each segment body (what the cache keeps so that the next
+ * segment's first k - 1 conv outputs can be recomputed): tail_out [n_seg, k-1, C] = rows
+ * end-(k-1) .. end-1 of x [n_tokens, C] for body [begin, end) = seg_bounds[s] (device, int64
+ * [n_seg][2]), zero where a row falls before begin.  dtype of x and tail_out: HYPIC_F32 or
+ * HYPIC_BF16.  1 <= k <= 64.  Bad bounds are recorded as HYPIC_EDEVICE (hypic_stream_status)
+ * and give zero rows.
+ */
+hypic_status hypic_conv_tail(int32_t C, int32_t k, int32_t n_seg, const int64_t *seg_bounds, int64_t n_tokens,
+                             hypic_dtype dtype, const void *x, void *tail_out, hypic_stream_t stream);
+
+/*
+ * Depthwise causal convolution over the first w tokens of B segments, continuing from each
+ * previous segment's tail:
+ *   y[b, t, c] = act(bias[c] + sum_{j<k} weight[c, j] * x_{t-k+1+j}[c]),
+ * where x_s = x_seam[b, s] for s >= 0 and tail[b, k-1+s] for s < 0.  x_seam [B, w, C] and tail
+ * [B, k-1, C] in dtype (HYPIC_F32 or HYPIC_BF16; tail may be NULL when k == 1), weight [C, k]
+ * and bias [C] (or NULL) fp32, y_out [B, w, C] fp32.  act: hypic_activation.  1 <= k <= 64.
+ */
+hypic_status hypic_conv_seam(int32_t B, int32_t w, int32_t C, int32_t k, hypic_dtype dtype, const void *x_seam,
+                             const void *tail, const float *weight, const float *bias, int32_t act, float *y_out,
+                             hypic_stream_t stream);
+
 /*
  * Waits for `stream`, then returns and clears the status word of the current
  * device: HYPIC_OK, HYPIC_EDEVICE or HYPIC_ETIMEOUT (first error recorded by

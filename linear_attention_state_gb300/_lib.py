@@ -45,6 +45,10 @@ SIGNATURES = {
     "hypic_compose_bf16": (_i32, [_SP, _i32, _i32, _i32p, _i64, _vp, _vp, _fp, _fp, _vp]),
     "hypic_assemble_bf16": (_i32, [_SP, _i32, _i32, _i32, _i32p, _i64, _vp, _vp, _vp, _vp, _vp, _fp, _fp, _fp,
                                    _fp, _fp, _vp]),
+    "hypic_rope_shift": (_i32, [_i64, _i32, _i32, ctypes.c_double, _i64, _i32, _vp, _vp, _vp]),
+    "hypic_state_rerotate": (_i32, [_SP, _i64, _fp, _i32, ctypes.c_double, _i64, _vp]),
+    "hypic_conv_tail": (_i32, [_i32, _i32, _i32, _i64p, _i64, _i32, _vp, _vp, _vp]),
+    "hypic_conv_seam": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _fp, _fp, _i32, _fp, _vp]),
     "hypic_stream_status": (_i32, [_vp]),
     "hypic_selftest_bounded_wait": (_i32, [_i64, _vp]),
 }

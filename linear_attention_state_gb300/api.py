@@ -232,6 +232,73 @@ def assemble(pool_T, pool_S, idx, seam_k, seam_v, seam_alpha=None, seam_beta=Non
     return S_out, o
 
 
+# ---- boundary patches (HYPIC notes, Method 6; paper Eqs. (7), (8)) ------------------------
+
+_ACT = {"identity": 0, "silu": 1}
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise ValueError(f"expected float32 or bfloat16, got {t.dtype}")
+
+
+def rope_shift(K, delta, rot_dim=None, base=10000.0, out=None, stream=None):
+    """K_b = R(delta) K_a on the last axis of K [..., d] (rotate-half pairs, rot_dim dims rotated)."""
+    lib = L.load()
+    _cuda(K, "K")
+    d = K.shape[-1]
+    rows = K.numel() // d if d else 0
+    out = out if out is not None else torch.empty_like(K)
+    _cuda(out, "out", K.dtype)
+    st = lib.hypic_rope_shift(rows, d, rot_dim or d, float(base), int(delta), _dt(K), _p(K), _p(out), _stream(stream))
+    L.check(st, "hypic_rope_shift")
+    return out
+
+
+def state_rerotate(S, delta, rot_dim=None, base=10000.0, family="scalar", stream=None):
+    """S_{C|b} = R(delta) S_{C|a} in place on the rows of S [n, H, d_k, d_v] (scalar families only)."""
+    lib = L.load()
+    _cuda(S, "S", torch.float32)
+    n, H, dk, dv = S.shape
+    sh = L.shape(H, dk, family, "f32")
+    sh.d_v = dv
+    st = lib.hypic_state_rerotate(ctypes.byref(sh), n, _p(S), rot_dim or dk, float(base), int(delta), _stream(stream))
+    L.check(st, "hypic_state_rerotate")
+    return S
+
+
+def conv_tail(x, bounds, k, stream=None):
+    """Last k - 1 inputs of each body [begin, end) = bounds[s] of x [n_tokens, C] -> [n_seg, k-1, C]."""
+    lib = L.load()
+    _cuda(x, "x"), _cuda(bounds, "bounds", torch.int64)
+    n_tokens, C = x.shape
+    n_seg = bounds.shape[0]
+    tail = torch.zeros((n_seg, max(k - 1, 0), C), device=x.device, dtype=x.dtype)
+    st = lib.hypic_conv_tail(C, k, n_seg, _p(bounds), n_tokens, _dt(x), _p(x), _p(tail), _stream(stream))
+    L.check(st, "hypic_conv_tail")
+    return tail
+
+
+def conv_seam(x_seam, tail, weight, bias=None, act="identity", stream=None):
+    """Causal conv outputs of the first w tokens of B segments: x_seam [B, w, C], tail [B, k-1, C]."""
+    lib = L.load()
+    _cuda(x_seam, "x_seam"), _cuda(weight, "weight", torch.float32)
+    B, w, C = x_seam.shape
+    k = weight.shape[1]
+    if k > 1:
+        _cuda(tail, "tail", x_seam.dtype)
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+    y = torch.empty((B, w, C), device=x_seam.device, dtype=torch.float32)
+    st = lib.hypic_conv_seam(B, w, C, k, _dt(x_seam), _p(x_seam), _p(tail if k > 1 else None), _p(weight), _p(bias),
+                             _ACT[act], _p(y), _stream(stream))
+    L.check(st, "hypic_conv_seam")
+    return y
+
+
 def stream_status(stream=None) -> int:
     """Wait for the stream; return and clear the device status word (0 = no error recorded)."""
     return int(L.load().hypic_stream_status(_stream(stream)))

@@ -322,6 +322,53 @@ hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T,
   return from_cuda(launch_chain(a, (cudaStream_t)stream));
 }
 
+static bool ok_dtype(hypic_dtype d) { return d == HYPIC_F32 || d == HYPIC_BF16; }
+static bool ok_rope(int32_t d, int32_t r, double base) {
+  return d >= 2 && d <= 512 && r >= 2 && r <= d && (r % 2) == 0 && base > 1.0 && base < 1e300;
+}
+
+hypic_status hypic_rope_shift(int64_t n_rows, int32_t d, int32_t rot_dim, double base, int64_t delta,
+                              hypic_dtype dtype, const void *K_in, void *K_out, hypic_stream_t stream) {
+  if (n_rows < 0 || !ok_rope(d, rot_dim, base) || !ok_dtype(dtype)) return HYPIC_EINVAL;
+  if (n_rows == 0) return HYPIC_OK;
+  if (!ok_ptr(K_in) || !ok_ptr(K_out)) return HYPIC_EINVAL;
+  return from_cuda(launch_rope_shift(K_in, K_out, n_rows, d, rot_dim, base, (long long)delta, dtype,
+                                     (cudaStream_t)stream));
+}
+
+hypic_status hypic_state_rerotate(const hypic_shape *sh, int64_t n, float *S_inout, int32_t rot_dim, double base,
+                                  int64_t delta, hypic_stream_t stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (sh->family != HYPIC_FAM_SCALAR_CONST && sh->family != HYPIC_FAM_SCALAR) return HYPIC_EUNSUPPORTED;
+  if (n < 0 || !ok_rope(sh->d_k, rot_dim, base)) return HYPIC_EINVAL;
+  if (n == 0 || sh->H == 0) return HYPIC_OK;
+  if (!ok_ptr(S_inout)) return HYPIC_EINVAL;
+  return from_cuda(launch_state_rerotate(S_inout, n * sh->H, sh->d_k, sh->d_v, rot_dim, base, (long long)delta,
+                                         (cudaStream_t)stream));
+}
+
+hypic_status hypic_conv_tail(int32_t C, int32_t k, int32_t n_seg, const int64_t *seg_bounds, int64_t n_tokens,
+                             hypic_dtype dtype, const void *x, void *tail_out, hypic_stream_t stream) {
+  if (C < 0 || k < 1 || k > 64 || n_seg < 0 || n_tokens < 0 || !ok_dtype(dtype)) return HYPIC_EINVAL;
+  if (n_seg == 0 || C == 0 || k == 1) return HYPIC_OK;
+  if (!ok_ptr(seg_bounds) || !ok_ptr(tail_out) || (n_tokens > 0 && !ok_ptr(x))) return HYPIC_EINVAL;
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  return from_cuda(launch_conv_tail(x, n_tokens, C, k, n_seg, seg_bounds, tail_out, dtype, err, (cudaStream_t)stream));
+}
+
+hypic_status hypic_conv_seam(int32_t B, int32_t w, int32_t C, int32_t k, hypic_dtype dtype, const void *x_seam,
+                             const void *tail, const float *weight, const float *bias, int32_t act, float *y_out,
+                             hypic_stream_t stream) {
+  if (B < 0 || w < 0 || C < 0 || k < 1 || k > 64 || !ok_dtype(dtype)) return HYPIC_EINVAL;
+  if (act != HYPIC_ACT_IDENTITY && act != HYPIC_ACT_SILU) return HYPIC_EINVAL;
+  if (B == 0 || w == 0 || C == 0) return HYPIC_OK;
+  if (!ok_ptr(x_seam) || !ok_ptr(weight) || !ok_opt(bias) || !ok_ptr(y_out)) return HYPIC_EINVAL;
+  if (k > 1 && !ok_ptr(tail)) return HYPIC_EINVAL;
+  return from_cuda(launch_conv_seam(x_seam, tail, weight, bias, B, w, C, k, act, dtype, y_out, (cudaStream_t)stream));
+}
+
 hypic_status hypic_selftest_bounded_wait(int64_t limit_cycles, hypic_stream_t stream) {
   if (limit_cycles < 0 || limit_cycles > 4000000000LL) return HYPIC_EINVAL;
   int *err = nullptr;

@@ -30,7 +30,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-FAMILIES = {"scalar_const": 0, "scalar": 1, "diag": 2, "delta": 3, "gated_delta": 4}
+FAMILIES = {"scalar_const": 0, "scalar": 1, "diag": 2, "delta": 3, "gated_delta": 4, "kda": 5}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hypic_oracle.c")
@@ -70,11 +70,11 @@ def _gates(family, alpha, beta, n, dk):
         alpha = _f64(np.reshape(np.asarray(alpha, dtype=np.float64), (-1,))[:1])
     elif fam == 3:
         alpha = np.ones(1)
-    elif fam == 2:
+    elif fam in (2, 5):
         alpha = _f64(alpha).reshape(n, dk)
     else:
         alpha = _f64(alpha).reshape(n)
-    if fam in (3, 4):
+    if fam in (3, 4, 5):
         beta = _f64(beta).reshape(n)
     else:
         beta = np.zeros(1)

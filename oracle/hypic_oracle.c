@@ -12,7 +12,8 @@
  *     (Motivation 2, paper Eq. (2));
  *   - per-variant T_i, u_i (Method 3, paper Table 1): RetNet/Lightning gamma*I,
  *     Mamba2 a_i*I, GLA diag(g_i) (all with u_i = k_i v_i^T), DeltaNet
- *     I - b k k^T and GDN g_i (I - b k k^T) (both with u_i = b k_i v_i^T);
+ *     I - b k k^T, GDN g_i (I - b k k^T) and KDA (I - b k k^T) diag(g_i)
+ *     (these three with u_i = b k_i v_i^T);
  *   - segment pair T_C = T_m...T_1, S_{C|0} = sum_t T_m...T_{t+1} u_t
  *     (Method 2, "segments as affine maps");
  *   - composition (T_B,B_B) o (T_A,B_A) = (T_B T_A, T_B B_A + B_B) and the
@@ -27,20 +28,20 @@
  * Transition storage by family (the "T_C families" table, paper Table 3):
  *   SCALAR_CONST, SCALAR : one number
  *   DIAG                 : d_k numbers (the diagonal)
- *   DELTA, GATED_DELTA   : dense d_k x d_k
+ *   DELTA, GATED_DELTA, KDA : dense d_k x d_k
  *
  * Gate layout for one head over `len` tokens:
  *   SCALAR_CONST : alpha[0]            (gamma of the head, every token)
  *   SCALAR, GATED_DELTA : alpha[t]
- *   DIAG         : alpha[t*d_k + i]
+ *   DIAG, KDA    : alpha[t*d_k + i]
  *   DELTA        : alpha unused (a = 1)
- *   beta[t] is read by DELTA and GATED_DELTA only.
+ *   beta[t] is read by DELTA, GATED_DELTA and KDA only.
  */
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-enum { FAM_SCALAR_CONST = 0, FAM_SCALAR = 1, FAM_DIAG = 2, FAM_DELTA = 3, FAM_GATED_DELTA = 4 };
+enum { FAM_SCALAR_CONST = 0, FAM_SCALAR = 1, FAM_DIAG = 2, FAM_DELTA = 3, FAM_GATED_DELTA = 4, FAM_KDA = 5 };
 
 int orc_t_size(int fam, int dk)
 {
@@ -79,6 +80,22 @@ static void step(int fam, int dk, int dv, double *S, const double *k,
         for (i = 0; i < dk; i++)
             for (j = 0; j < dv; j++)
                 S[i * dv + j] = a * S[i * dv + j] + (with_write ? k[i] * v[j] : 0.0);
+        return;
+    }
+    if (fam == FAM_KDA) {
+        /* T_t = (I - b k k^T) diag(g_t): first the per-channel gate, then the erase. */
+        const double *g = alpha + t * dk;
+        double b = beta[t];
+        for (i = 0; i < dk; i++)
+            for (j = 0; j < dv; j++) S[i * dv + j] *= g[i];
+        for (j = 0; j < dv; j++) {
+            double acc = 0.0;
+            for (i = 0; i < dk; i++) acc += k[i] * S[i * dv + j];
+            tmp[j] = acc; /* (k^T diag(g) S)_j */
+        }
+        for (i = 0; i < dk; i++)
+            for (j = 0; j < dv; j++)
+                S[i * dv + j] = S[i * dv + j] - b * k[i] * tmp[j] + (with_write ? b * k[i] * v[j] : 0.0);
         return;
     }
     /* DELTA / GATED_DELTA */

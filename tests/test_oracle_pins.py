@@ -36,8 +36,8 @@ import pytest
 import oracle as O
 
 GOLD = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta"]
-DENSE = ("delta", "gated_delta")
+FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta", "kda"]
+DENSE = ("delta", "gated_delta", "kda")
 
 
 def _softplus(z):
@@ -51,7 +51,7 @@ def rand_inputs(rng, fam, L, dk, dv, gate_div=8.0):
     q /= np.linalg.norm(q, axis=1, keepdims=True)
     v = rng.standard_normal((L, dv))
     beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(L)))
-    if fam == "diag":
+    if fam in ("diag", "kda"):
         alpha = np.exp(-_softplus(rng.standard_normal((L, dk))) / gate_div)
     elif fam == "scalar_const":
         alpha = np.array([0.9 + 0.09 * rng.random()])
@@ -95,6 +95,8 @@ def dense_step_matrices(fam, k, v, alpha, beta, t):
     erase = eye - beta[t] * np.outer(kt, kt)
     if fam == "delta":
         return erase, beta[t] * np.outer(kt, vt)
+    if fam == "kda":
+        return erase @ np.diag(alpha[t]), beta[t] * np.outer(kt, vt)
     return alpha[t] * erase, beta[t] * np.outer(kt, vt)
 
 
@@ -325,6 +327,17 @@ def pin_special_cases(orc):
     Tb = orc.transition("delta", kk, None, np.ones(2))
     assert rel(Ta, Tb) < 1e-13
     assert rel(Ta, np.eye(dk) - np.outer(k[0], k[0])) < 1e-13
+    # KDA (Table 1): beta = 0 leaves the per-channel decay of GLA with no writes; g = 1 is
+    # DeltaNet; a per-token gate repeated over the channels, g_t = a_t 1, is GDN.
+    g = np.exp(-_softplus(rng.standard_normal((L, dk))) / 8.0)
+    T, S = orc.segment_pair("kda", k, v, g, np.zeros(L))
+    assert rel(T, np.diag(np.prod(g, axis=0))) < 1e-13
+    assert np.all(S == 0)
+    T1, S1 = orc.segment_pair("kda", k, v, np.ones((L, dk)), beta)
+    assert rel(T1, T2) < 1e-14 and rel(S1, S2) < 1e-14
+    T3, S3 = orc.segment_pair("kda", k, v, np.repeat(alpha[:, None], dk, axis=1), beta)
+    T4, S4 = orc.segment_pair("gated_delta", k, v, alpha, beta)
+    assert rel(T3, T4) < 1e-13 and rel(S3, S4) < 1e-13
 
 
 def pin_spectral_bound(orc):
@@ -376,15 +389,21 @@ def test_oracle_pin(pin):
 # Mutations of the oracle source: each is a plausible mistake that some pin must catch.
 MUTANTS = {
     "write_without_beta": ("TS + (with_write ? b * k[i] * v[j] : 0.0)", "TS + (with_write ? k[i] * v[j] : 0.0)"),
-    "erase_sign_flipped": ("S[i * dv + j] - b * k[i] * tmp[j]", "S[i * dv + j] + b * k[i] * tmp[j]"),
+    "erase_sign_flipped": ("a * (S[i * dv + j] - b * k[i] * tmp[j])", "a * (S[i * dv + j] + b * k[i] * tmp[j])"),
     "gate_decays_write": ("TS + (with_write ? b * k[i] * v[j] : 0.0)", "TS + (with_write ? a * b * k[i] * v[j] : 0.0)"),
     "transposed_T_apply": ("acc += T[i * dk + l] * X[l * ncol + j]", "acc += T[l * dk + i] * X[l * ncol + j]"),
     "compose_order_swapped": ("mul_T(fam, dk, T2, T1, T3);", "mul_T(fam, dk, T1, T2, T3);"),
-    "diag_gate_off_by_one": ("const double *g = alpha + t * dk;", "const double *g = alpha + (t > 0 ? t - 1 : 0) * dk;"),
+    "diag_gate_off_by_one": ("const double *g = alpha + t * dk;", "const double *g = alpha + (t > 0 ? t - 1 : 0) * dk;",
+                             2),
     "transition_drops_token": ("for (t = 0; t < len; t++) p *= gate_scalar", "for (t = 1; t < len; t++) p *= gate_scalar"),
     "output_reads_k": ("acc += q[t * dk + i] * S[i * dv + j];", "acc += k[t * dk + i] * S[i * dv + j];"),
     "erase_uses_v": ("for (i = 0; i < dk; i++) acc += k[i] * S[i * dv + j];",
-                     "for (i = 0; i < dk; i++) acc += (v ? v[i % dv] : k[i]) * S[i * dv + j];"),
+                     "for (i = 0; i < dk; i++) acc += (v ? v[i % dv] : k[i]) * S[i * dv + j];", 2),
+    "kda_gate_on_value_index": ("for (j = 0; j < dv; j++) S[i * dv + j] *= g[i];",
+                                "for (j = 0; j < dv; j++) S[i * dv + j] *= g[j % dk];"),
+    "kda_erase_sign_flipped": ("S[i * dv + j] - b * k[i] * tmp[j] + (with_write", "S[i * dv + j] + b * k[i] * tmp[j] + (with_write"),
+    "kda_gate_decays_write": ("+ (with_write ? b * k[i] * v[j] : 0.0);\n        return;",
+                              "+ (with_write ? g[i] * b * k[i] * v[j] : 0.0);\n        return;"),
     "compose_drops_addend": ("S[i] = Y[i] + S0[(size_t)j * dk * dv + i];", "S[i] = Y[i];"),
 }
 
@@ -393,8 +412,8 @@ MUTANTS = {
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistakes(name, tmp_path):
     src = open(os.path.join(os.path.dirname(O.__file__), "hypic_oracle.c")).read()
-    old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    old, new, count = (MUTANTS[name] + (1,))[:3]
+    assert src.count(old) == count, f"mutation anchor for {name} not found exactly {count} times"
     path_c = tmp_path / "mutant.c"
     path_so = tmp_path / "mutant.so"
     path_c.write_text(src.replace(old, new))

@@ -33,10 +33,11 @@
  *   DIAG          T_i = diag(alpha_i),            u_i = k v^T   T_C: d_k floats
  *   DELTA         T_i = I - b_i k k^T,            u_i = b k v^T T_C: d_k x d_k
  *   GATED_DELTA   T_i = a_i (I - b_i k k^T),      u_i = b k v^T T_C: d_k x d_k
+ *   KDA           T_i = (I - b_i k k^T) diag(g_i), u_i = b k v^T T_C: d_k x d_k
  * Token layouts: k, q, v [tokens, H, d] in the shape's in_dtype (fp32 or
  *   bf16); alpha fp32 [tokens, H] (SCALAR, GATED_DELTA), [tokens, H, d_k]
- *   (DIAG), [H] (SCALAR_CONST), ignored for DELTA; beta fp32 [tokens, H]
- *   (DELTA, GATED_DELTA only).  States and pairs are fp32, row index = key
+ *   (DIAG, and g of KDA), [H] (SCALAR_CONST), ignored for DELTA; beta fp32
+ *   [tokens, H] (DELTA, GATED_DELTA, KDA only).  States and pairs are fp32, row index = key
  *   channel: S [.., H, d_k, d_v], T [.., H, t_size].
  */
 #ifndef HYPIC_H
@@ -67,7 +68,8 @@ typedef enum {
     HYPIC_FAM_SCALAR = 1,
     HYPIC_FAM_DIAG = 2,
     HYPIC_FAM_DELTA = 3,
-    HYPIC_FAM_GATED_DELTA = 4
+    HYPIC_FAM_GATED_DELTA = 4,
+    HYPIC_FAM_KDA = 5       /* builds on the token-by-token path at every size */
 } hypic_family;
 
 typedef enum { HYPIC_F32 = 0, HYPIC_BF16 = 1 } hypic_dtype;

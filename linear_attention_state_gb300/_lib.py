@@ -10,7 +10,7 @@ LIB_PATH = os.path.join(PKG, "libhypic.so")
 
 HYPIC_OK, HYPIC_EINVAL, HYPIC_EUNSUPPORTED, HYPIC_ECUDA, HYPIC_ETIMEOUT, HYPIC_ENOSPACE, HYPIC_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6)
-FAMILY = {"scalar_const": 0, "scalar": 1, "diag": 2, "delta": 3, "gated_delta": 4}
+FAMILY = {"scalar_const": 0, "scalar": 1, "diag": 2, "delta": 3, "gated_delta": 4, "kda": 5}
 DTYPE = {"f32": 0, "bf16": 1}
 
 # Every symbol include/hypic.h declares, with (restype, argtypes).

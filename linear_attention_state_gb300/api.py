@@ -59,7 +59,7 @@ def _in_dtype(k):
 
 def _gates(family, alpha, beta):
     alpha = _cuda(alpha, "alpha", torch.float32, allow_none=family == "delta")
-    beta = _cuda(beta, "beta", torch.float32, allow_none=family not in ("delta", "gated_delta"))
+    beta = _cuda(beta, "beta", torch.float32, allow_none=family not in ("delta", "gated_delta", "kda"))
     return alpha, beta
 
 

@@ -36,13 +36,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
 bool ok_opt(const void *p) { return p == nullptr || aligned16(p); }
 
-bool dense_family(int f) { return f == HYPIC_FAM_DELTA || f == HYPIC_FAM_GATED_DELTA; }
+bool dense_family(int f) { return f == HYPIC_FAM_DELTA || f == HYPIC_FAM_GATED_DELTA || f == HYPIC_FAM_KDA; }
 
 // Shape checks common to every call.  Returns HYPIC_OK or the error.
 hypic_status check_shape(const hypic_shape *s) {
   if (!s) return HYPIC_EINVAL;
   if (s->H < 0 || s->d_k <= 0 || s->d_v <= 0) return HYPIC_EINVAL;
-  if (s->family < HYPIC_FAM_SCALAR_CONST || s->family > HYPIC_FAM_GATED_DELTA) return HYPIC_EINVAL;
+  if (s->family < HYPIC_FAM_SCALAR_CONST || s->family > HYPIC_FAM_KDA) return HYPIC_EINVAL;
   if (s->in_dtype != HYPIC_F32 && s->in_dtype != HYPIC_BF16) return HYPIC_EINVAL;
   if (s->d_k != s->d_v) return HYPIC_EUNSUPPORTED;
   const int d = s->d_k;
@@ -208,8 +208,7 @@ static hypic_status chain_common(const hypic_shape *sh, int32_t B, int32_t n, in
   hypic_status r = check_shape(sh);
   if (r != HYPIC_OK) return r;
   // bf16 pools: delta families only on the d = 128 tensor-core chain
-  const bool dense = sh->family == HYPIC_FAM_DELTA || sh->family == HYPIC_FAM_GATED_DELTA;
-  if (pair_bf16 && dense && sh->d_k != 128) return HYPIC_EUNSUPPORTED;
+  if (pair_bf16 && dense_family(sh->family) && sh->d_k != 128) return HYPIC_EUNSUPPORTED;
   if (B < 0 || n < 0 || w < 0 || pool_size < 0) return HYPIC_EINVAL;
   if (B == 0 || sh->H == 0) return HYPIC_OK;
   if (!ok_ptr(S_out) || !ok_opt(S_init) || !ok_opt(o_out)) return HYPIC_EINVAL;

@@ -45,10 +45,11 @@ __device__ __forceinline__ void stage_T(float *dst, const float *src, int tid) {
   for (int c = tid; c < chunks; c += kThreads) cp_async16(dst + 4 * c, src + 4 * c);
 }
 
-// Seam advance on the shared-memory state for the delta families.
+// Seam advance on the shared-memory state for the dense families: the gate first (a scalar a_t,
+// 1, or KDA's per-channel g_t), y = gate * x, then x = y + b (v_j - k . y) k.
 template <int D, typename Tin>
 __device__ void seam_dense(const ChainArgs &a, float *S, float *sk, float *sq, float *red,
-                           float *sab, int b, int j, int h) {
+                           float *sab, float *sg, int b, int j, int h) {
   constexpr int PARTS = kThreads / D;
   constexpr int RP = D / PARTS;
   const int tid = threadIdx.x, col = tid % D, part = tid / D;
@@ -64,29 +65,32 @@ __device__ void seam_dense(const ChainArgs &a, float *S, float *sk, float *sq, f
       sk[tid] = to_f32<Tin>(K[g]);
       sk[D + tid] = to_f32<Tin>(V[g]);
       if (a.o_out) sq[tid] = to_f32<Tin>(Q[g]);
+      if (a.fam == HYPIC_FAM_KDA) sg[tid] = a.seam.alpha[g];
     }
     if (tid == 0) {
       sab[0] = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam.alpha[tok * H + h] : 1.f;
       sab[1] = a.seam.beta[tok * H + h];
     }
     __syncthreads();
+    const bool kda = a.fam == HYPIC_FAM_KDA;
     float c = 0.f;
 #pragma unroll 8
     for (int r = 0; r < RP; ++r) {
       const int i = part * RP + r;
-      c = fmaf(sk[i], S[i * D + col], c);
+      const float y = (kda ? sg[i] : sab[0]) * S[i * D + col];
+      S[i * D + col] = y;
+      c = fmaf(sk[i], y, c);
     }
     red[part * D + col] = c;
     __syncthreads();
     c = 0.f;
 #pragma unroll
     for (int p = 0; p < PARTS; ++p) c += red[p * D + col];
-    const float at = sab[0];
-    const float coef = sab[1] * (sk[D + col] - at * c);
+    const float coef = sab[1] * (sk[D + col] - c);
 #pragma unroll 8
     for (int r = 0; r < RP; ++r) {
       const int i = part * RP + r;
-      S[i * D + col] = fmaf(coef, sk[i], at * S[i * D + col]);
+      S[i * D + col] = fmaf(coef, sk[i], S[i * D + col]);
     }
     if (a.o_out) {
       __syncthreads();
@@ -119,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_dense_kernel(ChainArgs a) {
   float *sq = sk + 2 * D;
   float *red = sq + D;         // kThreads floats
   float *sab = red + kThreads;  // 2 floats
+  float *sg = sab + 4;          // D floats: KDA seam gate
 
   const int nhalf = a.scan ? 2 : 1;
   const int half = blockIdx.x % nhalf;
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_dense_kernel(ChainArgs a) {
         for (int c = 0; c < TM; ++c) add[r][c] = isT ? 0.f : __ldg(S0 + (size_t)(i0 + r) * D + j0 + c);
       }
     }
-    if (!a.scan && a.w > 0 && j >= 1) seam_dense<D, Tin>(a, S, sk, sq, red, sab, b, j, h);
+    if (!a.scan && a.w > 0 && j >= 1) seam_dense<D, Tin>(a, S, sk, sq, red, sab, sg, b, j, h);
 
     const float *T = Tb + (j & 1) * DD;
     float acc[TM][TM];
@@ -312,12 +317,12 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) chain_diag_kernel(ChainArgs 
 
 template <int D, typename Tin>
 cudaError_t launch_d(const ChainArgs &a, cudaStream_t st) {
-  const bool dense = a.fam == HYPIC_FAM_DELTA || a.fam == HYPIC_FAM_GATED_DELTA;
+  const bool dense = a.fam == HYPIC_FAM_DELTA || a.fam == HYPIC_FAM_GATED_DELTA || a.fam == HYPIC_FAM_KDA;
   if (dense) {
     if (a.pair_bf16) return cudaErrorInvalidValue;  // rejected by the API before any launch
     const long long blocks = (long long)a.B * a.H * (a.scan ? 2 : 1);
     if (blocks <= 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * (3 * D * D + 3 * D + kThreads + 2);
+    const size_t smem = sizeof(float) * (3 * D * D + 3 * D + kThreads + 4 + D);
     cudaError_t e = cudaFuncSetAttribute(chain_dense_kernel<D, Tin>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

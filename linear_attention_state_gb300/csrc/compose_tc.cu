@@ -317,16 +317,25 @@ __global__ void __launch_bounds__(NT, 1)
     if (step + 1 < a.n) {
       // (4) Seam tokens of the next segment, token by token on the register column.
       if (a.w > 0) {
-        float *sk = sS0, *sq = sS0 + D;
+        // Gate first (a_t, 1, or KDA's per-channel g_t), y = gate * x, then
+        // x = y + b (v_j - k . y) k.
+        float *sk = sS0, *sq = sS0 + D, *sg = sS0 + 2 * D;
+        const bool kda = a.fam == HYPIC_FAM_KDA;
         for (int t = 0; t < a.w; ++t) {
           const size_t tok = ((size_t)b * (a.n - 1) + step) * a.w + t;
           const size_t g = (tok * H + h) * D;
-          if (half == 0) sk[j] = ld_tok<Tin>(SK, g + j);
-          else if (a.o_out) sq[j] = ld_tok<Tin>(SQ, g + j);
+          if (half == 0) {
+            sk[j] = ld_tok<Tin>(SK, g + j);
+            if (kda) sg[j] = a.seam_alpha[g + j];
+          } else if (a.o_out) {
+            sq[j] = ld_tok<Tin>(SQ, g + j);
+          }
           const float at = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
           const float bt = a.seam_beta[tok * H + h];
           const float vj = ld_tok<Tin>(SV, g + j);
           __syncthreads();
+#pragma unroll
+          for (int r = 0; r < R; ++r) x[r] *= kda ? sg[i0 + r] : at;
           float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
 #pragma unroll
           for (int r = 0; r < R; r += 4) {
@@ -338,9 +347,9 @@ __global__ void __launch_bounds__(NT, 1)
           red[half][j] = (c0 + c1) + (c2 + c3);
           __syncthreads();
           const float kx = red[0][j] + red[1][j];
-          const float coef = bt * (vj - at * kx);
+          const float coef = bt * (vj - kx);
 #pragma unroll
-          for (int r = 0; r < R; ++r) x[r] = fmaf(coef, sk[i0 + r], at * x[r]);
+          for (int r = 0; r < R; ++r) x[r] = fmaf(coef, sk[i0 + r], x[r]);
           if (a.o_out) {
             float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(NT, 1)
 }  // namespace
 
 bool compose_tc_supported(int D_, int fam) {
-  return D_ == D && (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
+  return D_ == D && (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA || fam == HYPIC_FAM_KDA);
 }
 
 template <typename Tin, bool PB>

@@ -3,6 +3,7 @@
 //
 // Each column of the state evolves on its own: for the delta families
 //   x <- a (x - b k (k . x)) + b v_j k   =   a x + b (v_j - a (k . x)) k,
+// and for KDA (T = (I - b k k^T) diag(g)) y = g * x, x <- y + b (v_j - k . y) k,
 // so one thread owns one column of the state in registers and the k, q vectors
 // of a tile of tokens are staged in shared memory and read as broadcasts.  The
 // build runs over the augmented state [T | S] (d_k x (d_k + d_v)) from [I | 0]:
@@ -17,7 +18,7 @@
 namespace hypic {
 namespace {
 
-enum Kind { KIND_SCALAR = 0, KIND_DIAG = 1, KIND_DELTA = 2 };
+enum Kind { KIND_SCALAR = 0, KIND_DIAG = 1, KIND_DELTA = 2, KIND_KDA = 3 };
 
 constexpr int kTile = 16;  // tokens staged per shared-memory tile
 
@@ -36,7 +37,8 @@ template <int D, int KIND, typename Tin>
 __global__ void __launch_bounds__(D >= 64 ? 64 : D) recurrent_kernel(RecurrentArgs a) {
   constexpr int TPC = D >= 64 ? 64 : D;  // columns (threads) per block
   const bool build = a.T_out != nullptr;
-  const bool dense_build = build && KIND == KIND_DELTA;
+  const bool dense_build = build && (KIND == KIND_DELTA || KIND == KIND_KDA);
+  constexpr bool CHANNEL_GATE = KIND == KIND_DIAG || KIND == KIND_KDA;
   const int ncols = dense_build ? 2 * D : D;
   const int ncb = ncols / TPC;
   const int cb = blockIdx.x % ncb;
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) recurrent_kernel(RecurrentAr
 
   __shared__ __align__(16) float sk[kTile][D];
   __shared__ __align__(16) float sq[kTile][D];
-  __shared__ __align__(16) float sg[kTile][KIND == KIND_DIAG ? D : 1];
+  __shared__ __align__(16) float sg[kTile][CHANNEL_GATE ? D : 1];
   __shared__ float sa[kTile], sb[kTile];
 
   const Tin *K = static_cast<const Tin *>(a.src.k);
@@ -86,14 +88,14 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) recurrent_kernel(RecurrentAr
       const size_t g = ((size_t)(beg + t0 + t) * H + h) * D + i;
       sk[t][i] = to_f32<Tin>(K[g]);
       if (want_o) sq[t][i] = to_f32<Tin>(Q[g]);
-      if (KIND == KIND_DIAG) sg[t][i] = a.src.alpha[g];
+      if (CHANNEL_GATE) sg[t][i] = a.src.alpha[g];
     }
     for (int t = tid; t < nt; t += TPC) {
       const size_t g = (size_t)(beg + t0 + t) * H + h;
       float av = 1.f, bv = 1.f;
       if (fam == HYPIC_FAM_SCALAR_CONST) av = a.src.alpha[h];
       else if (fam == HYPIC_FAM_SCALAR || fam == HYPIC_FAM_GATED_DELTA) av = a.src.alpha[g];
-      if (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA) bv = a.src.beta[g];
+      if (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA || fam == HYPIC_FAM_KDA) bv = a.src.beta[g];
       sa[t] = av;
       sb[t] = bv;
     }
@@ -122,6 +124,31 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) recurrent_kernel(RecurrentAr
           x[4 * i + 1] = fmaf(coef, kv.y, at * x[4 * i + 1]);
           x[4 * i + 2] = fmaf(coef, kv.z, at * x[4 * i + 2]);
           x[4 * i + 3] = fmaf(coef, kv.w, at * x[4 * i + 3]);
+        }
+      } else if (KIND == KIND_KDA) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(sg[t]);
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) {
+          const float4 kv = k4[i];
+          const float4 gv = g4[i];
+          x[4 * i + 0] *= gv.x;
+          x[4 * i + 1] *= gv.y;
+          x[4 * i + 2] *= gv.z;
+          x[4 * i + 3] *= gv.w;
+          c0 = fmaf(kv.x, x[4 * i + 0], c0);
+          c1 = fmaf(kv.y, x[4 * i + 1], c1);
+          c2 = fmaf(kv.z, x[4 * i + 2], c2);
+          c3 = fmaf(kv.w, x[4 * i + 3], c3);
+        }
+        const float coef = sb[t] * (vj - ((c0 + c1) + (c2 + c3)));
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) {
+          const float4 kv = k4[i];
+          x[4 * i + 0] = fmaf(coef, kv.x, x[4 * i + 0]);
+          x[4 * i + 1] = fmaf(coef, kv.y, x[4 * i + 1]);
+          x[4 * i + 2] = fmaf(coef, kv.z, x[4 * i + 2]);
+          x[4 * i + 3] = fmaf(coef, kv.w, x[4 * i + 3]);
         }
       } else if (KIND == KIND_SCALAR) {
 #pragma unroll
@@ -176,12 +203,14 @@ __global__ void __launch_bounds__(D >= 64 ? 64 : D) recurrent_kernel(RecurrentAr
 template <int D, typename Tin>
 cudaError_t launch_d(const RecurrentArgs &a, cudaStream_t st) {
   constexpr int TPC = D >= 64 ? 64 : D;
-  const bool dense = a.fam == HYPIC_FAM_DELTA || a.fam == HYPIC_FAM_GATED_DELTA;
+  const bool dense = a.fam == HYPIC_FAM_DELTA || a.fam == HYPIC_FAM_GATED_DELTA || a.fam == HYPIC_FAM_KDA;
   const int ncols = (a.T_out && dense) ? 2 * D : D;
   const long long blocks = (long long)a.n_seg * a.H * (ncols / TPC);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (dense)
+  if (a.fam == HYPIC_FAM_KDA)
+    recurrent_kernel<D, KIND_KDA, Tin><<<(unsigned)blocks, TPC, 0, st>>>(a);
+  else if (dense)
     recurrent_kernel<D, KIND_DELTA, Tin><<<(unsigned)blocks, TPC, 0, st>>>(a);
   else if (a.fam == HYPIC_FAM_DIAG)
     recurrent_kernel<D, KIND_DIAG, Tin><<<(unsigned)blocks, TPC, 0, st>>>(a);

@@ -37,7 +37,7 @@ def gates(family, tok, h, b, e):
         a = None
     else:
         a = np64(alpha[b:e, h])
-    bb = np64(beta[b:e, h]) if family in ("delta", "gated_delta") else None
+    bb = np64(beta[b:e, h]) if family in ("delta", "gated_delta", "kda") else None
     return a, bb
 
 

@@ -18,7 +18,7 @@ import workloads as W
 from refs import TOL_BF16, TOL_F32, np64, relerr
 
 pytestmark = pytest.mark.gpu
-FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta"]
+FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta", "kda"]
 DEV = "cuda"
 
 
@@ -66,7 +66,7 @@ def test_rounding_is_nearest_even_bit_for_bit(family):
 @pytest.mark.parametrize("family", FAMS)
 @pytest.mark.parametrize("d", [16, 128])
 def test_compose_over_bf16_pool(family, d):
-    if d != 128 and family in ("delta", "gated_delta"):
+    if d != 128 and family in ("delta", "gated_delta", "kda"):
         pytest.skip("bf16 pools of the delta families run on the d = 128 tensor-core chain only")
     P, H, B, n = 11, 3, 4, 7
     T, S = random_pool(family, P, H, d, key=10 + d + FAMS.index(family))
@@ -103,37 +103,42 @@ def test_bf16_pool_differs_from_fp32_pool_by_the_storage_rounding():
         assert 0.0 < e < 1e-2, e
 
 
-@pytest.mark.parametrize("family", ["gated_delta", "diag"])
-def test_assemble_over_bf16_pool_with_seams(family):
-    P, H, d, B, n, w = 6, 2, 128, 2, 4, 8
-    T, S = random_pool(family, P, H, d, key=90 + FAMS.index(family))
-    T_lp, S_lp = hy.pairs_to_bf16(T, S, family=family)
+@pytest.mark.parametrize("family", ["gated_delta", "diag", "kda"])
+@pytest.mark.parametrize("d,storage", [(128, "bf16"), (128, "f32"), (16, "f32")])
+def test_assemble_with_seams(family, d, storage):
+    """Seams then composition per segment; the seam update of each family (KDA's per-channel gate
+    included) on the tensor-core chain (d = 128) and the SIMT chains (d = 16)."""
+    P, H, B, n, w = 6, 2, 2, 4, 8
+    T, S = random_pool(family, P, H, d, key=90 + d + FAMS.index(family))
+    if storage == "bf16":
+        T, S = hy.pairs_to_bf16(T, S, family=family)
     idx = torch.tensor([[0, 3, 1, 5], [2, 4, 0, 1]], dtype=torch.int32, device=DEV)
-    g = W.generator(DEV, 45, FAMS.index(family))
-    tok = W.draw_tokens(g, B * (n - 1) * w, H, d, family, "bf16", DEV,
-                        gate_div=16.0 if family == "diag" else None)
+    g = W.generator(DEV, 45, FAMS.index(family) + d)
+    in_dtype = "bf16" if d == 128 else "f32"
+    tok = W.draw_tokens(g, B * (n - 1) * w, H, d, family, in_dtype, DEV,
+                        gate_div=16.0 if family in ("diag", "kda") else None)
     shp = (B, n - 1, w, H, d)
     sk, sv, sq = tok["k"].view(shp), tok["v"].view(shp), tok["q"].view(shp)
-    sa = tok["alpha"] if family == "scalar_const" else tok["alpha"].view((B, n - 1, w) + tok["alpha"].shape[1:])
+    sa = tok["alpha"].view((B, n - 1, w) + tok["alpha"].shape[1:])
     sb = tok["beta"].view(B, n - 1, w, H)
-    S_out, o = hy.assemble(T_lp, S_lp, idx, sk, sv, seam_alpha=sa, seam_beta=sb, seam_q=sq, family=family)
+    S_out, o = hy.assemble(T, S, idx, sk, sv, seam_alpha=sa, seam_beta=sb, seam_q=sq, family=family)
     assert hy.stream_status() == 0
-    Th, Sh = np64(T_lp), np64(S_lp)
+    Th, Sh = np64(T), np64(S)
     worst_s = worst_o = 0.0
     for b in range(B):
         for h in range(H):
             Sr = None
             for j in range(n):
                 if j >= 1:
-                    a_ = np64(tok["alpha"][h:h + 1]) if family == "scalar_const" else np64(sa[b, j - 1, :, h])
-                    bb = np64(sb[b, j - 1, :, h]) if family in ("delta", "gated_delta") else None
-                    Sr, orf = oracle.run(family, np64(sk[b, j - 1, :, h]), np64(sv[b, j - 1, :, h]), a_, bb,
-                                         q=np64(sq[b, j - 1, :, h]), S0=Sr)
+                    bb = np64(sb[b, j - 1, :, h]) if family in ("delta", "gated_delta", "kda") else None
+                    Sr, orf = oracle.run(family, np64(sk[b, j - 1, :, h]), np64(sv[b, j - 1, :, h]),
+                                         np64(sa[b, j - 1, :, h]), bb, q=np64(sq[b, j - 1, :, h]), S0=Sr)
                     worst_o = max(worst_o, relerr(np64(o[b, j - 1, :, h]), orf))
                 p = int(idx[b, j])
                 Sr = oracle.compose(family, Th[p:p + 1, h].reshape(1, -1), Sh[p:p + 1, h], S_init=Sr)
             worst_s = max(worst_s, relerr(np64(S_out[b, h]), Sr))
-    assert worst_s <= TOL_BF16 and worst_o <= TOL_BF16, (worst_s, worst_o)
+    tol = TOL_BF16 if in_dtype == "bf16" else TOL_F32
+    assert worst_s <= tol and worst_o <= tol, (worst_s, worst_o)
 
 
 def test_n_zero_and_in_place_over_bf16_pool():

@@ -16,7 +16,7 @@ import workloads as W
 from refs import TOL_BF16, TOL_F32, host_tokens, np64, ref_pair, ref_run, relerr, t_as_dense
 
 pytestmark = pytest.mark.gpu
-FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta"]
+FAMS = ["scalar_const", "scalar", "diag", "delta", "gated_delta", "kda"]
 DEV = "cuda"
 
 

@@ -64,7 +64,7 @@ def draw_tokens(gen: torch.Generator, n: int, H: int, d: int, family: str, in_dt
     q = unit_rows() if need_q else None
     v = torch.randn((n, H, d), generator=gen, device=device, dtype=f32).to(dt)
     beta = torch.sigmoid(torch.randn((n, H), generator=gen, device=device, dtype=f32))
-    if family == "diag":
+    if family in ("diag", "kda"):
         z = torch.randn((n, H, d), generator=gen, device=device, dtype=f32)
         alpha = torch.exp(-torch.nn.functional.softplus(z) / (gate_div or 16.0))
     elif family == "scalar_const":

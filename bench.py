@@ -32,6 +32,8 @@ METRIC = "segment tokens/s (build) and compositions/s, % tensor/HBM roofline, 1 
 D = 128
 FLOP_PER_CHUNK_WY = 3 * 2 * 64 * 64 * D + 2 * 2 * 64 * D * (2 * D)  # G, U, W; W.X and K^T.R per 64-token chunk
 FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
+# with per-token outputs: + Q S_p (2 C d^2), Q K^T and M Wm (2 C^2 d each) per chunk
+FLOP_PER_HEAD_TOKEN_WY_O = (FLOP_PER_CHUNK_WY + 2 * 64 * D * D + 4 * 64 * 64 * D) // 64  # 245,760
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 # dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
@@ -315,6 +317,46 @@ def scan_measure(steps, warmup, dev, peaks):
     return res
 
 
+def build_outputs_measure(steps, warmup, dev, peaks):
+    """The 32k-token build with every body token's output (q read, o written): the cold-segment
+    forward fused with pair construction.  Reported beside the pair-only build of the headline."""
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import workloads as W
+    w = W.BUILD_32K
+    tok = w.draw_request(dev)
+    bounds = torch.tensor(w.body_bounds(), device=dev)
+    ws_bytes = hy.build_workspace_bytes(w.H, w.d, w.n_seg, w.seg_len, family=w.family, in_dtype=w.in_dtype,
+                                        want_o=True)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    T = torch.empty((w.n_seg, w.H, w.d * w.d), device=dev)
+    S = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
+    o = torch.zeros((tok["k"].shape[0], w.H, w.d), device=dev)
+
+    def fn(ev):
+        if ev is not None:
+            ev[0].record()
+        hy.segment_build_batched(tok["k"], tok["v"], bounds, tok["alpha"], tok["beta"], q=tok["q"], family=w.family,
+                                 max_len=w.seg_len, want_o=True, out=(T, S), ws=ws, o_out=o)
+        if ev is not None:
+            ev[1].record()
+            ev[2].record()
+
+    _, k1, _ = run_timed(fn, steps, warmup, torch.cuda.synchronize)
+    tb = sum(k1) / len(k1) / 1e3
+    ht = sum(e - b for b, e in w.body_bounds()) * w.H
+    fl = FLOP_PER_HEAD_TOKEN_WY_O * ht
+    res = {"workload": w.name + "_with_outputs", "build_ms": tb * 1e3, "body_head_tokens_per_s": ht / tb,
+           "roofline": {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": fl / tb / 1e12 / peaks["bf16_tflops"], "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY_O,
+                        "traffic": None},
+           "status": hy.stream_status()}
+    del tok, ws, T, S, o
+    torch.cuda.empty_cache()
+    return res
+
+
 def boundary_measure(steps, warmup, dev, peaks):
     """Boundary patches, HBM-bound: RoPE shift of one 32k-token segment's keys (8 heads x 128
     dims, bf16, out of place) and re-rotation of 2,048 scalar-family states (64 segments x 32
@@ -446,6 +488,8 @@ def main():
                     help="time only the affine scan (profiling aid; prints its own line)")
     ap.add_argument("--boundary-only", action="store_true",
                     help="time only the boundary patches (profiling aid; prints its own line)")
+    ap.add_argument("--outputs-only", action="store_true",
+                    help="time only the build with per-token outputs (profiling aid; prints its own line)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -485,9 +529,11 @@ def main():
                               "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
                               "warmup": args.warmup, "compose_pool": res}))
         return
-    if args.decay_only or args.scan_only or args.boundary_only:
+    if args.decay_only or args.scan_only or args.boundary_only or args.outputs_only:
         fn, what = ((decay_build_measure, "decay-family builds") if args.decay_only else
-                    (scan_measure, "affine scan") if args.scan_only else (boundary_measure, "boundary patches"))
+                    (scan_measure, "affine scan") if args.scan_only else
+                    (build_outputs_measure, "build with outputs") if args.outputs_only else
+                    (boundary_measure, "boundary patches"))
         res = fn(args.steps, args.warmup, dev, peaks)
         if rank == 0:
             print(json.dumps({"metric": what, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -543,8 +589,9 @@ def main():
     e2e_ms, _, _ = run_timed(e2e_step, args.steps, min(args.warmup, 3), sync_all, kernel_events=False)
     e2e_value = req.tokens * world / (e2e_ms / 1e3 / args.steps)
 
-    decay = scan = bnd = None
+    decay = scan = bnd = outs = None
     if not args.no_compose:
+        outs = build_outputs_measure(args.steps, args.warmup, dev, peaks)
         decay = decay_build_measure(args.steps, args.warmup, dev, peaks)
         scan = scan_measure(args.steps, args.warmup, dev, peaks)
         bnd = boundary_measure(args.steps, args.warmup, dev, peaks)
@@ -581,6 +628,7 @@ def main():
             "decay_builds": decay,
             "affine_scan": scan,
             "boundary_patches": bnd,
+            "build_with_outputs": outs,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": req.launches_per_step * args.steps,

@@ -132,6 +132,15 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
 size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
 
 /*
+ * The same for builds that also emit per-token outputs (q and o_out given): the tensor-core
+ * build then keeps a 66,560-byte record per (64-token chunk, head) -- the 49,664 bytes above
+ * plus gamma_t and the intra-chunk matrix M_ts = exp(G_t - G_s) q_t.k_s -- so any size holding
+ * one head's records (n_seg * ceil(max_len / 64) * 66,560 bytes) works, and less gives
+ * HYPIC_ENOSPACE.  0 when the shape builds without a workspace.
+ */
+size_t hypic_build_workspace_bytes_outputs(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
+
+/*
  * Allocation-free batched build.  No counterpart in the paper: it exists for
  * callers that cannot allocate device memory themselves -- code embedded in a
  * host framework that owns every device allocation through its own pool and

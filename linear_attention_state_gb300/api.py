@@ -75,7 +75,8 @@ def segment_build(k, v, alpha=None, beta=None, q=None, family="gated_delta", wan
     T = torch.empty((H, t_size(family, d)), device=k.device, dtype=torch.float32)
     S = torch.empty((H, d, d), device=k.device, dtype=torch.float32)
     o = torch.empty((n, H, d), device=k.device, dtype=torch.float32) if want_o else None
-    ws_bytes = lib.hypic_build_workspace_bytes(ctypes.byref(sh), 1, n)
+    query = lib.hypic_build_workspace_bytes_outputs if want_o else lib.hypic_build_workspace_bytes
+    ws_bytes = query(ctypes.byref(sh), 1, n)
     ws = torch.empty(ws_bytes, device=k.device, dtype=torch.uint8) if ws_bytes else None
     st = lib.hypic_segment_build(ctypes.byref(sh), _p(k), _p(v), _p(q if want_o else None), _p(alpha), _p(beta), n,
                                  _p(T), _p(S), _p(o), _p(ws), ws_bytes, _stream(stream))
@@ -84,14 +85,16 @@ def segment_build(k, v, alpha=None, beta=None, q=None, family="gated_delta", wan
     return (T, S, o) if want_o else (T, S)
 
 
-def build_workspace_bytes(H, d, n_seg, max_len, family="gated_delta", in_dtype="bf16") -> int:
+def build_workspace_bytes(H, d, n_seg, max_len, family="gated_delta", in_dtype="bf16", want_o=False) -> int:
     """Preferred workspace of a batched build (0 when the shape needs none)."""
     sh = L.shape(H, d, family, in_dtype)
-    return int(L.load().hypic_build_workspace_bytes(ctypes.byref(sh), n_seg, max_len))
+    lib = L.load()
+    query = lib.hypic_build_workspace_bytes_outputs if want_o else lib.hypic_build_workspace_bytes
+    return int(query(ctypes.byref(sh), n_seg, max_len))
 
 
 def segment_build_batched(k, v, bounds, alpha=None, beta=None, q=None, family="gated_delta", max_len=None,
-                          want_o=False, out=None, ws=None, stream=None):
+                          want_o=False, out=None, ws=None, o_out=None, stream=None):
     """Pairs of n_seg bodies [begin, end) = bounds[i] (int64 [n_seg, 2] on the device) of one token axis."""
     lib = L.load()
     _cuda(k, "k"), _cuda(v, "v", k.dtype)
@@ -110,9 +113,13 @@ def segment_build_batched(k, v, bounds, alpha=None, beta=None, q=None, family="g
     else:
         T, S = out
         _cuda(T, "T_out", torch.float32), _cuda(S, "S_out", torch.float32)
-    o = torch.zeros((n_tok, H, d), device=k.device, dtype=torch.float32) if want_o else None
+    if want_o and o_out is not None:
+        o = _cuda(o_out, "o_out", torch.float32)
+    else:
+        o = torch.zeros((n_tok, H, d), device=k.device, dtype=torch.float32) if want_o else None
     if ws is None:
-        ws_bytes = lib.hypic_build_workspace_bytes(ctypes.byref(sh), n_seg, max_len)
+        query = lib.hypic_build_workspace_bytes_outputs if want_o else lib.hypic_build_workspace_bytes
+        ws_bytes = query(ctypes.byref(sh), n_seg, max_len)
         ws = torch.empty(ws_bytes, device=k.device, dtype=torch.uint8) if ws_bytes else None
     else:
         _cuda(ws, "ws", torch.uint8)

@@ -84,7 +84,8 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
                   !force_recurrent();
   const bool dtc = tokens && build_decay_tc_supported(sh->d_k, sh->family, sh->in_dtype, o_out != nullptr) &&
                    !force_recurrent();
-  if (tc && (ws_bytes < build_tc_min_workspace(n_seg, seg.max_len) || !ok_ptr(ws))) return HYPIC_ENOSPACE;
+  if (tc && (ws_bytes < build_tc_min_workspace(n_seg, seg.max_len, o_out != nullptr) || !ok_ptr(ws)))
+    return HYPIC_ENOSPACE;
   int *err = nullptr;
   cudaError_t e = status_word(&err);
   if (e != cudaSuccess) return HYPIC_ECUDA;
@@ -137,7 +138,13 @@ const char *hypic_strerror(hypic_status s) {
 size_t hypic_build_workspace_bytes(const hypic_shape *sh, int32_t n_seg, int64_t max_len) {
   if (check_shape(sh) != HYPIC_OK || n_seg <= 0 || max_len <= 0) return 0;
   if (!build_tc_supported(sh->d_k, sh->family, sh->in_dtype, false)) return 0;
-  return build_tc_workspace_bytes(sh->H, n_seg, max_len);
+  return build_tc_workspace_bytes(sh->H, n_seg, max_len, false);
+}
+
+size_t hypic_build_workspace_bytes_outputs(const hypic_shape *sh, int32_t n_seg, int64_t max_len) {
+  if (check_shape(sh) != HYPIC_OK || n_seg <= 0 || max_len <= 0) return 0;
+  if (!build_tc_supported(sh->d_k, sh->family, sh->in_dtype, true)) return 0;
+  return build_tc_workspace_bytes(sh->H, n_seg, max_len, true);
 }
 
 size_t hypic_scan_workspace_bytes(const hypic_shape *sh, int32_t n) {

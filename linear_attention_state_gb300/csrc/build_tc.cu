@@ -55,7 +55,14 @@ constexpr uint32_t WS_WH = 0, WS_WL = 16384, WS_AVH = 32768, WS_AVL = 40960, WS_
 constexpr uint32_t WS_TILES = 49152;  // the four tiles, contiguous
 constexpr uint32_t WS_SC_BYTES = 272;  // 65 floats rounded up to 16 bytes
 constexpr uint32_t WS_REC = 49664;  // bytes per (chunk, head)
-constexpr size_t WS_CAP = (size_t)1 << 30;  // preferred workspace size bound
+// With per-token outputs the record also holds gamma_t = exp(G_t) (64 floats after the scales)
+// and the intra-chunk matrix M_ts = exp(G_t - G_s) q_t.k_s (s <= t) as hi and lo K-major
+// [64 t][64 s] tiles.
+constexpr uint32_t WS_GAM = WS_SC + 272;     // 64 floats
+constexpr uint32_t WS_SCG_BYTES = 528;       // scales, gamma_C, padding, gamma_t
+constexpr uint32_t WS_MH = 50176, WS_ML = WS_MH + 8192;
+constexpr uint32_t WS_REC_O = WS_ML + 8192;  // 66,560
+constexpr size_t WS_CAP = (size_t)4 << 30;  // preferred workspace size bound
 
 struct BuildTcArgs {
   int H;       // heads of the token tensors
@@ -67,7 +74,10 @@ struct BuildTcArgs {
   int fam;
   const float *alpha, *beta;
   float *T_out, *S_out;
+  float *o_out;  // [tokens, H, D] or null
   uint8_t *ws;
+  uint32_t rec_bytes;  // WS_REC, or WS_REC_O with outputs
+  int t_only;          // chain_tc_kernel runs the T half only (the S half comes from chain_so_kernel)
   int *err;
 };
 
@@ -83,7 +93,7 @@ __device__ __forceinline__ bool seg_bounds(const BuildTcArgs &a, int s, int64_t 
 }
 
 __device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, int hh) {
-  return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * WS_REC;
+  return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * a.rec_bytes;
 }
 
 // hi = bf16(v), lo = bf16(v - hi) for 8 values, packed for one 16-byte store each.
@@ -110,8 +120,14 @@ constexpr uint32_t P_OFF_L = 16384;   // fp32 [64][LS]: L, then A in place (lowe
 constexpr uint32_t P_OFF_AB = P_OFF_L;  // K-major [64 t][64 s] bf16 tiles, 8 KB each
 constexpr uint32_t P_OFF_WT = 0;      // Wk^T hi, lo staged for the store, over K and L once both are consumed
 constexpr uint32_t P_SMEM = P_OFF_L + 64 * LS * 4 + 1024;  // + alignment slack
+constexpr uint32_t P_OFF_Q = 34816;   // with outputs: 16 KB Q chunk, two [64 t][64 i] boxes
+constexpr uint32_t P_SMEM_O = P_OFF_Q + 16384 + 1024;
 
-__global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, BuildTcArgs a) {
+template <bool WO>
+__global__ void __launch_bounds__(NT, WO ? 4 : 6)
+    wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
+                   BuildTcArgs a) {
+  constexpr uint32_t TCOLS = WO ? 128 : 64;  // Gram (and Q K^T at column 64)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
@@ -136,12 +152,16 @@ __global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ 
     mbar_init(&bar_mma, 1);
     mbar_fence_init();
     ok_flag = 1;
-    mbar_arrive_expect_tx(&bar_tma, 16384);
+    mbar_arrive_expect_tx(&bar_tma, WO ? 32768 : 16384);
     tma_load_2d(sm + P_OFF_K, &mapK, &bar_tma, h * D, (int)t0);
     tma_load_2d(sm + P_OFF_K + 8192, &mapK, &bar_tma, h * D + 64, (int)t0);
+    if (WO) {
+      tma_load_2d(sm + P_OFF_Q, &mapQ, &bar_tma, h * D, (int)t0);
+      tma_load_2d(sm + P_OFF_Q + 8192, &mapQ, &bar_tma, h * D + 64, (int)t0);
+    }
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_slot, 64);
+    tmem_alloc(&tmem_slot, TCOLS);
     tmem_relinquish();
   }
   // gates: G_t = inclusive log2-cumsum of a, masked beyond the body
@@ -174,6 +194,15 @@ __global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ 
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
         mma_f16(tmem, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id, kk > 0);
+      }
+      if (WO) {
+        // Q K^T (M = 64 t, N = 64 s, K = 128 i), Q and K exact in bf16
+        const uint32_t qb = smem_u32(sm + P_OFF_Q);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_f16(tmem + 64, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id, kk > 0);
+        }
       }
       mma_commit(&bar_mma);
       if (!mbar_wait_cycles(&bar_mma, 0, a.err)) ok_flag = 0;
@@ -225,10 +254,41 @@ __global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ 
       }
     }
   }
+  if (WO && ok_flag) {
+    // M_ts = 2^(G_t - G_s) (Q K^T)_ts for s <= t, split hi + lo into the K-major [t][s] tiles of
+    // the record; gamma_t = 2^(G_t).
+    uint8_t *rec = ws_rec(a, s, c, hh);
+    const int t = warp * 16 + lane;
+    const float et = lane < 16 ? sE[t] : 0.f;
+    const float Gt = lane < 16 ? sG[t] : 0.f;
+#pragma unroll 1
+    for (int hb = 0; hb < C; hb += 32) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 64 + hb, v);
+      if (lane < 16) {
+#pragma unroll
+        for (int q = 0; q < 32; q += 8) {
+          float m8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int sc = hb + q + e;
+            const float dec = separable ? et * sF[sc] : exp2f(Gt - sG[sc]);
+            m8[e] = sc <= t ? dec * v[q + e] : 0.f;
+          }
+          uint4 hi, lo;
+          split8(m8, hi, lo);
+          const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)((hb + q) >> 3));
+          *reinterpret_cast<uint4 *>(rec + WS_MH + off) = hi;
+          *reinterpret_cast<uint4 *>(rec + WS_ML + off) = lo;
+        }
+      }
+    }
+    if (tid < C) reinterpret_cast<float *>(rec + WS_GAM)[tid] = exp2f(sG[tid]);
+  }
   tc_fence_before();
   __syncthreads();
   if (!ok_flag) {
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
     return;
   }
 
@@ -377,7 +437,7 @@ __global__ void __launch_bounds__(NT, 6) wy_prep_kernel(const __grid_constant__ 
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (warp == 0) tmem_dealloc(tmem, TCOLS);
   if (ok_flag && tid == 0) {
     bulk_store(rec + WS_WH, sm + P_OFF_WT, 32768);
     bulk_store_commit();
@@ -509,6 +569,7 @@ __global__ void __launch_bounds__(NT2, 1)
         const uint32_t stg = sb + st * STAGE_BYTES;
         if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err)) return false;
         tc_fence_after();
+        if (a.t_only) return true;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t av = sdesc_sw128(stg + STAGE_V + kk * 2048, 8192, 1024);
@@ -522,7 +583,8 @@ __global__ void __launch_bounds__(NT2, 1)
         const uint32_t par = (uint32_t)c & 1u;
         const uint32_t stg = sb + (c & 1) * STAGE_BYTES;
         // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
-        for (int hf = 0; hf < 2 && ok; ++hf) {
+        const int nh = a.t_only ? 1 : 2;
+        for (int hf = 0; hf < nh && ok; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
           tc_fence_after();
           const uint32_t xlo = sb + OFF_XLO + hf * 32768;
@@ -540,7 +602,7 @@ __global__ void __launch_bounds__(NT2, 1)
         // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next chunk's -U^T
         // is queued right behind the S update, before its commit, so the pipe does not wait
         // for the commits; the S half's update barrier then also covers it.
-        for (int hf = 0; hf < 2 && ok; ++hf) {
+        for (int hf = 0; hf < nh && ok; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r2[hf], par, a.err))) break;
           tc_fence_after();
 #pragma unroll
@@ -550,7 +612,7 @@ __global__ void __launch_bounds__(NT2, 1)
             mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);
           }
-          if (hf == 1 && c + 1 < nchunks) ok = issue_u(c + 1);
+          if (hf == nh - 1 && c + 1 < nchunks) ok = issue_u(c + 1);
           if (!ok) break;
           mma_commit(&bar_x[hf]);
         }
@@ -573,7 +635,8 @@ __global__ void __launch_bounds__(NT2, 1)
     }
     tmem_st_wait();
     bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
+    const int my_chunks = (a.t_only && half == 1) ? 0 : nchunks;
+    for (int c = 0; c < my_chunks && ok; ++c) {
       const int st = c & 1;
       const uint32_t par = (uint32_t)c & 1u;
       if (c > 0 && !(ok = mbar_wait_sleep(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
@@ -631,7 +694,7 @@ __global__ void __launch_bounds__(NT2, 1)
       tc_fence_before();
       mbar_arrive(&bar_r2[half]);
     }
-    if (ok && nchunks > 0) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)(nchunks - 1) & 1u, a.err);
+    if (ok && my_chunks > 0) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)(my_chunks - 1) & 1u, a.err);
     if (!ok) abort_flag = 1;
   }
   __syncthreads();
@@ -646,7 +709,7 @@ __global__ void __launch_bounds__(NT2, 1)
         mbar_wait_cycles(&bar_empty[i], (uint32_t)k, nullptr, 100000000LL);
       }
   }
-  if (!abort_flag && !issuer && !producer) {
+  if (!abort_flag && !issuer && !producer && !(a.t_only && half == 1)) {
     // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
     float *out = (half ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
     const uint32_t tx = tmem + lane_base + tm_x(half);
@@ -663,34 +726,327 @@ __global__ void __launch_bounds__(NT2, 1)
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
-size_t bytes_per_head(int n_seg, int64_t max_len) {
+// ------------------------------------------------------------------------------------------------
+// Kernel 3 (builds with per-token outputs): per (segment, head) -- the S half again, with outputs.
+//
+// Within a chunk, with S_p the state at the chunk start, gamma_t = exp(G_t) and Wm the rows of
+// effective writes (Wm = U - Wk S_p, the quantity whose scaled form is R), the post-update state
+// of token t is S_t = gamma_t S_p + sum_{s<=t} exp(G_t - G_s) k_s Wm_s^T, so
+//   o_t^T = q_t^T S_t:   O^T = S_p^T Q^T diag(gamma) + Wm^T M^T,  M_ts = exp(G_t - G_s) q_t.k_s (s <= t).
+// This kernel runs the S-half chain of chain_tc_kernel and adds the two output products: the
+// inter-chunk one reuses the state pieces the P product reads (A = S_p^T hi and lo, both kept in
+// tensor memory here; B = the chunk's Q tile, exact bf16, K-major), the intra-chunk one takes
+// Wm^T in bf16 hi + lo pieces (A, tensor memory) and M from the prep kernel's record (B).  The
+// outputs of chunk c are read out (scaled by gamma_t, summed) while chunk c + 1's P product runs;
+// gamma_t is read from the workspace record, which stays unchanged while the stage is refilled.
+// T_C comes from chain_tc_kernel, run for the T half only; this kernel writes S_{C|0} and o.
+constexpr uint32_t SO_K = 0, SO_V = 16384, SO_Q = 32768, SO_REC = 49152, SO_M = SO_REC + WS_TILES;
+constexpr uint32_t SO_STAGE = SO_M + 16384;  // 112 KB
+constexpr uint32_t SO_SMEM = 2 * SO_STAGE + 1024;
+constexpr uint32_t SO_X = 0, SO_XH = 128, SO_XL = 192, SO_P = 256, SO_OI = 320, SO_OA = 384, SO_WM = 448;
+constexpr int SO_NT = 256 + 64;  // converters + MMA warp + TMA warp
+
+__global__ void __launch_bounds__(SO_NT, 1)
+    chain_so_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                    const __grid_constant__ CUtensorMap mapQ, BuildTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  // rd: the converters have read chunk c's outputs out (the output accumulators may be reused)
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1, bar_r2, bar_p, bar_x, bar_o, bar_rd;
+  __shared__ __align__(16) float s_sc[2][WS_SCG_BYTES / 4];  // scales, gamma_C, gamma_t per stage
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const bool issuer = warp == 8, producer = warp == 9;
+  const int row = tid & 127, part = (tid >> 7) & 1;
+  const int hh = blockIdx.x % a.Hb;
+  const int s = blockIdx.x / a.Hb;
+  const int h = a.h0 + hh;
+  int64_t beg, end;
+  if (!seg_bounds(a, s, beg, end)) return;  // reported by chain_tc_kernel
+  const int nchunks = (int)((end - beg + C - 1) / C);
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    mbar_init(&bar_r1, 256);
+    mbar_init(&bar_r2, 256);
+    mbar_init(&bar_p, 1);
+    mbar_init(&bar_x, 1);
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_rd, 256);
+    mbar_fence_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+  if (producer) {
+    if (lane == 0) {
+      prefetch_tmap(&mapK);
+      prefetch_tmap(&mapV);
+      prefetch_tmap(&mapQ);
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c & 1;
+        if (c >= 2 && !(ok = mbar_wait_cycles(&bar_empty[st], (uint32_t)((c >> 1) - 1) & 1u, a.err))) break;
+        const int rowt = (int)(beg + (int64_t)c * C);
+        uint8_t *stg = sm + st * SO_STAGE;
+        const uint8_t *rec = ws_rec(a, s, c, hh);
+        mbar_arrive_expect_tx(&bar_full[st], 3u * 16384u + WS_TILES + 16384u + WS_SCG_BYTES);
+        tma_load_2d(stg + SO_K, &mapK, &bar_full[st], h * D, rowt);
+        tma_load_2d(stg + SO_K + 8192, &mapK, &bar_full[st], h * D + 64, rowt);
+        tma_load_2d(stg + SO_V, &mapV, &bar_full[st], h * D, rowt);
+        tma_load_2d(stg + SO_V + 8192, &mapV, &bar_full[st], h * D + 64, rowt);
+        tma_load_2d(stg + SO_Q, &mapQ, &bar_full[st], h * D, rowt);
+        tma_load_2d(stg + SO_Q + 8192, &mapQ, &bar_full[st], h * D + 64, rowt);
+        bulk_load(stg + SO_REC, rec, WS_TILES, &bar_full[st]);
+        bulk_load(stg + SO_M, rec + WS_MH, 16384, &bar_full[st]);
+        bulk_load(&s_sc[st][0], rec + WS_SC, WS_SCG_BYTES, &bar_full[st]);
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (issuer) {
+    if (lane == 0) {
+      const uint32_t id_u = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = V^T (MN-major), B K-major
+      const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces, B = Wk^T (MN-major)
+      const uint32_t id_k = idesc_f32acc(1, 1, 0, 0, 128, 64);   // A = TMEM pieces, B K-major (Q, M)
+      const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces, B = K (MN-major)
+      auto stage_ready = [&](int c) -> bool {
+        const uint32_t stg = sb + (c & 1) * SO_STAGE;
+        if (!mbar_wait_cycles(&bar_full[c & 1], ((uint32_t)c >> 1) & 1u, a.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t av = sdesc_sw128(stg + SO_V + kk * 2048, 8192, 1024);
+          mma_f16(tmem + SO_P, av, sdesc_sw128(stg + SO_REC + WS_AVH + kk * 32, 16, 1024), id_u, kk > 0);
+          mma_f16(tmem + SO_P, av, sdesc_sw128(stg + SO_REC + WS_AVL + kk * 32, 16, 1024), id_u, 1);
+        }
+        return true;
+      };
+      bool ok = nchunks == 0 || stage_ready(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const uint32_t par = (uint32_t)c & 1u;
+        const uint32_t stg = sb + (c & 1) * SO_STAGE;
+        if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
+        tc_fence_after();
+        // P^T += X^T Wk^T (hi.hi + hi.lo + lo.hi), then O_inter^T = X^T Q^T (hi + lo; Q exact)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t wh = sdesc_sw128(stg + SO_REC + WS_WH + kk * 2048, 16384, 1024);
+          const uint64_t wl = sdesc_sw128(stg + SO_REC + WS_WL + kk * 2048, 16384, 1024);
+          mma_f16_tmem_a(tmem + SO_P, tmem + SO_XH + kk * 8, wh, id_p, 1);
+          mma_f16_tmem_a(tmem + SO_P, tmem + SO_XH + kk * 8, wl, id_p, 1);
+          mma_f16_tmem_a(tmem + SO_P, tmem + SO_XL + kk * 8, wh, id_p, 1);
+        }
+        mma_commit(&bar_p);
+        // the previous chunk's outputs must have been read out before the accumulators are reused
+        if (c > 0 && !(ok = mbar_wait_cycles(&bar_rd, par ^ 1u, a.err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bq = sdesc_sw128(stg + SO_Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XH + kk * 8, bq, id_k, kk > 0);
+          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XL + kk * 8, bq, id_k, 1);
+        }
+        if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
+        tc_fence_after();
+        // X^T += R^T K, then O_intra^T = Wm^T M^T (hi.hi + hi.lo + lo.hi)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bk = sdesc_sw128(stg + SO_K + kk * 2048, 8192, 1024);
+          const uint32_t pc = tmem + SO_P + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_f16_tmem_a(tmem + SO_X, pc, bk, id_x, 1);
+          mma_f16_tmem_a(tmem + SO_X, pc + 16, bk, id_x, 1);
+        }
+        mma_commit(&bar_x);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t mh = sdesc_sw128(stg + SO_M + kk * 32, 16, 1024);
+          const uint64_t ml = sdesc_sw128(stg + SO_M + 8192 + kk * 32, 16, 1024);
+          const uint32_t wc = tmem + SO_WM + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_f16_tmem_a(tmem + SO_OA, wc, mh, id_k, kk > 0);
+          mma_f16_tmem_a(tmem + SO_OA, wc, ml, id_k, 1);
+          mma_f16_tmem_a(tmem + SO_OA, wc + 16, mh, id_k, 1);
+        }
+        mma_commit(&bar_o);
+        mma_commit(&bar_empty[c & 1]);
+        if (c + 1 < nchunks && !(ok = stage_ready(c + 1))) break;
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ conversion warps (0-7)
+    const uint32_t tx = tmem + lane_base + SO_X, tp = tmem + lane_base + SO_P;
+    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = 0.f;
+      tmem_st16(tx + c0, v);
+    }
+    tmem_st_wait();
+    // Outputs of chunk cc: o_t[j] = gamma_t O_inter[j][t] + O_intra[j][t], this thread's 32 t.
+    auto readout = [&](int cc) {
+      float oi[32], oa[32];
+      tmem_ld32(tmem + lane_base + SO_OI + 32 * part, oi);
+      tmem_ld32(tmem + lane_base + SO_OA + 32 * part, oa);
+      const int64_t t0 = beg + (int64_t)cc * C;
+      const float *gam = reinterpret_cast<const float *>(ws_rec(a, s, cc, hh) + WS_GAM);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int t = 32 * part + q;
+        if (t0 + t < end) a.o_out[((size_t)(t0 + t) * a.H + h) * D + row] = fmaf(gam[t], oi[q], oa[q]);
+      }
+    };
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c & 1;
+      const uint32_t par = (uint32_t)c & 1u;
+      if (c > 0 && !(ok = mbar_wait_cycles(&bar_x, par ^ 1u, a.err))) break;  // previous update done
+      if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
+      tc_fence_after();
+      const float *sR = s_sc[st];
+      const float gamma_C = sR[C];
+      // (1) X^T (= S_p^T) -> hi and lo pieces in tensor memory; gamma_C X^T back.
+#pragma unroll
+      for (int cb = 0; cb < 64; cb += 32) {
+        float xv[32];
+        tmem_ld32(tx + 64 * part + cb, xv);
+        float ph[16], pl[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          uint32_t hi, lo;
+          split2_pair(xv[2 * q], xv[2 * q + 1], hi, lo);
+          ph[q] = __uint_as_float(hi);
+          pl[q] = __uint_as_float(lo);
+        }
+        tmem_st16(tmem + lane_base + SO_XH + (64 * part + cb) / 2, ph);
+        tmem_st16(tmem + lane_base + SO_XL + (64 * part + cb) / 2, pl);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) xv[q] *= gamma_C;
+        tmem_st32(tx + 64 * part + cb, xv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_r1);
+      if (c > 0) {
+        // chunk c - 1's outputs, while this chunk's P product runs
+        if (!(ok = mbar_wait_cycles(&bar_o, par ^ 1u, a.err))) break;
+        tc_fence_after();
+        readout(c - 1);
+        tc_fence_before();
+        mbar_arrive(&bar_rd);
+      }
+      // (2) Wm^T = -(P^T - U^T): R^T = Wm^T diag(exp(G_C - G_t)) pieces in place, Wm^T pieces aside.
+      if (!(ok = mbar_wait_cycles(&bar_p, par, a.err))) break;
+      tc_fence_after();
+      {
+        float pv[32];
+        tmem_ld32(tp + 32 * part, pv);
+        float rh[16], rl[16], wh[16], wl[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int t = 32 * part + 2 * q;
+          uint32_t hi, lo;
+          split2_pair(-pv[2 * q] * sR[t], -pv[2 * q + 1] * sR[t + 1], hi, lo);
+          rh[q] = __uint_as_float(hi);
+          rl[q] = __uint_as_float(lo);
+          split2_pair(-pv[2 * q], -pv[2 * q + 1], hi, lo);
+          wh[q] = __uint_as_float(hi);
+          wl[q] = __uint_as_float(lo);
+        }
+        tmem_st16(tp + 32 * part, rh);
+        tmem_st16(tp + 32 * part + 16, rl);
+        tmem_st16(tmem + lane_base + SO_WM + 32 * part, wh);
+        tmem_st16(tmem + lane_base + SO_WM + 32 * part + 16, wl);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_r2);
+    }
+    if (ok && nchunks > 0) {
+      if ((ok = mbar_wait_cycles(&bar_o, (uint32_t)(nchunks - 1) & 1u, a.err))) {
+        tc_fence_after();
+        readout(nchunks - 1);
+      }
+    }
+    if (ok) {
+      // S_{C|0}: X^T lane j holds column j; this thread's 64 rows i.
+      float *out = a.S_out + ((size_t)s * a.H + h) * D * D;
+#pragma unroll
+      for (int cb = 0; cb < 64; cb += 32) {
+        float xv[32];
+        tmem_ld32(tx + 64 * part + cb, xv);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) out[(size_t)(64 * part + cb + q) * D + row] = xv[q];
+      }
+    }
+    if (!ok) abort_flag = 1;
+  }
+  __syncthreads();
+  if (abort_flag && tid == 0) {
+    for (int k = 0; k < 2; ++k) {
+      mbar_wait_cycles(&bar_o, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_rd, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_x, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_p, (uint32_t)k, nullptr, 100000000LL);
+      for (int i = 0; i < 2; ++i) {
+        mbar_wait_cycles(&bar_full[i], (uint32_t)k, nullptr, 100000000LL);
+        mbar_wait_cycles(&bar_empty[i], (uint32_t)k, nullptr, 100000000LL);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+size_t bytes_per_head(int n_seg, int64_t max_len, bool want_o) {
   const int64_t chunks = (max_len + C - 1) / C;
-  return (size_t)n_seg * (size_t)(chunks > 0 ? chunks : 1) * WS_REC;
+  return (size_t)n_seg * (size_t)(chunks > 0 ? chunks : 1) * (want_o ? WS_REC_O : WS_REC);
 }
 
 }  // namespace
 
 bool build_tc_supported(int D_, int fam, int in_dtype, bool want_o) {
-  return D_ == D && in_dtype == HYPIC_BF16 && !want_o &&
-         (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
+  (void)want_o;  // with or without per-token outputs
+  return D_ == D && in_dtype == HYPIC_BF16 && (fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GATED_DELTA);
 }
 
-size_t build_tc_min_workspace(int n_seg, int64_t max_len) { return bytes_per_head(n_seg, max_len); }
+size_t build_tc_min_workspace(int n_seg, int64_t max_len, bool want_o) {
+  return bytes_per_head(n_seg, max_len, want_o);
+}
 
-size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len) {
+size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o) {
   if (H <= 0 || n_seg <= 0) return 0;
-  const size_t per = bytes_per_head(n_seg, max_len);
+  const size_t per = bytes_per_head(n_seg, max_len, want_o);
   size_t heads = WS_CAP / per;
   if (heads < 1) heads = 1;
   if (heads > (size_t)H) heads = (size_t)H;
   return heads * per;
 }
 
-// Runs the build over head blocks that fit the workspace: prep then chain for each block.
+// Runs the build over head blocks that fit the workspace: prep then chain for each block (and,
+// with per-token outputs, the S chain that emits them).
 cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, cudaStream_t st) {
-  const size_t per = bytes_per_head(r.n_seg, r.seg.max_len);
-  const int Hb = (int)((ws_bytes / per) < (size_t)r.H ? ws_bytes / per : (size_t)r.H);
-  if (Hb < 1 || ws == nullptr) return cudaErrorMemoryAllocation;
+  const bool wo = r.o_out != nullptr;
+  const size_t per = bytes_per_head(r.n_seg, r.seg.max_len, wo);
+  const int hb_max = (int)((ws_bytes / per) < (size_t)r.H ? ws_bytes / per : (size_t)r.H);
+  if (hb_max < 1 || ws == nullptr) return cudaErrorMemoryAllocation;
+  // as few blocks as the workspace allows, of equal size (no small tail block)
+  const int nblk = (r.H + hb_max - 1) / hb_max;
+  const int Hb = (r.H + nblk - 1) / nblk;
   BuildTcArgs a{};
   a.H = r.H;
   a.n_seg = r.n_seg;
@@ -705,26 +1061,42 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
   a.beta = r.src.beta;
   a.T_out = r.T_out;
   a.S_out = r.S_out;
+  a.o_out = r.o_out;
   a.ws = static_cast<uint8_t *>(ws);
+  a.rec_bytes = wo ? WS_REC_O : WS_REC;
+  a.t_only = wo ? 1 : 0;
   a.err = r.err;
   const uint64_t n_tok = r.seg.n_tokens < 0 ? (uint64_t)1 << 31 : (uint64_t)r.seg.n_tokens;
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mq;
   if (!make_tmap_bf16_2d(&mk, r.src.k, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
     return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&mv, r.src.v, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(wy_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+  if (wo) {
+    if (!make_tmap_bf16_2d(&mq, r.src.q, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
+      return cudaErrorInvalidValue;
+  } else {
+    mq = mk;  // not read
+  }
+  cudaError_t e = wo ? cudaFuncSetAttribute(wy_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_O)
+                     : cudaFuncSetAttribute(wy_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if (wo) {
+    e = cudaFuncSetAttribute(chain_so_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SO_SMEM);
+    if (e != cudaSuccess) return e;
+  }
   for (int h0 = 0; h0 < r.H; h0 += Hb) {
     a.h0 = h0;
     a.Hb = (r.H - h0) < Hb ? (r.H - h0) : Hb;
     const long long g1 = (long long)r.n_seg * a.max_chunks * a.Hb;
     const long long g2 = (long long)r.n_seg * a.Hb;
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    wy_prep_kernel<<<(unsigned)g1, NT, P_SMEM, st>>>(mk, a);
+    if (wo) wy_prep_kernel<true><<<(unsigned)g1, NT, P_SMEM_O, st>>>(mk, mq, a);
+    else wy_prep_kernel<false><<<(unsigned)g1, NT, P_SMEM, st>>>(mk, mq, a);
     chain_tc_kernel<<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+    if (wo) chain_so_kernel<<<(unsigned)g2, SO_NT, SO_SMEM, st>>>(mk, mv, mq, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

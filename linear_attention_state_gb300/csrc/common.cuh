@@ -52,12 +52,12 @@ struct RecurrentArgs {
 };
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t st);
 
-// Chunked tcgen05 build (d = 128, bf16 inputs, delta families, no per-token outputs).
+// Chunked tcgen05 build (d = 128, bf16 inputs, delta families, with or without per-token outputs).
 // The workspace holds per-(chunk, head) operand records; the build runs over blocks
 // of heads that fit in the workspace it is given (at least one head).
 bool build_tc_supported(int D, int fam, int in_dtype, bool want_o);
-size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len);  // preferred size
-size_t build_tc_min_workspace(int n_seg, int64_t max_len);          // one head
+size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o);  // preferred size
+size_t build_tc_min_workspace(int n_seg, int64_t max_len, bool want_o);          // one head
 cudaError_t launch_build_tc(const RecurrentArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Tensor-core build for the scalar and diagonal decay families (d = 128, bf16 inputs, no

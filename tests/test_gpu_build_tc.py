@@ -14,7 +14,7 @@ import torch
 
 import linear_attention_state_gb300 as hy
 import workloads as W
-from refs import TOL_BF16, host_tokens, np64, ref_pair, relerr
+from refs import TOL_BF16, host_tokens, np64, ref_pair, ref_run, relerr
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -101,3 +101,53 @@ def test_tensor_core_path_agrees_with_recurrent_path(monkeypatch):
             assert relerr(np64(S[s, h]), np64(S2[s, h])) <= TOL_BF16
             assert relerr(np64(T[s, h]), np64(T2[s, h]), tau=1e-30) <= TOL_BF16
     assert os.environ.get("HYPIC_BUILD_PATH") is None
+
+
+# ---- builds that also emit per-token outputs (o_t = q_t^T S_t from the zero state) ----------
+
+@pytest.mark.parametrize("family", ["delta", "gated_delta"])
+def test_ragged_bodies_with_outputs(family):
+    lens = [0, 1, 37, 63, 64, 65, 128, 200, 1000]
+    H, gap = 3, 7
+    n = sum(lens) + gap * (len(lens) + 1)
+    g = W.generator(DEV, 6300, 1 if family == "delta" else 2)
+    tok = W.draw_tokens(g, n, H, 128, family, "bf16", DEV)
+    bounds, off = [], gap
+    for L_ in lens:
+        bounds.append((off, off + L_))
+        off += L_ + gap
+    T, S, o = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                       tok["beta"], q=tok["q"], family=family, want_o=True)
+    assert hy.stream_status() == 0
+    host = host_tokens(tok, list(range(H)))
+    eT = eS = eO = 0.0
+    for s, (b, e) in enumerate(bounds):
+        for h in range(H):
+            Tr, Sr = ref_pair(family, host, h, b, e)
+            eT = max(eT, relerr(np64(T[s, h]), Tr))
+            if e > b:
+                eS = max(eS, relerr(np64(S[s, h]), Sr))
+                _, orf = ref_run(family, host, h, b, e, want_o=True)
+                eO = max(eO, relerr(np64(o[b:e, h]), orf))
+    print(f"{family} with outputs: T {eT:.2e} S {eS:.2e} o {eO:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16 and eO <= TOL_BF16
+    # tokens outside every body keep the zeros the binding put there
+    assert float(o[:gap].abs().max()) == 0.0
+
+
+def test_outputs_agree_with_recurrent_path(monkeypatch):
+    lens = [300, 64, 5]
+    H = 2
+    n = sum(lens) + 8
+    g = W.generator(DEV, 6301, 0)
+    tok = W.draw_tokens(g, n, H, 128, "gated_delta", "bf16", DEV)
+    bounds = torch.tensor([(0, 300), (300, 364), (364, 369)], device=DEV)
+    _, _, o1 = hy.segment_build_batched(tok["k"], tok["v"], bounds, tok["alpha"], tok["beta"], q=tok["q"],
+                                        family="gated_delta", want_o=True)
+    monkeypatch.setenv("HYPIC_BUILD_PATH", "recurrent")
+    _, _, o2 = hy.segment_build_batched(tok["k"], tok["v"], bounds, tok["alpha"], tok["beta"], q=tok["q"],
+                                        family="gated_delta", want_o=True)
+    monkeypatch.delenv("HYPIC_BUILD_PATH")
+    assert hy.stream_status() == 0
+    for h in range(H):
+        assert relerr(np64(o1[:369, h]), np64(o2[:369, h])) <= TOL_BF16

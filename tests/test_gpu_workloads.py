@@ -245,3 +245,23 @@ def test_long_mixed_full_size_sampled_heads():
     print(f"long mixed: S {wS:.2e} seams {wo:.2e}")
     del pool_T, pool_S
     assert max(wS, wo) <= TOL_BF16
+
+
+def test_build_32k_with_outputs_sampled_heads():
+    """The 32k-token build emitting every body token's output (the cold-segment forward fused
+    with pair construction): outputs of two sampled heads against the oracle run per body."""
+    w = W.BUILD_32K
+    tok = w.draw_request(DEV)
+    bounds = w.body_bounds()
+    T, S, o = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                       tok["beta"], q=tok["q"], family=w.family, max_len=w.seg_len, want_o=True)
+    assert hy.stream_status() == 0
+    heads = [0, w.H - 1]
+    host = host_tokens(tok, heads)
+    worst = 0.0
+    for i, h in enumerate(heads):
+        for (b, e) in bounds[:3]:
+            _, orf = ref_run(w.family, host, i, b, e, want_o=True)
+            worst = max(worst, relerr(np64(o[b:e, h]), orf))
+    print(f"build 32k outputs: {worst:.2e}")
+    assert worst <= TOL_BF16

@@ -44,6 +44,53 @@ __device__ void rope_table(float *cs, float *sn, int half, int r, double base, l
   }
 }
 
+// 16-byte groups of one element type: 8 bf16 or 4 fp32.
+template <typename T>
+struct Vec {
+  static constexpr int N = 16 / sizeof(T);
+  uint4 raw;
+  __device__ __forceinline__ float get(int i) const { return to_f32<T>(reinterpret_cast<const T *>(&raw)[i]); }
+  __device__ __forceinline__ void set(int i, float x) { reinterpret_cast<T *>(&raw)[i] = from_f32<T>(x); }
+};
+
+// Vectorised form for rows whose rotated half and pass-through part are whole 16-byte groups
+// (16-byte aligned rows): one thread turns N consecutive pairs.
+template <typename T>
+__global__ void __launch_bounds__(NT) rope_shift_vec_kernel(const T *__restrict__ in, T *__restrict__ out,
+                                                            int64_t rows, int d, int r, double base, long long delta) {
+  __shared__ float cs[MAX_HALF], sn[MAX_HALF];
+  constexpr int N = Vec<T>::N;
+  const int half = r / 2;
+  rope_table(cs, sn, half, r, base, delta);
+  __syncthreads();
+  const int gpr = half / N + (in != out ? (d - r) / N : 0);  // 16-byte groups per row
+  const int64_t total = rows * gpr;
+  for (int64_t e = (int64_t)blockIdx.x * NT + threadIdx.x; e < total; e += (int64_t)gridDim.x * NT) {
+    const int64_t row = e / gpr;
+    const int g = (int)(e - row * gpr);
+    const T *src = in + row * d;
+    T *dst = out + row * d;
+    if (g < half / N) {
+      const int i0 = g * N;
+      Vec<T> x, y;
+      x.raw = *reinterpret_cast<const uint4 *>(src + i0);
+      y.raw = *reinterpret_cast<const uint4 *>(src + i0 + half);
+      Vec<T> xo, yo;
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const float a = x.get(q), b = y.get(q), c = cs[i0 + q], sv = sn[i0 + q];
+        xo.set(q, c * a - sv * b);
+        yo.set(q, sv * a + c * b);
+      }
+      *reinterpret_cast<uint4 *>(dst + i0) = xo.raw;
+      *reinterpret_cast<uint4 *>(dst + i0 + half) = yo.raw;
+    } else {
+      const int c0 = r + (g - half / N) * N;
+      *reinterpret_cast<uint4 *>(dst + c0) = *reinterpret_cast<const uint4 *>(src + c0);
+    }
+  }
+}
+
 // Rows of length d (token x head); rotated pairs then the pass-through dims.
 template <typename T>
 __global__ void __launch_bounds__(NT) rope_shift_kernel(const T *__restrict__ in, T *__restrict__ out, int64_t rows,
@@ -67,6 +114,29 @@ __global__ void __launch_bounds__(NT) rope_shift_kernel(const T *__restrict__ in
       const int c = r + (i - half);
       dst[c] = src[c];
     }
+  }
+}
+
+// S [mats, dk, dv] in place, 4 columns per thread (dv a multiple of 4).
+__global__ void __launch_bounds__(NT) state_rerotate_vec_kernel(float *__restrict__ S, int64_t mats, int dk, int dv,
+                                                                int r, double base, long long delta) {
+  __shared__ float cs[MAX_HALF], sn[MAX_HALF];
+  const int half = r / 2;
+  rope_table(cs, sn, half, r, base, delta);
+  __syncthreads();
+  const int q4 = dv / 4;
+  const int64_t per_mat = (int64_t)half * q4;
+  const int64_t total = mats * per_mat;
+  for (int64_t e = (int64_t)blockIdx.x * NT + threadIdx.x; e < total; e += (int64_t)gridDim.x * NT) {
+    const int64_t m = e / per_mat;
+    const int rem = (int)(e - m * per_mat);
+    const int i = rem / q4, j = 4 * (rem - i * q4);
+    float4 *px = reinterpret_cast<float4 *>(S + (m * dk + i) * dv + j);
+    float4 *py = reinterpret_cast<float4 *>(S + (m * dk + i + half) * dv + j);
+    const float4 x = *px, y = *py;
+    const float c = cs[i], sv = sn[i];
+    *px = make_float4(c * x.x - sv * y.x, c * x.y - sv * y.y, c * x.z - sv * y.z, c * x.w - sv * y.w);
+    *py = make_float4(sv * x.x + c * y.x, sv * x.y + c * y.y, sv * x.z + c * y.z, sv * x.w + c * y.w);
   }
 }
 
@@ -148,6 +218,19 @@ cudaError_t launch_rope_shift(const void *in, void *out, int64_t rows, int d, in
                               int dtype, cudaStream_t st) {
   const int64_t total = rows * (r / 2 + (in != out ? d - r : 0));
   if (total <= 0) return cudaSuccess;
+  const int n = dtype == HYPIC_BF16 ? 8 : 4;  // elements per 16-byte group
+  const bool vec = (r / 2) % n == 0 && (d - r) % n == 0 && d % n == 0 &&
+                   (reinterpret_cast<uintptr_t>(in) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+  if (vec) {
+    const int64_t groups = rows * ((r / 2) / n + (in != out ? (d - r) / n : 0));
+    if (dtype == HYPIC_BF16)
+      rope_shift_vec_kernel<__nv_bfloat16><<<grid_for(groups), NT, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(in), static_cast<__nv_bfloat16 *>(out), rows, d, r, base, delta);
+    else
+      rope_shift_vec_kernel<float><<<grid_for(groups), NT, 0, st>>>(static_cast<const float *>(in),
+                                                                    static_cast<float *>(out), rows, d, r, base, delta);
+    return cudaGetLastError();
+  }
   if (dtype == HYPIC_BF16)
     rope_shift_kernel<__nv_bfloat16><<<grid_for(total), NT, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(in), static_cast<__nv_bfloat16 *>(out), rows, d, r, base, delta);
@@ -161,6 +244,10 @@ cudaError_t launch_state_rerotate(float *S, int64_t mats, int dk, int dv, int r,
                                   cudaStream_t st) {
   const int64_t total = mats * (r / 2) * dv;
   if (total <= 0) return cudaSuccess;
+  if (dv % 4 == 0 && (reinterpret_cast<uintptr_t>(S) & 15) == 0) {
+    state_rerotate_vec_kernel<<<grid_for(total / 4), NT, 0, st>>>(S, mats, dk, dv, r, base, delta);
+    return cudaGetLastError();
+  }
   state_rerotate_kernel<<<grid_for(total), NT, 0, st>>>(S, mats, dk, dv, r, base, delta);
   return cudaGetLastError();
 }

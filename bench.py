@@ -42,6 +42,11 @@ BUILD_TC_TRAFFIC = 277_341_000 + 749_664_256 + 1_349_144_000 + 27_557_632
 # The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from the capture
 # summarised in profiles/build_decay_tc_32h_d128_64x512.md.
 DECAY_TC_TRAFFIC = {"scalar_const": 536_935_000 + 112_331_264, "diag": 1_073_959_000 + 122_754_304}
+# The same for compose_tc_kernel on the full warm-cache workload (generator-drawn pool of 256 x 960
+# pairs, 64 requests x 16), from the one-pass capture in profiles/compose_tc_pool16_B64x8.md: the
+# pool is re-read from L2, so DRAM traffic is far below the 128 KiB (fp32) / 64 KiB (bf16)
+# algorithmic bytes per composition.
+COMPOSE_TC_TRAFFIC = {"f32": 42_967_890_944 + 4_018_890_752, "bf16": 16_075_031_808 + 4_012_372_736}
 
 
 def load_peaks():
@@ -426,7 +431,7 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
     out = torch.empty((pw.B, H, d, d), device=dev)
     comps = pw.B * pw.n * H
 
-    def timed(pT, pS, bytes_per_comp, name):
+    def timed(pT, pS, bytes_per_comp, name, traffic):
         torch.cuda.synchronize()
 
         def fn(ev):
@@ -443,18 +448,19 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
         return {"workload": name, "compositions_per_s": comps / (total_ms / 1e3 / steps),
                 "ms_per_step": total_ms / steps,
                 "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                             "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"],
+                             "traffic": traffic if (pool is None and n is None) else None,
                              "bytes_per_composition": bytes_per_comp, "peak_source": peaks["source"]},
                 "status": hy.stream_status()}
 
     res = None
     if storage in ("f32", "both"):
-        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION, pw.name)
+        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION, pw.name, COMPOSE_TC_TRAFFIC["f32"])
     if storage in ("bf16", "both"):
         T_lp, S_lp = hy.pairs_to_bf16(pool_T, pool_S, family="gated_delta")
         del pool_T, pool_S
         torch.cuda.empty_cache()
-        lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2, pw.name + "_bf16pairs")
+        lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2, pw.name + "_bf16pairs", COMPOSE_TC_TRAFFIC["bf16"])
         del T_lp, S_lp
         if res is None:
             res = lp

@@ -254,9 +254,11 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
-    fence_proxy_async();  // B pieces are read by the MMA; the staging buffer is refilled by TMA
-    tc_fence_before();
-    __syncthreads();
+    if (!PB) {
+      fence_proxy_async();  // B pieces are read by the MMA; the staging buffer is refilled by TMA
+      tc_fence_before();
+      __syncthreads();
+    }
     if (tid == 0) {
       tc_fence_after();
       // fp32: the staging buffer is consumed.  bf16: the other buffer's MMAs (step - 1) are done.
@@ -287,24 +289,39 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       mma_commit(&bar_m);
-      if (!mbar_wait_cycles(&bar_m, ph, a.err)) abort_flag = 1;
-      if (addend && !mbar_wait_cycles(&bar_s, ph, a.err)) abort_flag = 1;
     }
+    // While the MMAs run, every thread loads its rows of S_{C|0} column j into x (the state itself
+    // now lives in tensor memory as the A pieces, so x is free).
+    if (addend) {
+      int got = 1;
+      if ((tid & 31) == 0) got = mbar_wait_cycles(&bar_s, ph, a.err) ? 1 : 0;
+      __syncwarp();
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) abort_flag = 1;
+      if (PB) {
+        const __nv_bfloat16 *s0b = reinterpret_cast<const __nv_bfloat16 *>(sS0);
+#pragma unroll
+        for (int r = 0; r < R; ++r) x[r] = __bfloat162float(s0b[(i0 + r) * D + j]);
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) x[r] = sS0[(i0 + r) * D + j];
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) x[r] = 0.f;
+    }
+    if (tid == 0 && !mbar_wait_cycles(&bar_m, ph, a.err)) abort_flag = 1;
     __syncthreads();
     tc_fence_after();
     if (abort_flag) break;
 
-    // (3) Epilogue: rows i0.. of column j of S_new = D row j (+ S_{C|0}).
-    tmem_ld64(tmem + lane_base + TM_D + i0, x);
-    if (addend) {
-      if (PB) {
-        const __nv_bfloat16 *s0b = reinterpret_cast<const __nv_bfloat16 *>(sS0);
+    // (3) Epilogue: rows i0.. of column j of S_new = D row j + S_{C|0}.
 #pragma unroll
-        for (int r = 0; r < R; ++r) x[r] += __bfloat162float(s0b[(i0 + r) * D + j]);
-      } else {
+    for (int hb = 0; hb < R; hb += 32) {
+      float dv[32];
+      tmem_ld32(tmem + lane_base + TM_D + i0 + hb, dv);
 #pragma unroll
-        for (int r = 0; r < R; ++r) x[r] += sS0[(i0 + r) * D + j];
-      }
+      for (int r = 0; r < 32; ++r) x[hb + r] += dv[r];
     }
     if (a.scan) {
       float *rec = (isT ? a.T_rec : a.S_rec) + ((size_t)step * H + h) * D * D;

@@ -77,7 +77,6 @@ struct BuildTcArgs {
   float *o_out;  // [tokens, H, D] or null
   uint8_t *ws;
   uint32_t rec_bytes;  // WS_REC, or WS_REC_O with outputs
-  int t_only;          // chain_tc_kernel runs the T half only (the S half comes from chain_so_kernel)
   int *err;
 };
 
@@ -483,6 +482,7 @@ __device__ __forceinline__ void split2_pair(float a, float b, uint32_t &hi, uint
   lo = *reinterpret_cast<const uint32_t *>(&lp);
 }
 
+template <bool T_ONLY>
 __global__ void __launch_bounds__(NT2, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     BuildTcArgs a) {
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(NT2, 1)
         const uint32_t stg = sb + st * STAGE_BYTES;
         if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err)) return false;
         tc_fence_after();
-        if (a.t_only) return true;
+        if (T_ONLY) return true;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t av = sdesc_sw128(stg + STAGE_V + kk * 2048, 8192, 1024);
@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(NT2, 1)
         const uint32_t par = (uint32_t)c & 1u;
         const uint32_t stg = sb + (c & 1) * STAGE_BYTES;
         // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
-        const int nh = a.t_only ? 1 : 2;
+        constexpr int nh = T_ONLY ? 1 : 2;
         for (int hf = 0; hf < nh && ok; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
           tc_fence_after();
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(NT2, 1)
     }
     tmem_st_wait();
     bool ok = true;
-    const int my_chunks = (a.t_only && half == 1) ? 0 : nchunks;
+    const int my_chunks = (T_ONLY && half == 1) ? 0 : nchunks;
     for (int c = 0; c < my_chunks && ok; ++c) {
       const int st = c & 1;
       const uint32_t par = (uint32_t)c & 1u;
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(NT2, 1)
         mbar_wait_cycles(&bar_empty[i], (uint32_t)k, nullptr, 100000000LL);
       }
   }
-  if (!abort_flag && !issuer && !producer && !(a.t_only && half == 1)) {
+  if (!abort_flag && !issuer && !producer && !(T_ONLY && half == 1)) {
     // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
     float *out = (half ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
     const uint32_t tx = tmem + lane_base + tm_x(half);
@@ -1064,7 +1064,6 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
   a.o_out = r.o_out;
   a.ws = static_cast<uint8_t *>(ws);
   a.rec_bytes = wo ? WS_REC_O : WS_REC;
-  a.t_only = wo ? 1 : 0;
   a.err = r.err;
   const uint64_t n_tok = r.seg.n_tokens < 0 ? (uint64_t)1 << 31 : (uint64_t)r.seg.n_tokens;
   CUtensorMap mk, mv, mq;
@@ -1081,7 +1080,8 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
   cudaError_t e = wo ? cudaFuncSetAttribute(wy_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_O)
                      : cudaFuncSetAttribute(wy_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = wo ? cudaFuncSetAttribute(chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
+         : cudaFuncSetAttribute(chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (wo) {
     e = cudaFuncSetAttribute(chain_so_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SO_SMEM);
@@ -1095,7 +1095,8 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (wo) wy_prep_kernel<true><<<(unsigned)g1, NT, P_SMEM_O, st>>>(mk, mq, a);
     else wy_prep_kernel<false><<<(unsigned)g1, NT, P_SMEM, st>>>(mk, mq, a);
-    chain_tc_kernel<<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+    if (wo) chain_tc_kernel<true><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+    else chain_tc_kernel<false><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
     if (wo) chain_so_kernel<<<(unsigned)g2, SO_NT, SO_SMEM, st>>>(mk, mv, mq, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -84,6 +84,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t phase, i
 // for the default limit).
 __device__ __forceinline__ bool mbar_wait_cycles(uint64_t *bar, uint32_t phase, int *err,
                                                  long long limit = 2000000000LL) {
+  if (mbar_try_wait(bar, phase)) return true;  // already complete: no clock read
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, phase)) {
     if (clock64() - t0 > limit) {

@@ -562,52 +562,65 @@ __global__ void __launch_bounds__(NT2, 1)
       const uint32_t id_u = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = V^T (MN-major), B K-major
       const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces, B = Wk^T (MN-major)
       const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces (TMEM), B = K
+      // Shared-memory descriptors as a base per operand plus constant offsets: the address field
+      // holds addr >> 4 in its low 14 bits and no operand crosses 256 KB, so an offset of off
+      // bytes adds off >> 4 to the descriptor.
+      constexpr uint64_t DSTG = STAGE_BYTES >> 4;
+      const uint64_t dV = sdesc_sw128(sb + STAGE_V, 8192, 1024);
+      const uint64_t dK = sdesc_sw128(sb + STAGE_K, 8192, 1024);
+      const uint64_t dAVH = sdesc_sw128(sb + STAGE_REC + WS_AVH, 16, 1024);
+      const uint64_t dAVL = sdesc_sw128(sb + STAGE_REC + WS_AVL, 16, 1024);
+      const uint64_t dWH = sdesc_sw128(sb + STAGE_REC + WS_WH, 16384, 1024);
+      const uint64_t dWL = sdesc_sw128(sb + STAGE_REC + WS_WL, 16384, 1024);
+      const uint64_t dXL = sdesc_sw128(sb + OFF_XLO, 16, 1024);
       // -U^T of chunk c into the S half's P^T (M = 128 j, N = 64 t, K = 64 s).  It follows the
       // previous chunk's S update in the pipe, which has read the R^T pieces stored there.
       auto issue_u = [&](int c) -> bool {
         const int st = c & 1;
-        const uint32_t stg = sb + st * STAGE_BYTES;
         if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err)) return false;
         tc_fence_after();
         if (T_ONLY) return true;
+        const uint64_t so = st ? DSTG : 0;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t av = sdesc_sw128(stg + STAGE_V + kk * 2048, 8192, 1024);
-          mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVH + kk * 32, 16, 1024), id_u, kk > 0);
-          mma_f16(tmem + tm_p(1), av, sdesc_sw128(stg + STAGE_REC + WS_AVL + kk * 32, 16, 1024), id_u, 1);
+          const uint64_t av = dV + so + kk * 128;
+          mma_f16(tmem + tm_p(1), av, dAVH + so + kk * 2, id_u, kk > 0);
+          mma_f16(tmem + tm_p(1), av, dAVL + so + kk * 2, id_u, 1);
         }
         return true;
       };
       bool ok = nchunks == 0 || issue_u(0);
+      constexpr int nh = T_ONLY ? 1 : 2;
       for (int c = 0; c < nchunks && ok; ++c) {
         const uint32_t par = (uint32_t)c & 1u;
-        const uint32_t stg = sb + (c & 1) * STAGE_BYTES;
+        const uint64_t so = (c & 1) ? DSTG : 0;
         // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
-        constexpr int nh = T_ONLY ? 1 : 2;
-        for (int hf = 0; hf < nh && ok; ++hf) {
+#pragma unroll
+        for (int hf = 0; hf < nh; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
           tc_fence_after();
-          const uint32_t xlo = sb + OFF_XLO + hf * 32768;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t wh = sdesc_sw128(stg + STAGE_REC + WS_WH + kk * 2048, 16384, 1024);
-            const uint64_t wl = sdesc_sw128(stg + STAGE_REC + WS_WL + kk * 2048, 16384, 1024);
-            const uint64_t al = sdesc_sw128(xlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t wh = dWH + so + kk * 128;
+            const uint64_t wl = dWL + so + kk * 128;
+            const uint64_t al = dXL + hf * 2048 + (kk >> 2) * 1024 + (kk & 3) * 2;
             mma_f16_tmem_a(tmem + tm_p(hf), tmem + tm_xp(hf) + kk * 8, wh, id_p, (hf == 1 || kk > 0) ? 1u : 0u);
             mma_f16_tmem_a(tmem + tm_p(hf), tmem + tm_xp(hf) + kk * 8, wl, id_p, 1);
             mma_f16(tmem + tm_p(hf), al, wh, id_p, 1);
           }
           mma_commit(&bar_p[hf]);
         }
+        if (!ok) break;
         // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next chunk's -U^T
         // is queued right behind the S update, before its commit, so the pipe does not wait
         // for the commits; the S half's update barrier then also covers it.
-        for (int hf = 0; hf < nh && ok; ++hf) {
+#pragma unroll
+        for (int hf = 0; hf < nh; ++hf) {
           if (!(ok = mbar_wait_cycles(&bar_r2[hf], par, a.err))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bk = sdesc_sw128(stg + STAGE_K + kk * 2048, 8192, 1024);
+            const uint64_t bk = dK + so + kk * 128;
             const uint32_t pc = tmem + tm_p(hf) + 32 * (kk >> 1) + 8 * (kk & 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);

@@ -126,8 +126,13 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
  * processes the heads in blocks that fit the workspace it is given, so any size
  * that holds one head's records (n_seg * ceil(max_len / 64) * 49,664 bytes)
  * works, and less gives HYPIC_ENOSPACE.  The preferred size covers all heads up
- * to about 1 GiB.  The workspace is caller-owned device memory, 16-byte aligned,
- * and must not be used by anything else until the stream reaches the end of the call.
+ * to about 4 GiB of records, plus min(n_seg * heads, 256) * 131,072 + 3,072 bytes
+ * for the split chain schedule: with more (segment, head) units than the GPU holds
+ * chain CTAs at once, one CTA per SM runs an equal share of all chunks and a cut
+ * segment's two pairs are composed in the kernel (a cooperative launch).  Without
+ * that room each unit gets its own CTA; results agree to rounding either way.  The
+ * workspace is caller-owned device memory, 16-byte aligned, and must not be used
+ * by anything else until the stream reaches the end of the call.
  */
 size_t hypic_build_workspace_bytes(const hypic_shape *shape, int32_t n_seg, int64_t max_len);
 

@@ -22,7 +22,9 @@
 //     bf16, A diag(b gamma) split hi + lo).  Stored to the workspace as ready-made
 //     128-byte-swizzled operand tiles: Wk^T hi + lo, -A diag(b) hi + lo, and the
 //     per-token scales exp(G_C - G_t) and gamma_C.
-//   chain_tc_kernel (one CTA per segment and head): the state-dependent chain.  The
+//   chain_tc_kernel (one CTA per segment and head, or with more of those than the GPU
+//     holds at once, one CTA per SM running an equal share of all chunk steps, cut
+//     segments rejoined by composing their two pairs): the state-dependent chain.  The
 //     CTA keeps both 128 x 128 fp32 column halves of X (T and S, which evolve
 //     independently) in tensor memory for the whole segment, transposed.  Per chunk:
 //     TMA brings K, V and the chunk's record (double buffered); -U^T = V^T (-A diag(b))^T
@@ -35,6 +37,8 @@
 // exact in bf16) and every product accumulates in fp32 in TMEM.  Padded tokens of
 // a ragged last chunk get b = 0 and a = 1, which makes them exact identity steps.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "tc_ptx.cuh"
 #include "tma_host.h"
@@ -78,6 +82,13 @@ struct BuildTcArgs {
   uint8_t *ws;
   uint32_t rec_bytes;  // WS_REC, or WS_REC_O with outputs
   int *err;
+  // chain schedule: n_units = n_seg * Hb units of max_chunks steps, q_steps steps per chain CTA;
+  // with q_steps > max_chunks, per-CTA pair slots, their publish flags and the CTAs' schedule
+  // (both written by the prep kernel)
+  int n_units, q_steps, n_flags;
+  float *part;
+  int *flags;
+  int *sched;  // per chain CTA: its chunk steps, then 1 (ends on a cut unit's head) | 2 (bad bounds)
 };
 
 __device__ __forceinline__ bool seg_bounds(const BuildTcArgs &a, int s, int64_t &beg, int64_t &end) {
@@ -93,6 +104,62 @@ __device__ __forceinline__ bool seg_bounds(const BuildTcArgs &a, int s, int64_t 
 
 __device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, int hh) {
   return a.ws + (((size_t)s * a.max_chunks + c) * a.Hb + hh) * a.rec_bytes;
+}
+
+// Work of one chain CTA: the chunk steps [lo, hi) of a list that runs through the units (segment,
+// head) in order, max_chunks steps per unit (steps past a segment's end are empty).  With
+// q_steps == max_chunks each CTA owns one whole unit.  With more steps per CTA (a grid of one CTA
+// per SM, launched cooperatively so that all CTAs are resident together) a unit may be cut once,
+// between neighbouring CTAs b and b + 1: CTA b + 1 runs the unit's tail first and publishes its
+// pair (T_B, S_B) in slot b + 1; CTA b runs the unit's head last and finishes with the composition
+// X = T_B X_A + [0 | S_B] (the composition law of segment pairs) before writing the unit's result.
+enum : int { PIECE_WHOLE = 0, PIECE_HEAD = 1, PIECE_TAIL = 2, PIECE_NONE = 3 };
+struct Piece {
+  int s, hh;       // the unit
+  int64_t beg;     // first token of its body
+  int c_lo, c_hi;  // valid chunks [c_lo, c_hi) in this CTA's share
+  int kind;
+  bool ok;         // segment bounds valid
+};
+__device__ __forceinline__ Piece piece_of(const BuildTcArgs &a, long long u, long long lo, long long hi) {
+  Piece p;
+  p.s = (int)(u / a.Hb);
+  p.hh = (int)(u % a.Hb);
+  int64_t beg = 0, end = 0;
+  p.ok = seg_bounds(a, p.s, beg, end);
+  p.beg = beg;
+  const int nch = p.ok ? (int)((end - beg + C - 1) / C) : 0;
+  const long long u0 = u * a.max_chunks;
+  const long long s_lo = lo > u0 ? lo - u0 : 0;
+  const long long s_hi = hi - u0 < a.max_chunks ? hi - u0 : a.max_chunks;
+  p.c_lo = (int)(s_lo < nch ? s_lo : nch);
+  p.c_hi = (int)(s_hi < nch ? s_hi : nch);
+  if (s_lo == 0)
+    p.kind = s_hi >= nch ? PIECE_WHOLE : PIECE_HEAD;
+  else
+    p.kind = s_lo < nch ? PIECE_TAIL : PIECE_NONE;
+  return p;
+}
+
+// Split chain schedule, written by the prep kernel's first CTA (the chain runs after it): the
+// chain CTAs' publish flags cleared, and per chain CTA its number of chunk steps and whether it
+// ends on a cut unit's head (or meets a unit with bad bounds).  The chain then reads its loop
+// bounds with plain loads.
+__device__ __noinline__ void chain_schedule(const BuildTcArgs &a) {
+  const long long total = (long long)a.n_units * a.max_chunks;
+  for (int b = threadIdx.x; b < a.n_flags; b += blockDim.x) {
+    a.flags[b] = 0;
+    const long long lo = (long long)b * a.q_steps;
+    const long long hi = lo + a.q_steps < total ? lo + a.q_steps : total;
+    int J = 0, f = 0;
+    for (long long u = lo / a.max_chunks; u * a.max_chunks < hi; ++u) {
+      const Piece p = piece_of(a, u, lo, hi);
+      J += p.c_hi - p.c_lo;
+      f = (f & 2) | (p.kind == PIECE_HEAD ? 1 : 0) | (p.ok ? 0 : 2);
+    }
+    a.sched[2 * b] = J;
+    a.sched[2 * b + 1] = f;
+  }
 }
 
 // hi = bf16(v), lo = bf16(v - hi) for 8 values, packed for one 16-byte store each.
@@ -125,7 +192,7 @@ constexpr uint32_t P_SMEM_O = P_OFF_Q + 16384 + 1024;
 template <bool WO>
 __global__ void __launch_bounds__(NT, WO ? 4 : 6)
     wy_prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
-                   BuildTcArgs a) {
+                   const __grid_constant__ BuildTcArgs a) {
   constexpr uint32_t TCOLS = WO ? 128 : 64;  // Gram (and Q K^T at column 64)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
@@ -137,6 +204,7 @@ __global__ void __launch_bounds__(NT, WO ? 4 : 6)
   float *sA = sL;  // A = (I + L)^{-1} replaces L in place, row stride LS
   float *sT = sL + 32;  // [32][32] with row stride LS: rows 0..31, columns 32..63 of L (never read as L)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (blockIdx.x == 0 && a.flags) chain_schedule(a);
   const int hh = blockIdx.x % a.Hb;
   const int c = (blockIdx.x / a.Hb) % a.max_chunks;
   const int s = (blockIdx.x / a.Hb) / a.max_chunks;
@@ -482,10 +550,201 @@ __device__ __forceinline__ void split2_pair(float a, float b, uint32_t &hi, uint
   lo = *reinterpret_cast<const uint32_t *>(&lp);
 }
 
+// This CTA's step range [lo, hi).
+__device__ __forceinline__ void cta_steps(const BuildTcArgs &a, long long &lo, long long &hi) {
+  const long long total = (long long)a.n_units * a.max_chunks;
+  lo = (long long)blockIdx.x * a.q_steps;
+  hi = lo + a.q_steps < total ? lo + a.q_steps : total;
+}
+// The piece of unit u in this CTA's share.  Piece walks run where a piece starts or ends, so they
+// are kept out of line, away from the code of the chunk loops.
+__device__ __noinline__ Piece piece_at(const BuildTcArgs &a, int u) {
+  long long lo, hi;
+  cta_steps(a, lo, hi);
+  return piece_of(a, u, lo, hi);
+}
+__device__ __noinline__ int units_begin(const BuildTcArgs &a) {
+  long long lo, hi;
+  cta_steps(a, lo, hi);
+  return (int)(lo / a.max_chunks);
+}
+__device__ __noinline__ int units_end(const BuildTcArgs &a) {
+  long long lo, hi;
+  cta_steps(a, lo, hi);
+  return (int)((hi + a.max_chunks - 1) / a.max_chunks);
+}
+// The first unit from u on with chunks in this CTA's share (units_end if none).
+__device__ __noinline__ int next_busy_unit(const BuildTcArgs &a, int u) {
+  const int ue = units_end(a);
+  for (; u < ue; ++u) {
+    const Piece p = piece_at(a, u);
+    if (p.c_hi > p.c_lo) break;
+  }
+  return u;
+}
+
+__device__ __forceinline__ void st_release_gpu(int *f, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+// Waits (bounded) for a neighbour's published pair: true if it was published intact.
+__device__ __forceinline__ bool wait_published(const int *f, int *err, long long limit = 2000000000LL) {
+  const long long t0 = clock64();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v != 0) return v == 1;
+    if (clock64() - t0 > limit) {
+      set_error(err, HYPIC_ETIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
+// The composition of a cut unit stages T_B as bf16 hi and lo K-major tiles ([128 i][64 j] blocks
+// of 16 KB) in stage 0, which no chunk uses any more by then.
+constexpr uint32_t FX_TBH = 0, FX_TBL = 32768;
+
+// ---- conversion-thread helpers (thread t < 512: TMEM lane t & 127, column part (t >> 7) & 1,
+// half (t >> 8) & 1) --------------------------------------------------------------------------
+__device__ __forceinline__ int conv_row() { return threadIdx.x & 127; }
+__device__ __forceinline__ int conv_part() { return (threadIdx.x >> 7) & 1; }
+__device__ __forceinline__ int conv_half() { return (threadIdx.x >> 8) & 1; }
+
+// X^T = [I | 0]^T restricted to this thread's half and columns: I (T half) or 0 (S half).
+__device__ __noinline__ void conv_init_x(uint32_t tx) {
+  const int row = conv_row(), part = conv_part(), half = conv_half();
+  for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = (half == 0 && c0 + q == row) ? 1.f : 0.f;
+    tmem_st16(tx + c0, v);
+  }
+  tmem_st_wait();
+}
+// Copies this thread's 64 rows i of its half's X^T to out[i][n] (row-major [128][128]).
+__device__ __noinline__ void conv_write_x(uint32_t tx, float *out) {
+  const int row = conv_row(), part = conv_part();
+  for (int cb = 0; cb < 64; cb += 32) {
+    float xv[32];
+    tmem_ld32(tx + 64 * part + cb, xv);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) out[(size_t)(64 * part + cb + q) * D + row] = xv[q];
+  }
+}
+__device__ __forceinline__ float *unit_out(const BuildTcArgs &a, const Piece &p, int half) {
+  return (half ? a.S_out : a.T_out) + ((size_t)p.s * a.H + a.h0 + p.hh) * D * D;
+}
+// Units of this CTA with no chunks to run: empty bodies get [I | 0]; cuts past a body's end leave
+// nothing to do.
+__device__ __noinline__ void conv_empty_units(const BuildTcArgs &a) {
+  const int row = conv_row(), part = conv_part(), half = conv_half();
+  const int ue = units_end(a);
+  for (int u = units_begin(a); u < ue; ++u) {
+    const Piece p = piece_at(a, u);
+    if (p.kind != PIECE_WHOLE || p.c_hi > p.c_lo) continue;
+    float *out = unit_out(a, p, half);
+    for (int i = 64 * part; i < 64 * part + 64; ++i) out[(size_t)i * D + row] = (half == 0 && i == row) ? 1.f : 0.f;
+  }
+}
+// A cut unit's tail: publish (T_B, S_B) for the previous CTA, which composes it onto the head.
+__device__ __noinline__ void conv_publish(const BuildTcArgs &a, uint32_t tx, bool ok) {
+  if (ok) conv_write_x(tx, a.part + ((size_t)blockIdx.x * 2 + conv_half()) * D * D);
+  __threadfence();
+  const bool bad = bar_or_named(1, NCONV, !ok);
+  if (threadIdx.x == 0) st_release_gpu(&a.flags[blockIdx.x], bad ? 2 : 1);
+}
+// A cut unit's head (this CTA's last piece): stage T_B as the B tiles of X^T += X_A^T T_B^T, split
+// X_A^T like step (1) of a chunk, restart the accumulator at [0 | S_B]^T and hand over to the MMA
+// warp; then write the unit's result.  Both halves' last updates have landed before the tiles are
+// written over stage 0.
+__device__ __noinline__ bool conv_compose_head(const BuildTcArgs &a, const Piece &p, uint32_t tx, uint32_t txp,
+                                               uint8_t *xlo, uint8_t *sm, uint64_t *bar_r1h, uint64_t *bar_xh,
+                                               int J, bool ok) {
+  const int tid = threadIdx.x, row = conv_row(), part = conv_part(), half = conv_half();
+  const float *pairB = a.part + (size_t)(blockIdx.x + 1) * 2 * D * D;
+  if (tid == 0 && ok) ok = wait_published(&a.flags[blockIdx.x + 1], a.err);
+  const bool bad = bar_or_named(1, NCONV, !ok);
+  if (!bad) {
+    // T_B as K-major bf16 hi and lo tiles: thread -> row i, columns [32 qb, 32 qb + 32).
+    const int i = tid >> 2, qb = tid & 3;
+    const float *src = pairB + (size_t)i * D + 32 * qb;
+    for (int m = 0; m < 4; ++m) {
+      float v[8];
+      const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m));
+      const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m + 4));
+      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+      v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+      uint4 h8, l8;
+      split8(v, h8, l8);
+      const uint32_t col = 32u * qb + 8u * m;
+      const uint32_t off = (col / 64) * 16384u + sw128_offset((uint32_t)i, (col % 64) / 8);
+      *reinterpret_cast<uint4 *>(sm + FX_TBH + off) = h8;
+      *reinterpret_cast<uint4 *>(sm + FX_TBL + off) = l8;
+    }
+    // X_A^T pieces as in step (1); the accumulator restarts at [0 | S_B]^T.
+    const float *sB = pairB + (size_t)D * D;
+    for (int cb = 0; cb < 64; cb += 32) {
+      float xv[32];
+      tmem_ld32(tx + 64 * part + cb, xv);
+      float ph[16];
+      uint32_t pl[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        uint32_t hi2;
+        split2_pair(xv[2 * q], xv[2 * q + 1], hi2, pl[q]);
+        ph[q] = __uint_as_float(hi2);
+      }
+      tmem_st16(txp + (64 * part + cb) / 2, ph);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
+            make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) xv[q] = half ? __ldcg(sB + (size_t)(64 * part + cb + q) * D + row) : 0.f;
+      tmem_st32(tx + 64 * part + cb, xv);
+    }
+    tmem_st_wait();
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  bar_sync_named(1, NCONV);  // T_B tiles complete
+  mbar_arrive(bar_r1h);
+  const bool fx = mbar_wait_sleep(bar_xh, (uint32_t)J & 1u, a.err);
+  tc_fence_after();
+  ok = ok && !bad && fx;
+  if (ok) conv_write_x(tx, unit_out(a, p, half));
+  return ok;
+}
+// The MMA warp's part of a cut unit's head: X^T += X_A^T T_B^T on top of [0 | S_B]^T per half
+// (M = 128 n, N = 128 i, K = 128 j), hi.hi + hi.lo + lo.hi with T_B split like the chunk operands.
+__device__ __noinline__ bool mma_compose_head(uint32_t tmem, uint32_t sb, uint64_t *bar_r1, uint64_t *bar_x, int J,
+                                              int *err) {
+  const uint32_t id_f = idesc_f32acc(1, 1, 0, 0, 128, 128);
+  const uint64_t dTH = sdesc_sw128(sb + FX_TBH, 16, 1024);
+  const uint64_t dTL = sdesc_sw128(sb + FX_TBL, 16, 1024);
+  const uint64_t dXL = sdesc_sw128(sb + OFF_XLO, 16, 1024);
+  const uint32_t par = (uint32_t)J & 1u;
+  for (int hf = 0; hf < 2; ++hf) {
+    if (!mbar_wait_cycles(&bar_r1[hf], par, err)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t ko = (uint64_t)(kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+      const uint64_t al = dXL + hf * 2048 + (kk >> 2) * 1024 + (kk & 3) * 2;
+      mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTH + ko, id_f, 1);
+      mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTL + ko, id_f, 1);
+      mma_f16(tmem + tm_x(hf), al, dTH + ko, id_f, 1);
+    }
+    mma_commit(&bar_x[hf]);
+  }
+  return true;
+}
+
 template <bool T_ONLY>
 __global__ void __launch_bounds__(NT2, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                    BuildTcArgs a) {
+                    const __grid_constant__ BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // per half: r1 (X pieces ready), r2 (R pieces ready), p (P^T done), x (update done)
   // per stage: full (copies landed), empty (the chunk's last MMAs done)
@@ -499,16 +758,28 @@ __global__ void __launch_bounds__(NT2, 1)
   const int row = tid & 127;        // TMEM lane a conversion thread serves
   const int part = (tid >> 7) & 1;  // which half of that lane's columns
   const int half = (tid >> 8) & 1;  // 0: T columns, 1: S columns
-  const int hh = blockIdx.x % a.Hb;
-  const int s = blockIdx.x / a.Hb;
-  const int h = a.h0 + hh;
 
-  int64_t beg, end;
-  if (!seg_bounds(a, s, beg, end)) {
-    if (tid == 0) set_error(a.err, HYPIC_EDEVICE);
+  // This CTA's chunk steps J and whether it ends on a cut unit's head: from the schedule the prep
+  // kernel wrote, or with one unit per CTA straight from the unit's bounds.
+  int J = 0;
+  bool has_fix = false, bounds_ok = true;
+  if (a.sched) {
+    J = a.sched[2 * blockIdx.x];
+    const int f = a.sched[2 * blockIdx.x + 1];
+    has_fix = (f & 1) != 0;
+    bounds_ok = (f & 2) == 0;
+  } else {
+    int64_t beg, end;
+    bounds_ok = seg_bounds(a, (int)(blockIdx.x / a.Hb), beg, end);
+    J = bounds_ok ? (int)((end - beg + C - 1) / C) : 0;
+  }
+  if (!bounds_ok) {
+    if (tid == 0) {
+      set_error(a.err, HYPIC_EDEVICE);
+      if (a.flags) st_release_gpu(&a.flags[blockIdx.x], 2);  // a waiting neighbour goes on
+    }
     return;
   }
-  const int nchunks = (int)((end - beg + C - 1) / C);
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -533,25 +804,31 @@ __global__ void __launch_bounds__(NT2, 1)
 
   if (producer) {
     // ------------------------------------------------------------------------------- TMA warp
-    // Chunk c goes into stage c & 1 once chunk c - 2, the stage's previous user, has run its last
-    // MMAs (the converters are done with the stage before those are issued).
+    // Chunk step j goes into stage j & 1 once step j - 2, the stage's previous user, has run its
+    // last MMAs (the converters are done with the stage before those are issued).
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
       bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c & 1;
-        if (c >= 2 && !(ok = mbar_wait_cycles(&bar_empty[st], (uint32_t)((c >> 1) - 1) & 1u, a.err))) break;
-        const int rowt = (int)(beg + (int64_t)c * C);
-        uint8_t *stg = sm + st * STAGE_BYTES;
-        const uint8_t *rec = ws_rec(a, s, c, hh);
-        mbar_arrive_expect_tx(&bar_full[st], 32768u + WS_TILES + WS_SC_BYTES);
-        tma_load_2d(stg + STAGE_K, &mapK, &bar_full[st], h * D, rowt);
-        tma_load_2d(stg + STAGE_K + 8192, &mapK, &bar_full[st], h * D + 64, rowt);
-        tma_load_2d(stg + STAGE_V, &mapV, &bar_full[st], h * D, rowt);
-        tma_load_2d(stg + STAGE_V + 8192, &mapV, &bar_full[st], h * D + 64, rowt);
-        bulk_load(stg + STAGE_REC, rec, WS_TILES, &bar_full[st]);
-        bulk_load(sm + OFF_SC + st * 512, rec + WS_SC, WS_SC_BYTES, &bar_full[st]);
+      int j = 0;
+      const int ue = units_end(a);
+      for (int u = units_begin(a); u < ue && ok; ++u) {
+        const Piece p = piece_at(a, u);
+        const int h = a.h0 + p.hh;
+        for (int c = p.c_lo; c < p.c_hi; ++c, ++j) {
+          const int st = j & 1;
+          if (j >= 2 && !(ok = mbar_wait_cycles(&bar_empty[st], (uint32_t)((j >> 1) - 1) & 1u, a.err))) break;
+          const int rowt = (int)(p.beg + (int64_t)c * C);
+          uint8_t *stg = sm + st * STAGE_BYTES;
+          const uint8_t *rec = ws_rec(a, p.s, c, p.hh);
+          mbar_arrive_expect_tx(&bar_full[st], 32768u + WS_TILES + WS_SC_BYTES);
+          tma_load_2d(stg + STAGE_K, &mapK, &bar_full[st], h * D, rowt);
+          tma_load_2d(stg + STAGE_K + 8192, &mapK, &bar_full[st], h * D + 64, rowt);
+          tma_load_2d(stg + STAGE_V, &mapV, &bar_full[st], h * D, rowt);
+          tma_load_2d(stg + STAGE_V + 8192, &mapV, &bar_full[st], h * D + 64, rowt);
+          bulk_load(stg + STAGE_REC, rec, WS_TILES, &bar_full[st]);
+          bulk_load(sm + OFF_SC + st * 512, rec + WS_SC, WS_SC_BYTES, &bar_full[st]);
+        }
       }
       if (!ok) abort_flag = 1;
     }
@@ -573,14 +850,15 @@ __global__ void __launch_bounds__(NT2, 1)
       const uint64_t dWH = sdesc_sw128(sb + STAGE_REC + WS_WH, 16384, 1024);
       const uint64_t dWL = sdesc_sw128(sb + STAGE_REC + WS_WL, 16384, 1024);
       const uint64_t dXL = sdesc_sw128(sb + OFF_XLO, 16, 1024);
-      // -U^T of chunk c into the S half's P^T (M = 128 j, N = 64 t, K = 64 s).  It follows the
-      // previous chunk's S update in the pipe, which has read the R^T pieces stored there.
-      auto issue_u = [&](int c) -> bool {
-        const int st = c & 1;
-        if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err)) return false;
+      // -U^T of step j (in stage st = j & 1) into the S half's P^T (M = 128 j, N = 64 t,
+      // K = 64 s).  It follows the previous step's S update in the pipe, which has read the R^T
+      // pieces stored there.
+      auto issue_u = [&](int j, auto st_tag) -> bool {
+        constexpr int st = decltype(st_tag)::value;
+        if (!mbar_wait_cycles(&bar_full[st], ((uint32_t)j >> 1) & 1u, a.err)) return false;
         tc_fence_after();
         if (T_ONLY) return true;
-        const uint64_t so = st ? DSTG : 0;
+        constexpr uint64_t so = st ? DSTG : 0;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t av = dV + so + kk * 128;
@@ -589,15 +867,17 @@ __global__ void __launch_bounds__(NT2, 1)
         }
         return true;
       };
-      bool ok = nchunks == 0 || issue_u(0);
       constexpr int nh = T_ONLY ? 1 : 2;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const uint32_t par = (uint32_t)c & 1u;
-        const uint64_t so = (c & 1) ? DSTG : 0;
+      // One chunk step in stage ST (= j & 1, so the stage offsets and barrier parities are
+      // constants); the loop below runs the steps two at a time.
+      auto step = [&](const int j, auto st_tag) -> bool {
+        constexpr int ST = decltype(st_tag)::value;
+        constexpr uint32_t par = ST;
+        constexpr uint64_t so = ST ? DSTG : 0;
         // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
 #pragma unroll
         for (int hf = 0; hf < nh; ++hf) {
-          if (!(ok = mbar_wait_cycles(&bar_r1[hf], par, a.err))) break;
+          if (!mbar_wait_cycles(&bar_r1[hf], par, a.err)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -610,13 +890,12 @@ __global__ void __launch_bounds__(NT2, 1)
           }
           mma_commit(&bar_p[hf]);
         }
-        if (!ok) break;
-        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next chunk's -U^T
+        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next step's -U^T
         // is queued right behind the S update, before its commit, so the pipe does not wait
         // for the commits; the S half's update barrier then also covers it.
 #pragma unroll
         for (int hf = 0; hf < nh; ++hf) {
-          if (!(ok = mbar_wait_cycles(&bar_r2[hf], par, a.err))) break;
+          if (!mbar_wait_cycles(&bar_r2[hf], par, a.err)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -625,89 +904,119 @@ __global__ void __launch_bounds__(NT2, 1)
             mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);
           }
-          if (hf == nh - 1 && c + 1 < nchunks) ok = issue_u(c + 1);
-          if (!ok) break;
+          if (hf == nh - 1 && j + 1 < J && !issue_u(j + 1, std::integral_constant<int, 1 - ST>{})) return false;
           mma_commit(&bar_x[hf]);
         }
-        if (ok) mma_commit(&bar_empty[c & 1]);
+        mma_commit(&bar_empty[ST]);
+        return true;
+      };
+      bool ok = J == 0 || issue_u(0, std::integral_constant<int, 0>{});
+      for (int j = 0; j < J && ok; j += 2) {
+        ok = step(j, std::integral_constant<int, 0>{});
+        if (ok && j + 1 < J) ok = step(j + 1, std::integral_constant<int, 1>{});
       }
+      if constexpr (!T_ONLY)
+        if (ok && has_fix) ok = mma_compose_head(tmem, sb, bar_r1, bar_x, J, a.err);
       if (!ok) abort_flag = 1;
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------------- conversion warps
-    // X^T starts at [I | 0]^T restricted to this half: I (T half) or 0 (S half).
     const uint32_t tx = tmem + lane_base + tm_x(half), txp = tmem + lane_base + tm_xp(half);
     const uint32_t tp = tmem + lane_base + tm_p(half);
     uint8_t *xlo = sm + OFF_XLO + half * 32768 + part * 16384;
-    for (int c0 = 64 * part; c0 < 64 * part + 64; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = (half == 0 && c0 + q == row) ? 1.f : 0.f;
-      tmem_st16(tx + c0, v);
-    }
-    tmem_st_wait();
+    const bool idle = T_ONLY && half == 1;  // the T-only chain has no S half
+    if (!idle) conv_empty_units(a);
+    // Only the current unit and the step where its piece ends stay live across the chunk loop.
     bool ok = true;
-    const int my_chunks = (T_ONLY && half == 1) ? 0 : nchunks;
-    for (int c = 0; c < my_chunks && ok; ++c) {
-      const int st = c & 1;
-      const uint32_t par = (uint32_t)c & 1u;
-      if (c > 0 && !(ok = mbar_wait_sleep(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
-      if (!(ok = mbar_wait_sleep(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
-      tc_fence_after();
-      const float *sR = reinterpret_cast<const float *>(sm + OFF_SC + st * 512);
-      const float gamma_C = sR[C];
-      // (1) this thread's 64 rows i of X^T: hi pieces to TMEM, lo pieces to the shared A tile,
-      // gamma_C X^T back into the accumulator.
-#pragma unroll
-      for (int cb = 0; cb < 64; cb += 32) {
-        float xv[32];
-        tmem_ld32(tx + 64 * part + cb, xv);
-        float ph[16];
-        uint32_t pl[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint32_t hi;
-          split2_pair(xv[2 * q], xv[2 * q + 1], hi, pl[q]);
-          ph[q] = __uint_as_float(hi);
-        }
-        tmem_st16(txp + (64 * part + cb) / 2, ph);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
-              make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) xv[q] *= gamma_C;
-        tmem_st32(tx + 64 * part + cb, xv);
-      }
-      tmem_st_wait();
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(&bar_r1[half]);
-      // (2) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in place: this thread's
-      // columns t in [32 part, 32 part + 32) become 16 hi columns then 16 lo columns.
-      if (!(ok = mbar_wait_sleep(&bar_p[half], par, a.err))) break;
-      tc_fence_after();
-      {
-        float pv[32];
-        tmem_ld32(tp + 32 * part, pv);
-        float ph[16], pl[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int t = 32 * part + 2 * q;
-          uint32_t hi, lo;
-          split2_pair(-pv[2 * q] * sR[t], -pv[2 * q + 1] * sR[t + 1], hi, lo);
-          ph[q] = __uint_as_float(hi);
-          pl[q] = __uint_as_float(lo);
-        }
-        tmem_st16(tp + 32 * part, ph);
-        tmem_st16(tp + 32 * part + 16, pl);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(&bar_r2[half]);
+    const int my_steps = idle ? 0 : J;
+    int u = 0, piece_end = 0;
+    if (my_steps > 0) {
+      u = next_busy_unit(a, units_begin(a));
+      const Piece p = piece_at(a, u);
+      piece_end = p.c_hi - p.c_lo;
+      conv_init_x(tx);
     }
-    if (ok && my_chunks > 0) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)(my_chunks - 1) & 1u, a.err);
+    for (int j = 0; j < my_steps; ++j) {
+      do {
+        if (!ok) break;
+        const int st = j & 1;
+        const uint32_t par = (uint32_t)j & 1u;
+        if (j > 0 && !(ok = mbar_wait_sleep(&bar_x[half], par ^ 1u, a.err))) break;  // previous update done
+        if (!(ok = mbar_wait_sleep(&bar_full[st], ((uint32_t)j >> 1) & 1u, a.err))) break;
+        tc_fence_after();
+        const float *sR = reinterpret_cast<const float *>(sm + OFF_SC + st * 512);
+        const float gamma_C = sR[C];
+        // (1) this thread's 64 rows i of X^T: hi pieces to TMEM, lo pieces to the shared A tile,
+        // gamma_C X^T back into the accumulator.
+#pragma unroll
+        for (int cb = 0; cb < 64; cb += 32) {
+          float xv[32];
+          tmem_ld32(tx + 64 * part + cb, xv);
+          float ph[16];
+          uint32_t pl[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            uint32_t hi2;
+            split2_pair(xv[2 * q], xv[2 * q + 1], hi2, pl[q]);
+            ph[q] = __uint_as_float(hi2);
+          }
+          tmem_st16(txp + (64 * part + cb) / 2, ph);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
+                make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) xv[q] *= gamma_C;
+          tmem_st32(tx + 64 * part + cb, xv);
+        }
+        tmem_st_wait();
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&bar_r1[half]);
+        // (2) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in place: this thread's
+        // columns t in [32 part, 32 part + 32) become 16 hi columns then 16 lo columns.
+        if (!(ok = mbar_wait_sleep(&bar_p[half], par, a.err))) break;
+        tc_fence_after();
+        {
+          float pv[32];
+          tmem_ld32(tp + 32 * part, pv);
+          float ph[16], pl[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int t = 32 * part + 2 * q;
+            uint32_t hi2, lo2;
+            split2_pair(-pv[2 * q] * sR[t], -pv[2 * q + 1] * sR[t + 1], hi2, lo2);
+            ph[q] = __uint_as_float(hi2);
+            pl[q] = __uint_as_float(lo2);
+          }
+          tmem_st16(tp + 32 * part, ph);
+          tmem_st16(tp + 32 * part + 16, pl);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_r2[half]);
+      } while (false);
+      if (j + 1 != piece_end) continue;
+      // ---- end of a piece: the half's last update has landed
+      if (ok) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)j & 1u, a.err);
+      tc_fence_after();
+      const Piece p = piece_at(a, u);
+      if (p.kind == PIECE_WHOLE) {
+        if (ok) conv_write_x(tx, unit_out(a, p, half));
+      } else if constexpr (!T_ONLY) {
+        if (p.kind == PIECE_TAIL)
+          conv_publish(a, tx, ok);
+        else  // PIECE_HEAD, always this CTA's last piece
+          ok = conv_compose_head(a, p, tx, txp, xlo, sm, &bar_r1[half], &bar_x[half], J, ok);
+      }
+      if (j + 1 < my_steps) {
+        u = next_busy_unit(a, u + 1);
+        const Piece q = piece_at(a, u);
+        piece_end += q.c_hi - q.c_lo;
+        if (ok) conv_init_x(tx);  // the previous piece's X^T has been read out
+      }
+    }
     if (!ok) abort_flag = 1;
   }
   __syncthreads();
@@ -721,18 +1030,6 @@ __global__ void __launch_bounds__(NT2, 1)
         mbar_wait_cycles(&bar_full[i], (uint32_t)k, nullptr, 100000000LL);
         mbar_wait_cycles(&bar_empty[i], (uint32_t)k, nullptr, 100000000LL);
       }
-  }
-  if (!abort_flag && !issuer && !producer && !(T_ONLY && half == 1)) {
-    // X^T lane n holds column n of this half: write X[i][n] for this thread's 64 rows i.
-    float *out = (half ? a.S_out : a.T_out) + ((size_t)s * a.H + h) * D * D;
-    const uint32_t tx = tmem + lane_base + tm_x(half);
-#pragma unroll
-    for (int cb = 0; cb < 64; cb += 32) {
-      float xv[32];
-      tmem_ld32(tx + 64 * part + cb, xv);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) out[(size_t)(64 * part + cb + q) * D + row] = xv[q];
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1030,6 +1327,32 @@ size_t bytes_per_head(int n_seg, int64_t max_len, bool want_o) {
   return (size_t)n_seg * (size_t)(chunks > 0 ? chunks : 1) * (want_o ? WS_REC_O : WS_REC);
 }
 
+// Pair slots of the split chain schedule, after the records: one (T, S) pair per chain CTA (at
+// most kSplitSlots CTAs), then a publish flag each and the CTAs' schedule (two ints each).
+constexpr int kSplitSlots = 256;
+constexpr size_t kSlotBytes = 2 * D * D * sizeof(float);
+int split_slots(long long units) { return (int)(units < kSplitSlots ? (units > 0 ? units : 0) : kSplitSlots); }
+size_t split_bytes(long long units) {
+  const int n = split_slots(units);
+  return n ? (size_t)n * kSlotBytes + 3 * kSplitSlots * sizeof(int) : 0;  // + flags and schedule
+}
+
+// Chain CTAs the device keeps resident at once in a cooperative launch (0: no cooperative launch).
+int chain_resident_ctas() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int sms = 0, coop = 0, per = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, chain_tc_kernel<false>, NT2, SMEM_BYTES) != cudaSuccess)
+      return 0;
+    cache[dev] = (coop && sms * per > 0) ? sms * per : -1;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 }  // namespace
 
 bool build_tc_supported(int D_, int fam, int in_dtype, bool want_o) {
@@ -1047,7 +1370,7 @@ size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o) 
   size_t heads = WS_CAP / per;
   if (heads < 1) heads = 1;
   if (heads > (size_t)H) heads = (size_t)H;
-  return heads * per;
+  return heads * per + (want_o ? 0 : split_bytes((long long)n_seg * (long long)heads));
 }
 
 // Runs the build over head blocks that fit the workspace: prep then chain for each block (and,
@@ -1100,17 +1423,58 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     e = cudaFuncSetAttribute(chain_so_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SO_SMEM);
     if (e != cudaSuccess) return e;
   }
+  // The split chain schedule needs its pair slots after the records and a cooperative launch.
+  const size_t rec_end = (size_t)Hb * per;  // a multiple of 256 bytes
+  const bool split_room = !wo && ws_bytes >= rec_end + split_bytes((long long)r.n_seg * Hb);
+  const int resident = split_room ? chain_resident_ctas() : 0;
   for (int h0 = 0; h0 < r.H; h0 += Hb) {
     a.h0 = h0;
     a.Hb = (r.H - h0) < Hb ? (r.H - h0) : Hb;
     const long long g1 = (long long)r.n_seg * a.max_chunks * a.Hb;
-    const long long g2 = (long long)r.n_seg * a.Hb;
-    if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const long long units = (long long)r.n_seg * a.Hb;
+    if (g1 > 0x7fffffffLL || units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    a.n_units = (int)units;
+    a.q_steps = a.max_chunks;
+    a.part = nullptr;
+    a.flags = nullptr;
+    a.sched = nullptr;
+    a.n_flags = 0;
+    long long g2 = units;
+    const int cap = resident < kSplitSlots ? resident : kSplitSlots;
+    if (cap > 0 && units > cap) {
+      // more units than resident CTAs: cap CTAs, each an equal share of the chunk steps
+      const long long steps = units * a.max_chunks;
+      const long long q = (steps + cap - 1) / cap;
+      if (q > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      a.q_steps = (int)q;
+      g2 = (steps + q - 1) / q;
+      a.part = reinterpret_cast<float *>(a.ws + rec_end);
+      a.flags = reinterpret_cast<int *>(a.ws + rec_end + (size_t)split_slots(units) * kSlotBytes);
+      a.sched = a.flags + kSplitSlots;
+      a.n_flags = (int)g2;
+    }
     if (wo) wy_prep_kernel<true><<<(unsigned)g1, NT, P_SMEM_O, st>>>(mk, mq, a);
     else wy_prep_kernel<false><<<(unsigned)g1, NT, P_SMEM, st>>>(mk, mq, a);
-    if (wo) chain_tc_kernel<true><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
-    else chain_tc_kernel<false><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
-    if (wo) chain_so_kernel<<<(unsigned)g2, SO_NT, SO_SMEM, st>>>(mk, mv, mq, a);
+    if (wo) {
+      chain_tc_kernel<true><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+      chain_so_kernel<<<(unsigned)g2, SO_NT, SO_SMEM, st>>>(mk, mv, mq, a);
+    } else if (a.flags) {
+      // CTAs wait on their neighbours: all must be resident together
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)g2);
+      cfg.blockDim = dim3(NT2);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, chain_tc_kernel<false>, mk, mv, a);
+      if (e != cudaSuccess) return e;
+    } else {
+      chain_tc_kernel<false><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

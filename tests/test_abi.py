@@ -156,7 +156,9 @@ def test_binding_refuses_cpu_tensors():
 def test_build_workspace_contract(lib):
     sh = L.shape(32, 128, "gated_delta", "bf16")
     per_head = 8 * 64 * 49664
-    assert lib.hypic_build_workspace_bytes(ctypes.byref(sh), 8, 4096) == 32 * per_head
+    # the records of all heads, then pair slots for the chain (up to 256 CTAs), flags and schedule
+    split = min(8 * 32, 256) * 2 * 128 * 128 * 4 + 3 * 256 * 4
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(sh), 8, 4096) == 32 * per_head + split
     # shapes that run without a workspace
     for fam, dt in (("scalar", "bf16"), ("gated_delta", "f32")):
         s2 = L.shape(32, 128, fam, dt)

@@ -87,6 +87,44 @@ def test_deltanet_four_segments_of_256():
     assert eT <= TOL_BF16 and eS <= TOL_BF16
 
 
+@pytest.mark.parametrize("family,gate_div", [("delta", None), ("gated_delta", 1024.0)])
+def test_more_units_than_resident_ctas(family, gate_div):
+    """More (segment, head) units than chain CTAs fit on the GPU at once: the chain then runs one CTA
+    per SM over equal shares of all chunk steps and rejoins each segment it cuts by composing the two
+    pairs.  Ragged lengths put the cuts everywhere (inside a body, on its last chunk, past its end,
+    on empty bodies); a = 1 or slow decay keeps T_C large so the composed T half is really checked.
+    The same build with a workspace that holds only the records runs one CTA per unit."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    n_seg = sms // H + 10
+    special = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512]
+    gen = torch.Generator().manual_seed(77)
+    lens = [special[i % len(special)] if i % 3 == 0 else int(torch.randint(0, 513, (1,), generator=gen))
+            for i in range(n_seg)]
+    tok, bounds, T, S = run_case(family, lens, H, key=11, gate_div=gate_div)
+    records = n_seg * ((max(lens) + 63) // 64) * 49664 * H
+    ws = torch.empty(records, dtype=torch.uint8, device=DEV)
+    T1, S1 = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                      tok["beta"], family=family, ws=ws)
+    assert hy.stream_status() == 0
+    host = host_tokens(tok, list(range(H)))
+    err = {"split": [0.0, 0.0], "per unit": [0.0, 0.0]}
+    for s, (b, e) in enumerate(bounds):
+        for h in range(H):
+            Tr, Sr = ref_pair(family, host, h, b, e)
+            for key, (Tg, Sg) in (("split", (T, S)), ("per unit", (T1, S1))):
+                err[key][0] = max(err[key][0], relerr(np64(Tg[s, h]), Tr))
+                if e > b:
+                    err[key][1] = max(err[key][1], relerr(np64(Sg[s, h]), Sr))
+    print(f"{family}: {n_seg} x {H} units, max rel err T/S {err}")
+    for key in err:
+        assert err[key][0] <= TOL_BF16 and err[key][1] <= TOL_BF16, key
+    for s, (b, e) in enumerate(bounds):
+        if e == b:
+            assert torch.equal(T[s], torch.eye(128, device=DEV).expand(H, 128, 128))
+            assert float(S[s].abs().max()) == 0.0
+
+
 def test_tensor_core_path_agrees_with_recurrent_path(monkeypatch):
     lens = [300, 64, 5]
     H = 2

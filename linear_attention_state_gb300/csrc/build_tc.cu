@@ -868,13 +868,10 @@ __global__ void __launch_bounds__(NT2, 1)
         return true;
       };
       constexpr int nh = T_ONLY ? 1 : 2;
-      // One chunk step in stage ST (= j & 1, so the stage offsets and barrier parities are
-      // constants); the loop below runs the steps two at a time.
-      auto step = [&](const int j, auto st_tag) -> bool {
-        constexpr int ST = decltype(st_tag)::value;
-        constexpr uint32_t par = ST;
-        constexpr uint64_t so = ST ? DSTG : 0;
-        // P^T for each half (M = 128 n, N = 64 t, K = 128 i): hi.hi + hi.lo + lo.hi.
+      auto step = [&](const int j) -> bool {
+        const int ST = j & 1;
+        const uint32_t par = ST;
+        const uint64_t so = ST ? DSTG : 0;
 #pragma unroll
         for (int hf = 0; hf < nh; ++hf) {
           if (!mbar_wait_cycles(&bar_r1[hf], par, a.err)) return false;
@@ -890,9 +887,6 @@ __global__ void __launch_bounds__(NT2, 1)
           }
           mma_commit(&bar_p[hf]);
         }
-        // X^T += R^T K for each half (M = 128 n, N = 128 i, K = 64 t).  The next step's -U^T
-        // is queued right behind the S update, before its commit, so the pipe does not wait
-        // for the commits; the S half's update barrier then also covers it.
 #pragma unroll
         for (int hf = 0; hf < nh; ++hf) {
           if (!mbar_wait_cycles(&bar_r2[hf], par, a.err)) return false;
@@ -904,17 +898,17 @@ __global__ void __launch_bounds__(NT2, 1)
             mma_f16_tmem_a(tmem + tm_x(hf), pc, bk, id_x, 1);
             mma_f16_tmem_a(tmem + tm_x(hf), pc + 16, bk, id_x, 1);
           }
-          if (hf == nh - 1 && j + 1 < J && !issue_u(j + 1, std::integral_constant<int, 1 - ST>{})) return false;
+          if (hf == nh - 1 && j + 1 < J) {
+            const bool r = ST ? issue_u(j + 1, std::integral_constant<int, 0>{}) : issue_u(j + 1, std::integral_constant<int, 1>{});
+            if (!r) return false;
+          }
           mma_commit(&bar_x[hf]);
         }
         mma_commit(&bar_empty[ST]);
         return true;
       };
       bool ok = J == 0 || issue_u(0, std::integral_constant<int, 0>{});
-      for (int j = 0; j < J && ok; j += 2) {
-        ok = step(j, std::integral_constant<int, 0>{});
-        if (ok && j + 1 < J) ok = step(j + 1, std::integral_constant<int, 1>{});
-      }
+      for (int j = 0; j < J && ok; ++j) ok = step(j);
       if constexpr (!T_ONLY)
         if (ok && has_fix) ok = mma_compose_head(tmem, sb, bar_r1, bar_x, J, a.err);
       if (!ok) abort_flag = 1;

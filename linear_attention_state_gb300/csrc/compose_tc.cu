@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ uint64_t bar_t[2], bar_s, bar_m;  // bar_t[1]: second T buffer (bf16 pairs)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float red[2][D];  // partial column dot products of the two row halves
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   float *sS0 = reinterpret_cast<float *>(sm + (PB ? OFF_S016 : OFF_S0));
@@ -332,58 +331,274 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     __syncthreads();  // S0 staging is consumed
     if (step + 1 < a.n) {
-      // (4) Seam tokens of the next segment, token by token on the register column.
+      // (4) Seam tokens of the next segment, token by token on the register column: gate first
+      // (a_t, 1, or KDA's per-channel g_t), y = gate * x, then x = y + b (v_j - k . y) k and
+      // o_j = q . x = q . y + b (v_j - k . y) (q . k).  The S0 staging buffer is free here: a
+      // group of up to SG tokens lands in it in one coalesced pass (one memory latency per group),
+      // one warp per token forms q . k, and each token then needs a single barrier, the partial
+      // sums k . y and q . y of the two row halves alternating between two slots.
       if (a.w > 0) {
-        // Gate first (a_t, 1, or KDA's per-channel g_t), y = gate * x, then
-        // x = y + b (v_j - k . y) k.
-        float *sk = sS0, *sq = sS0 + D, *sg = sS0 + 2 * D;
+        constexpr int SG = 8;
         const bool kda = a.fam == HYPIC_FAM_KDA;
-        for (int t = 0; t < a.w; ++t) {
-          const size_t tok = ((size_t)b * (a.n - 1) + step) * a.w + t;
-          const size_t g = (tok * H + h) * D;
-          if (half == 0) {
-            sk[j] = ld_tok<Tin>(SK, g + j);
-            if (kda) sg[j] = a.seam_alpha[g + j];
-          } else if (a.o_out) {
-            sq[j] = ld_tok<Tin>(SQ, g + j);
-          }
-          const float at = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
-          const float bt = a.seam_beta[tok * H + h];
-          const float vj = ld_tok<Tin>(SV, g + j);
-          __syncthreads();
-#pragma unroll
-          for (int r = 0; r < R; ++r) x[r] *= kda ? sg[i0 + r] : at;
-          float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-          for (int r = 0; r < R; r += 4) {
-            c0 = fmaf(sk[i0 + r], x[r], c0);
-            c1 = fmaf(sk[i0 + r + 1], x[r + 1], c1);
-            c2 = fmaf(sk[i0 + r + 2], x[r + 2], c2);
-            c3 = fmaf(sk[i0 + r + 3], x[r + 3], c3);
-          }
-          red[half][j] = (c0 + c1) + (c2 + c3);
-          __syncthreads();
-          const float kx = red[0][j] + red[1][j];
-          const float coef = bt * (vj - kx);
-#pragma unroll
-          for (int r = 0; r < R; ++r) x[r] = fmaf(coef, sk[i0 + r], x[r]);
-          if (a.o_out) {
-            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; r += 4) {
-              o0 = fmaf(sq[i0 + r], x[r], o0);
-              o1 = fmaf(sq[i0 + r + 1], x[r + 1], o1);
-              o2 = fmaf(sq[i0 + r + 2], x[r + 2], o2);
-              o3 = fmaf(sq[i0 + r + 3], x[r + 3], o3);
+        const bool want_o = a.o_out != nullptr;
+        float *sK = sS0;               // [SG][D]
+        float *sQ = sK + SG * D;       // [SG][D]
+        float *sV = sQ + SG * D;       // [SG][D]
+        float *sGc = sV + SG * D;      // [SG][D], KDA channel gates
+        float *sA = sGc + SG * D;      // [SG] scalar gates
+        float *sB = sA + SG;           // [SG]
+        float *sQK = sB + SG;          // [SG]
+        float *redk = sQK + SG;        // [2][2][D]
+        float *redq = redk + 4 * D;    // [2][2][D]
+        for (int t0 = 0; t0 < a.w; t0 += SG) {
+          const int ng = a.w - t0 < SG ? a.w - t0 : SG;
+          const size_t tok0 = ((size_t)b * (a.n - 1) + step) * a.w + t0;
+          {
+            // all of the group's loads are issued before the first store (one memory latency)
+            constexpr int NL = SG * D / NT;
+            float lk[NL], lv[NL], lq[NL], lg[NL], la = 1.f, lb = 0.f;
+            if (tid < ng) {
+              const size_t tok = tok0 + tid;
+              la = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
+              lb = a.seam_beta[tok * H + h];
             }
-            __syncthreads();  // everyone has read red
-            red[half][j] = (o0 + o1) + (o2 + o3);
-            __syncthreads();
-            if (half == 0) a.o_out[g + j] = red[0][j] + red[1][j];
+#pragma unroll
+            for (int it = 0; it < NL; ++it) {
+              const int e = tid + it * NT, t = e / D, i = e % D;
+              if (t < ng) {
+                const size_t g = ((tok0 + t) * H + h) * D + i;
+                lk[it] = ld_tok<Tin>(SK, g);
+                lv[it] = ld_tok<Tin>(SV, g);
+                lq[it] = want_o ? ld_tok<Tin>(SQ, g) : 0.f;
+                lg[it] = kda ? a.seam_alpha[g] : 1.f;
+              }
+            }
+#pragma unroll
+            for (int it = 0; it < NL; ++it) {
+              const int e = tid + it * NT;
+              if (e / D < ng) {
+                sK[e] = lk[it];
+                sV[e] = lv[it];
+                sQ[e] = lq[it];
+                sGc[e] = lg[it];
+              }
+            }
+            if (tid < ng) {
+              sA[tid] = la;
+              sB[tid] = lb;
+            }
           }
-          fence_proxy_async();  // the buffer is refilled by TMA next
           __syncthreads();
+          if (!kda) {
+            // Scalar gates: the group in chunked form.  With D_ts = a_{s+1} ... a_t (s < t; D_tt = 1;
+            // gamma_t = a_0 ... a_t), u_t = k_t . x and p_t = q_t . x for the column x on entry, the
+            // effective writes w solve (I + L) w = b (v - gamma u), L_ts = b_t D_ts (k_t . k_s)
+            // (s < t); then o_t = gamma_t p_t + sum_{s <= t} D_ts (q_t . k_s) w_s and
+            // x <- gamma_last x + sum_s D_last,s w_s k_s.  Decay factors are products of gates,
+            // never quotients.
+            float *sL = redq + 4 * D;   // [SG][SG]: L (s < t), D (s >= t unused)
+            float *sM = sL + SG * SG;   // [SG][SG]: D_ts (q_t . k_s), s <= t
+            float *sGam = sM + SG * SG; // [SG]: gamma_t
+            float *sF = sGam + SG;      // [SG]: D_last,s
+            float *sU = sF + SG;        // [2 halves][SG][D]: partial k_t . x, then q_t . x
+            if (warp < ng) {
+              // warp t: (k_t . k_s) and (q_t . k_s) for s < ng, and row t of the decay products
+              const int t = warp, ln = tid & 31;
+              float gk[SG], gq[SG];
+#pragma unroll
+              for (int s2 = 0; s2 < SG; ++s2) {
+                gk[s2] = 0.f;
+                gq[s2] = 0.f;
+              }
+#pragma unroll
+              for (int i = ln; i < D; i += 32) {
+                const float kt = sK[t * D + i], qt = want_o ? sQ[t * D + i] : 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < SG; ++s2) {
+                  if (s2 < ng) {
+                    const float ks = sK[s2 * D + i];
+                    gk[s2] = fmaf(kt, ks, gk[s2]);
+                    gq[s2] = fmaf(qt, ks, gq[s2]);
+                  }
+                }
+              }
+#pragma unroll
+              for (int s2 = 0; s2 < SG; ++s2) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                  gk[s2] += __shfl_xor_sync(0xffffffffu, gk[s2], o);
+                  gq[s2] += __shfl_xor_sync(0xffffffffu, gq[s2], o);
+                }
+              }
+              if (ln == 0) {
+                float dts = 1.f;  // D_ts for s = t, t - 1, ...
+#pragma unroll
+                for (int s2 = SG - 1; s2 >= 0; --s2) {
+                  if (s2 <= t) {
+                    sM[t * SG + s2] = dts * gq[s2];
+                    if (s2 < t) sL[t * SG + s2] = sB[t] * dts * gk[s2];
+                    dts *= sA[s2];
+                  }
+                }
+                sGam[t] = dts;  // a_0 ... a_t
+                if (t == ng - 1) {
+                  float f = 1.f;
+                  for (int s2 = t; s2 >= 0; --s2) {
+                    sF[s2] = f;
+                    f *= sA[s2];
+                  }
+                }
+              }
+            }
+            // partial dot products of this thread's 64 rows
+            {
+              float u[SG];
+#pragma unroll
+              for (int t = 0; t < SG; ++t) u[t] = 0.f;
+#pragma unroll
+              for (int r = 0; r < R; r += 4) {
+#pragma unroll
+                for (int t = 0; t < SG; ++t) {
+                  if (t < ng) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(sK + t * D + i0 + r);
+                    u[t] = fmaf(k4.x, x[r], u[t]);
+                    u[t] = fmaf(k4.y, x[r + 1], u[t]);
+                    u[t] = fmaf(k4.z, x[r + 2], u[t]);
+                    u[t] = fmaf(k4.w, x[r + 3], u[t]);
+                  }
+                }
+              }
+#pragma unroll
+              for (int t = 0; t < SG; ++t)
+                if (t < ng) sU[(half * SG + t) * D + j] = u[t];
+            }
+            __syncthreads();
+            float wv[SG];
+            {
+              float uk[SG];
+#pragma unroll
+              for (int t = 0; t < SG; ++t)
+                if (t < ng) uk[t] = sU[t * D + j] + sU[(SG + t) * D + j];
+#pragma unroll
+              for (int t = 0; t < SG; ++t) {
+                if (t < ng) {
+                  float acc = sB[t] * (sV[t * D + j] - sGam[t] * uk[t]);
+#pragma unroll
+                  for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sL[t * SG + s2], wv[s2], acc);
+                  wv[t] = acc;
+                }
+              }
+            }
+            if (want_o) {
+              __syncthreads();  // sU is reused for q . x
+              float pq[SG];
+#pragma unroll
+              for (int t = 0; t < SG; ++t) pq[t] = 0.f;
+#pragma unroll
+              for (int r = 0; r < R; r += 4) {
+#pragma unroll
+                for (int t = 0; t < SG; ++t) {
+                  if (t < ng) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(sQ + t * D + i0 + r);
+                    pq[t] = fmaf(q4.x, x[r], pq[t]);
+                    pq[t] = fmaf(q4.y, x[r + 1], pq[t]);
+                    pq[t] = fmaf(q4.z, x[r + 2], pq[t]);
+                    pq[t] = fmaf(q4.w, x[r + 3], pq[t]);
+                  }
+                }
+              }
+#pragma unroll
+              for (int t = 0; t < SG; ++t)
+                if (t < ng) sU[(half * SG + t) * D + j] = pq[t];
+              __syncthreads();
+              if (half == 0) {
+#pragma unroll
+                for (int t = 0; t < SG; ++t) {
+                  if (t < ng) {
+                    float o = sGam[t] * (sU[t * D + j] + sU[(SG + t) * D + j]);
+#pragma unroll
+                    for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t * SG + s2], wv[s2], o);
+                    a.o_out[((tok0 + t) * H + h) * D + j] = o;
+                  }
+                }
+              }
+            }
+            // x <- gamma_last x + sum_s D_last,s w_s k_s
+            {
+              const float gl = sGam[ng - 1];
+              float cs[SG];
+#pragma unroll
+              for (int t = 0; t < SG; ++t) cs[t] = t < ng ? sF[t] * wv[t] : 0.f;
+#pragma unroll
+              for (int r = 0; r < R; r += 4) {
+                float v0 = gl * x[r], v1 = gl * x[r + 1], v2 = gl * x[r + 2], v3 = gl * x[r + 3];
+#pragma unroll
+                for (int t = 0; t < SG; ++t) {
+                  if (t < ng) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(sK + t * D + i0 + r);
+                    v0 = fmaf(cs[t], k4.x, v0);
+                    v1 = fmaf(cs[t], k4.y, v1);
+                    v2 = fmaf(cs[t], k4.z, v2);
+                    v3 = fmaf(cs[t], k4.w, v3);
+                  }
+                }
+                x[r] = v0;
+                x[r + 1] = v1;
+                x[r + 2] = v2;
+                x[r + 3] = v3;
+              }
+            }
+          } else {
+            if (want_o && warp < ng) {
+              float acc = 0.f;
+#pragma unroll
+              for (int i = (tid & 31); i < D; i += 32) acc = fmaf(sQ[warp * D + i], sK[warp * D + i], acc);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+              if ((tid & 31) == 0) sQK[warp] = acc;
+            }
+            for (int t = 0; t < ng; ++t) {
+              const int sl = t & 1;
+              const float *sk = sK + t * D, *sq = sQ + t * D;
+              if (kda) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) x[r] *= sGc[t * D + i0 + r];
+              } else {
+                const float at = sA[t];
+#pragma unroll
+                for (int r = 0; r < R; ++r) x[r] *= at;
+              }
+              float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+              for (int r = 0; r < R; r += 2) {
+                c0 = fmaf(sk[i0 + r], x[r], c0);
+                c1 = fmaf(sk[i0 + r + 1], x[r + 1], c1);
+              }
+              redk[(sl * 2 + half) * D + j] = c0 + c1;
+              if (want_o) {
+                float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+                for (int r = 0; r < R; r += 2) {
+                  e0 = fmaf(sq[i0 + r], x[r], e0);
+                  e1 = fmaf(sq[i0 + r + 1], x[r + 1], e1);
+                }
+                redq[(sl * 2 + half) * D + j] = e0 + e1;
+              }
+              __syncthreads();
+              const float kx = redk[sl * 2 * D + j] + redk[(sl * 2 + 1) * D + j];
+              const float coef = sB[t] * (sV[t * D + j] - kx);
+#pragma unroll
+              for (int r = 0; r < R; ++r) x[r] = fmaf(coef, sk[i0 + r], x[r]);
+              if (want_o && half == 0) {
+                const float qy = redq[sl * 2 * D + j] + redq[(sl * 2 + 1) * D + j];
+                a.o_out[((tok0 + t) * H + h) * D + j] = qy + coef * sQK[t];
+              }
+            }
+          }
+          __syncthreads();  // the group's tokens are consumed
         }
+        fence_proxy_async();  // the buffer is refilled by TMA next
+        __syncthreads();
       }
       if (tid == 0 && addend) issue_S(step + 1);
       write_pieces();

@@ -585,10 +585,21 @@ def main():
     h2d = sum(x.numel() * x.element_size() for x in host.values())
     d2h = S_host.numel() * 4 + o_host.numel() * 4
 
+    # The request's k, v and gates go through the host-input build, which copies segment groups on a
+    # second stream while the earlier ones build; the seam tokens (0.7 MB) are copied first.
+    bounds_host = torch.tensor(req.bounds_list, dtype=torch.int64)
+    copy_stream = torch.cuda.Stream()
+    seam_names = [n for n in host if n.startswith("seam_")]
+
     def e2e_step(ev):
-        for n, x in host.items():
-            getattr(req, n).copy_(x, non_blocking=True)
-        req.step(None)
+        for n in seam_names:
+            getattr(req, n).copy_(host[n], non_blocking=True)
+        hy.segment_build_batched_host(host["k"], host["v"], bounds_host, host["alpha"], host["beta"],
+                                      family=w.family, max_len=req.max_len,
+                                      dev=(req.k, req.v, req.alpha, req.beta, req.bounds), out=(req.T, req.S),
+                                      ws=req.ws, copy_stream=copy_stream)
+        hy.assemble(req.T, req.S, req.idx, req.seam_k, req.seam_v, req.seam_a, req.seam_b, seam_q=req.seam_q,
+                    family=w.family, out=req.S_out, o_out=req.o)
         S_host.copy_(req.S_out, non_blocking=True)
         o_host.copy_(req.o, non_blocking=True)
 

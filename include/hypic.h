@@ -120,6 +120,44 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
                                          void *ws, size_t ws_bytes, hypic_stream_t stream);
 
 /*
+ * (Both batched builds read whole 64-token chunks: the rows after a body's end up to its last
+ * chunk boundary, or the end of the token axis, are read and enter with zero gates, so they must
+ * hold finite values.)
+ *
+ * The batched build from inputs in host memory, with the host-to-device copies overlapped with
+ * the build (the segment bodies of one request arrive over the host link while the earlier ones
+ * are being built; the pair construction itself is that of hypic_segment_build_batched, HYPIC
+ * reading notes Method 2 and paper Sec. 5).  The segments are taken in groups of consecutive
+ * segments holding about an eighth of the body tokens each (at most 16 groups); each group's
+ * token rows (its first body's begin through the end of its last body's last 64-token chunk) are
+ * copied on copy_stream while the previous group builds on stream.
+ *   seg_bounds_host         host array [n_seg][2], checked on the host (HYPIC_EINVAL if a body
+ *                           leaves [0, n_tokens) or is longer than max_len) and copied to
+ *                           bounds_dev (device, [n_seg][2])
+ *   k_host, v_host          host [n_tokens, H, d] in in_dtype; alpha_host [n_tokens, H] (or
+ *                           [n_tokens, H, d] for DIAG and KDA), unused for DELTA; beta_host
+ *                           [n_tokens, H], delta families only.  Pinned memory lets the copies
+ *                           run asynchronously; pageable memory works but the copies then block.
+ *   k_dev, v_dev, alpha_dev, beta_dev
+ *                           device buffers of the same shapes, 16-byte aligned; only the rows of
+ *                           the bodies are written.  Caller-owned; the call makes the copies wait
+ *                           for the work already on stream before overwriting them.
+ *   T_out, S_out, ws        as in hypic_segment_build_batched (workspace sized by
+ *                           hypic_build_workspace_bytes for the whole request).
+ *   stream                  the build's stream; everything enqueued on it later sees the pairs.
+ *   copy_stream             the copies' stream (null or equal to stream: no overlap).
+ * Asynchronous; events the library creates once per device order the two streams.  Calls on one
+ * device are serialised on the host while they enqueue.
+ */
+hypic_status hypic_segment_build_batched_host(const hypic_shape *shape, int32_t n_seg,
+                                              const int64_t *seg_bounds_host, int64_t max_len, int64_t n_tokens,
+                                              const void *k_host, const void *v_host, const float *alpha_host,
+                                              const float *beta_host, void *k_dev, void *v_dev, float *alpha_dev,
+                                              float *beta_dev, int64_t *bounds_dev, float *T_out, float *S_out,
+                                              void *ws, size_t ws_bytes, hypic_stream_t stream,
+                                              hypic_stream_t copy_stream);
+
+/*
  * Workspace bytes the build prefers for n_seg bodies of at most max_len tokens
  * (0 when the shape runs without one).  The d = 128 bf16 delta-family build
  * keeps one 49,664-byte operand record per (64-token chunk, head) in it; it

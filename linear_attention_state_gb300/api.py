@@ -132,6 +132,71 @@ def segment_build_batched(k, v, bounds, alpha=None, beta=None, q=None, family="g
     return (T, S, o) if want_o else (T, S)
 
 
+def _host(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor (pinned for asynchronous copies)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def segment_build_batched_host(k, v, bounds, alpha=None, beta=None, family="gated_delta", max_len=None,
+                               dev=None, out=None, ws=None, stream=None, copy_stream=None, device="cuda"):
+    """The batched build from host tensors (pinned memory: the copies overlap the build).
+
+    k, v [n_tok, H, d], alpha/beta and bounds (int64 [n_seg, 2]) live on the host.  ``dev`` is a
+    tuple of device buffers (k, v, alpha, beta, bounds) of the same shapes (allocated when None);
+    the copies run on ``copy_stream`` (a new stream when None) while earlier segment groups build
+    on ``stream``.  Returns (T, S) on the device, ready on ``stream``."""
+    lib = L.load()
+    _host(k, "k"), _host(v, "v", k.dtype), _host(bounds, "bounds", torch.int64)
+    n_tok, H, d = k.shape
+    n_seg = bounds.shape[0]
+    alpha = _host(alpha, "alpha", torch.float32, allow_none=family == "delta")
+    beta = _host(beta, "beta", torch.float32, allow_none=family not in ("delta", "gated_delta", "kda"))
+    if max_len is None:
+        max_len = int((bounds[:, 1] - bounds[:, 0]).max().item()) if n_seg else 0
+    if dev is None:
+        dev = tuple(None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device)
+                    for t in (k, v, alpha, beta, bounds))
+    k_d, v_d, a_d, b_d, bn_d = dev
+    _cuda(k_d, "k_dev", k.dtype), _cuda(v_d, "v_dev", k.dtype), _cuda(bn_d, "bounds_dev", torch.int64)
+    if alpha is not None:
+        _cuda(a_d, "alpha_dev", torch.float32)
+    if beta is not None:
+        _cuda(b_d, "beta_dev", torch.float32)
+    sh = L.shape(H, d, family, _in_dtype(k))
+    if out is None:
+        T = torch.empty((n_seg, H, t_size(family, d)), device=k_d.device, dtype=torch.float32)
+        S = torch.empty((n_seg, H, d, d), device=k_d.device, dtype=torch.float32)
+    else:
+        T, S = out
+        _cuda(T, "T_out", torch.float32), _cuda(S, "S_out", torch.float32)
+    if ws is None:
+        ws_bytes = lib.hypic_build_workspace_bytes(ctypes.byref(sh), n_seg, max_len)
+        ws = torch.empty(ws_bytes, device=k_d.device, dtype=torch.uint8) if ws_bytes else None
+    else:
+        _cuda(ws, "ws", torch.uint8)
+        ws_bytes = ws.numel()
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=k_d.device)
+    st = lib.hypic_segment_build_batched_host(ctypes.byref(sh), n_seg, ctypes.c_void_p(bounds.data_ptr()), max_len,
+                                              n_tok, ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                              None if alpha is None else ctypes.c_void_p(alpha.data_ptr()),
+                                              None if beta is None else ctypes.c_void_p(beta.data_ptr()),
+                                              _p(k_d), _p(v_d), _p(a_d if alpha is not None else None),
+                                              _p(b_d if beta is not None else None), _p(bn_d), _p(T), _p(S), _p(ws),
+                                              ws_bytes, _stream(stream), _stream(copy_stream))
+    L.check(st, "hypic_segment_build_batched_host")
+    return T.view(_t_shape(family, (n_seg, H), d)), S
+
+
 def _pool_dtype(pool_T, pool_S):
     """fp32 pools, or bf16 pools (16-bit pair storage, see pairs_to_bf16); both the same."""
     dt = pool_S.dtype if isinstance(pool_S, torch.Tensor) else None

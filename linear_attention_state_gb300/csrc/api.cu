@@ -179,6 +179,112 @@ hypic_status hypic_segment_build_batched(const hypic_shape *sh, int32_t n_seg, c
                       ws_bytes, (cudaStream_t)stream);
 }
 
+hypic_status hypic_segment_build_batched_host(const hypic_shape *sh, int32_t n_seg, const int64_t *seg_bounds_host,
+                                              int64_t max_len, int64_t n_tokens, const void *k_host,
+                                              const void *v_host, const float *alpha_host, const float *beta_host,
+                                              void *k_dev, void *v_dev, float *alpha_dev, float *beta_dev,
+                                              int64_t *bounds_dev, float *T_out, float *S_out, void *ws,
+                                              size_t ws_bytes, hypic_stream_t stream, hypic_stream_t copy_stream) {
+  hypic_status r = check_shape(sh);
+  if (r != HYPIC_OK) return r;
+  if (n_seg < 0 || max_len < 0 || n_tokens < 0) return HYPIC_EINVAL;
+  if (n_seg == 0 || sh->H == 0) return HYPIC_OK;
+  if (!seg_bounds_host || !ok_ptr(bounds_dev)) return HYPIC_EINVAL;
+  const bool tokens = n_tokens > 0 && max_len > 0;
+  if (tokens) {
+    if (!k_host || !v_host || !ok_ptr(k_dev) || !ok_ptr(v_dev)) return HYPIC_EINVAL;
+    if (sh->family != HYPIC_FAM_DELTA && (!alpha_host || !ok_ptr(alpha_dev))) return HYPIC_EINVAL;
+    if (dense_family(sh->family) && (!beta_host || !ok_ptr(beta_dev))) return HYPIC_EINVAL;
+  }
+  // Host-side copy plan: the bodies' token rows, checked against the token axis here (the
+  // kernels check them again on the device).
+  for (int32_t i = 0; i < n_seg; ++i) {
+    const int64_t b = seg_bounds_host[2 * i], e = seg_bounds_host[2 * i + 1];
+    if (b < 0 || e < b || e - b > max_len || e > n_tokens) return HYPIC_EINVAL;
+  }
+  const size_t el = sh->in_dtype == HYPIC_BF16 ? 2 : 4;
+  const size_t row_kv = (size_t)sh->H * sh->d_k * el;
+  const bool per_channel_alpha = sh->family == HYPIC_FAM_DIAG || sh->family == HYPIC_FAM_KDA;
+  const size_t row_a = (size_t)sh->H * (per_channel_alpha ? sh->d_k : 1) * sizeof(float);
+  const size_t row_b = (size_t)sh->H * sizeof(float);
+  const int64_t tsz = hypic_t_size(sh);
+  cudaStream_t st = (cudaStream_t)stream, cp = copy_stream ? (cudaStream_t)copy_stream : st;
+  // Groups of consecutive segments holding about an eighth of the body tokens each (at most
+  // kMaxGroups), so that the last group's build, which no copy hides, stays short.
+  int64_t body_total = 0;
+  for (int32_t i = 0; i < n_seg; ++i) body_total += seg_bounds_host[2 * i + 1] - seg_bounds_host[2 * i];
+  constexpr int kMaxGroups = 16;
+  const int64_t target = body_total / 8 > 1 ? body_total / 8 : 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HYPIC_ECUDA;
+  static std::mutex mu[kMaxDevices];
+  static cudaEvent_t ev[kMaxDevices][kMaxGroups + 1];
+  static bool ev_ready[kMaxDevices];
+  std::lock_guard<std::mutex> lock(mu[dev]);
+  if (!ev_ready[dev]) {
+    for (int i = 0; i <= kMaxGroups; ++i)
+      if (cudaEventCreateWithFlags(&ev[dev][i], cudaEventDisableTiming) != cudaSuccess) return HYPIC_ECUDA;
+    ev_ready[dev] = true;
+  }
+  // The copies may overwrite the device buffers only after the work already on the compute
+  // stream (an earlier request reading them) is done.
+  if (cp != st) {
+    if (cudaEventRecord(ev[dev][kMaxGroups], st) != cudaSuccess) return HYPIC_ECUDA;
+    if (cudaStreamWaitEvent(cp, ev[dev][kMaxGroups], 0) != cudaSuccess) return HYPIC_ECUDA;
+  }
+  if (cudaMemcpyAsync(bounds_dev, seg_bounds_host, sizeof(int64_t) * 2 * n_seg, cudaMemcpyHostToDevice, cp) !=
+      cudaSuccess)
+    return HYPIC_ECUDA;
+  int32_t g0 = 0;
+  int groups = 0;
+  while (g0 < n_seg) {
+    int32_t g1 = g0 + 1;
+    if (groups == kMaxGroups - 1) {
+      g1 = n_seg;  // the last group takes the rest
+    } else {
+      int64_t acc = seg_bounds_host[2 * g0 + 1] - seg_bounds_host[2 * g0];
+      while (g1 < n_seg && acc < target) {
+        acc += seg_bounds_host[2 * g1 + 1] - seg_bounds_host[2 * g1];
+        ++g1;
+      }
+    }
+    // Token rows of the group's bodies, each through the end of its last 64-token chunk: the
+    // build reads whole chunks (rows past a body's end enter with zero gates), so those rows
+    // must hold the request's own tokens, as they do when the inputs are already on the device.
+    int64_t r0 = INT64_MAX, r1 = 0;
+    for (int32_t i = g0; i < g1; ++i) {
+      const int64_t b = seg_bounds_host[2 * i], e = seg_bounds_host[2 * i + 1];
+      if (e > b) {
+        const int64_t ep = b + (e - b + 63) / 64 * 64;
+        r0 = b < r0 ? b : r0;
+        r1 = (ep < n_tokens ? ep : n_tokens) > r1 ? (ep < n_tokens ? ep : n_tokens) : r1;
+      }
+    }
+    if (tokens && r1 > r0) {
+      const size_t n = (size_t)(r1 - r0);
+      auto h2d = [&](void *dst, const void *src, size_t row) {
+        return cudaMemcpyAsync(static_cast<char *>(dst) + r0 * row, static_cast<const char *>(src) + r0 * row,
+                               n * row, cudaMemcpyHostToDevice, cp);
+      };
+      if (h2d(k_dev, k_host, row_kv) != cudaSuccess || h2d(v_dev, v_host, row_kv) != cudaSuccess) return HYPIC_ECUDA;
+      if (sh->family != HYPIC_FAM_DELTA && h2d(alpha_dev, alpha_host, row_a) != cudaSuccess) return HYPIC_ECUDA;
+      if (dense_family(sh->family) && h2d(beta_dev, beta_host, row_b) != cudaSuccess) return HYPIC_ECUDA;
+    }
+    if (cp != st) {
+      if (cudaEventRecord(ev[dev][groups], cp) != cudaSuccess) return HYPIC_ECUDA;
+      if (cudaStreamWaitEvent(st, ev[dev][groups], 0) != cudaSuccess) return HYPIC_ECUDA;
+    }
+    SegMap m{bounds_dev + 2 * g0, 0, 0, 0, max_len, n_tokens};
+    r = build_common(sh, g1 - g0, m, k_dev, v_dev, nullptr, sh->family == HYPIC_FAM_DELTA ? nullptr : alpha_dev,
+                     dense_family(sh->family) ? beta_dev : nullptr, T_out + (size_t)g0 * sh->H * tsz,
+                     S_out + (size_t)g0 * sh->H * sh->d_k * sh->d_v, nullptr, tokens, ws, ws_bytes, st);
+    if (r != HYPIC_OK) return r;
+    ++groups;
+    g0 = g1;
+  }
+  return HYPIC_OK;
+}
+
 hypic_status hypic_seam_advance(const hypic_shape *sh, int32_t B, float *S_inout, const void *q,
                                 const void *k, const void *v, const float *alpha, const float *beta,
                                 int32_t w, float *o_out, hypic_stream_t stream) {

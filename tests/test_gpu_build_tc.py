@@ -189,3 +189,28 @@ def test_outputs_agree_with_recurrent_path(monkeypatch):
     assert hy.stream_status() == 0
     for h in range(H):
         assert relerr(np64(o1[:369, h]), np64(o2[:369, h])) <= TOL_BF16
+
+
+def test_build_from_host_inputs_matches_device_inputs():
+    """hypic_segment_build_batched_host: the bodies' rows are copied in segment groups on a second
+    stream while earlier groups build; the pairs equal those of the device-input build bit for bit
+    (same kernels, one CTA per unit in both) and the oracle's within the bf16-path tolerance."""
+    lens = [0, 1, 63, 64, 300, 700, 129, 2, 1000, 65]
+    H = 4
+    tok, bounds, T, S = run_case("gated_delta", lens, H, key=21)
+    host = {n: tok[n].cpu().pin_memory() for n in ("k", "v", "alpha", "beta")}
+    b_host = torch.tensor(bounds, dtype=torch.int64)
+    dev = tuple(torch.full_like(tok[n], float("nan")) for n in ("k", "v", "alpha", "beta")) + \
+        (torch.zeros(len(lens), 2, dtype=torch.int64, device=DEV),)
+    copy_stream = torch.cuda.Stream()
+    for _ in range(2):  # a second call reuses the device buffers and the library's events
+        T2, S2 = hy.segment_build_batched_host(host["k"], host["v"], b_host, host["alpha"], host["beta"],
+                                               family="gated_delta", dev=dev, copy_stream=copy_stream)
+        assert hy.stream_status() == 0
+        assert torch.equal(T2, T) and torch.equal(S2, S)
+    assert torch.equal(dev[4].cpu(), b_host)
+    hk = host_tokens(tok, list(range(H)))
+    for s in (4, 5, 8):
+        for h in range(H):
+            Tr, Sr = ref_pair("gated_delta", hk, h, *bounds[s])
+            assert relerr(np64(T2[s, h]), Tr) <= TOL_BF16 and relerr(np64(S2[s, h]), Sr) <= TOL_BF16

@@ -164,11 +164,13 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *shape, int32_t 
  * processes the heads in blocks that fit the workspace it is given, so any size
  * that holds one head's records (n_seg * ceil(max_len / 64) * 49,664 bytes)
  * works, and less gives HYPIC_ENOSPACE.  The preferred size covers all heads up
- * to about 4 GiB of records, plus min(n_seg * heads, 256) * 131,072 + 3,072 bytes
- * for the split chain schedule: with more (segment, head) units than the GPU holds
- * chain CTAs at once, one CTA per SM runs an equal share of all chunks and a cut
- * segment's two pairs are composed in the kernel (a cooperative launch).  Without
- * that room each unit gets its own CTA; results agree to rounding either way.  The
+ * to about 4 GiB of records, plus N * 131,072 + 3,072 bytes for the split chain
+ * schedule, N = min(256, max(U, U * ceil(max_len / 64) / 8)) with U = n_seg * heads:
+ * the chain then runs at most one CTA per SM over equal shares of all chunks (a
+ * cooperative launch), segments cut between CTAs (once when U exceeds the SMs,
+ * into pieces of at least 8 chunks when there are fewer units) are rejoined by
+ * composing their pieces' pairs in the kernel.  Without that room each unit gets
+ * its own CTA; results agree to rounding either way.  The
  * workspace is caller-owned device memory, 16-byte aligned, and must not be used
  * by anything else until the stream reaches the end of the call.
  */

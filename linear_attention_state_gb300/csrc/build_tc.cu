@@ -108,17 +108,19 @@ __device__ __forceinline__ uint8_t *ws_rec(const BuildTcArgs &a, int s, int c, i
 
 // Work of one chain CTA: the chunk steps [lo, hi) of a list that runs through the units (segment,
 // head) in order, max_chunks steps per unit (steps past a segment's end are empty).  With
-// q_steps == max_chunks each CTA owns one whole unit.  With more steps per CTA (a grid of one CTA
-// per SM, launched cooperatively so that all CTAs are resident together) a unit may be cut once,
-// between neighbouring CTAs b and b + 1: CTA b + 1 runs the unit's tail first and publishes its
-// pair (T_B, S_B) in slot b + 1; CTA b runs the unit's head last and finishes with the composition
-// X = T_B X_A + [0 | S_B] (the composition law of segment pairs) before writing the unit's result.
-enum : int { PIECE_WHOLE = 0, PIECE_HEAD = 1, PIECE_TAIL = 2, PIECE_NONE = 3 };
+// q_steps == max_chunks each CTA owns one whole unit.  Otherwise (a grid of at most one CTA per
+// SM, launched cooperatively so that all CTAs are resident together) a unit may be cut between
+// CTAs b, b + 1, ..., b + m: each later CTA runs its piece of the unit first (the whole of its
+// share, for a middle piece) from [I | 0] and publishes the pair in its slot; CTA b runs the
+// unit's head last and composes the m published pairs onto it in order, X <- T_c X + [0 | S_c]
+// (the composition law of segment pairs), before writing the unit's result.
+enum : int { PIECE_WHOLE = 0, PIECE_HEAD = 1, PIECE_TAIL = 2, PIECE_NONE = 3 };  // TAIL: also middle pieces
 struct Piece {
   int s, hh;       // the unit
   int64_t beg;     // first token of its body
   int c_lo, c_hi;  // valid chunks [c_lo, c_hi) in this CTA's share
   int kind;
+  int n_fix;       // a head: the later pieces to compose onto it
   bool ok;         // segment bounds valid
 };
 __device__ __forceinline__ Piece piece_of(const BuildTcArgs &a, long long u, long long lo, long long hi) {
@@ -138,13 +140,15 @@ __device__ __forceinline__ Piece piece_of(const BuildTcArgs &a, long long u, lon
     p.kind = s_hi >= nch ? PIECE_WHOLE : PIECE_HEAD;
   else
     p.kind = s_lo < nch ? PIECE_TAIL : PIECE_NONE;
+  // CTA b + c holds unit steps [s_hi + (c - 1) q, s_hi + c q): a piece while that starts before nch
+  p.n_fix = p.kind == PIECE_HEAD ? (int)((nch - s_hi + a.q_steps - 1) / a.q_steps) : 0;
   return p;
 }
 
 // Split chain schedule, written by the prep kernel's first CTA (the chain runs after it): the
-// chain CTAs' publish flags cleared, and per chain CTA its number of chunk steps and whether it
-// ends on a cut unit's head (or meets a unit with bad bounds).  The chain then reads its loop
-// bounds with plain loads.
+// chain CTAs' publish flags cleared, and per chain CTA its number of chunk steps and the number of
+// pairs it composes onto a cut unit's head at the end (bit 30: it meets a unit with bad bounds).
+// The chain then reads its loop bounds with plain loads.
 __device__ __noinline__ void chain_schedule(const BuildTcArgs &a) {
   const long long total = (long long)a.n_units * a.max_chunks;
   for (int b = threadIdx.x; b < a.n_flags; b += blockDim.x) {
@@ -155,7 +159,7 @@ __device__ __noinline__ void chain_schedule(const BuildTcArgs &a) {
     for (long long u = lo / a.max_chunks; u * a.max_chunks < hi; ++u) {
       const Piece p = piece_of(a, u, lo, hi);
       J += p.c_hi - p.c_lo;
-      f = (f & 2) | (p.kind == PIECE_HEAD ? 1 : 0) | (p.ok ? 0 : 2);
+      f = (f & (1 << 30)) | p.n_fix | (p.ok ? 0 : 1 << 30);  // only the last piece can be a head
     }
     a.sched[2 * b] = J;
     a.sched[2 * b + 1] = f;
@@ -662,81 +666,88 @@ __device__ __noinline__ bool conv_compose_head(const BuildTcArgs &a, const Piece
                                                uint8_t *xlo, uint8_t *sm, uint64_t *bar_r1h, uint64_t *bar_xh,
                                                int J, bool ok) {
   const int tid = threadIdx.x, row = conv_row(), part = conv_part(), half = conv_half();
-  const float *pairB = a.part + (size_t)(blockIdx.x + 1) * 2 * D * D;
-  if (tid == 0 && ok) ok = wait_published(&a.flags[blockIdx.x + 1], a.err);
-  const bool bad = bar_or_named(1, NCONV, !ok);
-  if (!bad) {
-    // T_B as K-major bf16 hi and lo tiles: thread -> row i, columns [32 qb, 32 qb + 32).
-    const int i = tid >> 2, qb = tid & 3;
-    const float *src = pairB + (size_t)i * D + 32 * qb;
-    for (int m = 0; m < 4; ++m) {
-      float v[8];
-      const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m));
-      const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m + 4));
-      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
-      v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
-      uint4 h8, l8;
-      split8(v, h8, l8);
-      const uint32_t col = 32u * qb + 8u * m;
-      const uint32_t off = (col / 64) * 16384u + sw128_offset((uint32_t)i, (col % 64) / 8);
-      *reinterpret_cast<uint4 *>(sm + FX_TBH + off) = h8;
-      *reinterpret_cast<uint4 *>(sm + FX_TBL + off) = l8;
-    }
-    // X_A^T pieces as in step (1); the accumulator restarts at [0 | S_B]^T.
-    const float *sB = pairB + (size_t)D * D;
-    for (int cb = 0; cb < 64; cb += 32) {
-      float xv[32];
-      tmem_ld32(tx + 64 * part + cb, xv);
-      float ph[16];
-      uint32_t pl[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        uint32_t hi2;
-        split2_pair(xv[2 * q], xv[2 * q + 1], hi2, pl[q]);
-        ph[q] = __uint_as_float(hi2);
+  bool bad = false;
+  for (int c = 1; c <= p.n_fix; ++c) {
+    const float *pairB = a.part + (size_t)(blockIdx.x + c) * 2 * D * D;
+    if (tid == 0 && ok && !bad) ok = wait_published(&a.flags[blockIdx.x + c], a.err);
+    // Past this barrier both halves' previous MMAs are done, so stage 0 is free.
+    bad = bar_or_named(1, NCONV, !ok || bad);
+    if (!bad) {
+      // T_B as K-major bf16 hi and lo tiles: thread -> row i, columns [32 qb, 32 qb + 32).
+      const int i = tid >> 2, qb = tid & 3;
+      const float *src = pairB + (size_t)i * D + 32 * qb;
+      for (int m = 0; m < 4; ++m) {
+        float v[8];
+        const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m));
+        const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + 8 * m + 4));
+        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+        v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+        uint4 h8, l8;
+        split8(v, h8, l8);
+        const uint32_t col = 32u * qb + 8u * m;
+        const uint32_t off = (col / 64) * 16384u + sw128_offset((uint32_t)i, (col % 64) / 8);
+        *reinterpret_cast<uint4 *>(sm + FX_TBH + off) = h8;
+        *reinterpret_cast<uint4 *>(sm + FX_TBL + off) = l8;
       }
-      tmem_st16(txp + (64 * part + cb) / 2, ph);
+      // X^T pieces as in step (1); the accumulator restarts at [0 | S_B]^T.
+      const float *sB = pairB + (size_t)D * D;
+      for (int cb = 0; cb < 64; cb += 32) {
+        float xv[32];
+        tmem_ld32(tx + 64 * part + cb, xv);
+        float ph[16];
+        uint32_t pl[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
-            make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+        for (int q = 0; q < 16; ++q) {
+          uint32_t hi2;
+          split2_pair(xv[2 * q], xv[2 * q + 1], hi2, pl[q]);
+          ph[q] = __uint_as_float(hi2);
+        }
+        tmem_st16(txp + (64 * part + cb) / 2, ph);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) xv[q] = half ? __ldcg(sB + (size_t)(64 * part + cb + q) * D + row) : 0.f;
-      tmem_st32(tx + 64 * part + cb, xv);
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4 *>(xlo + sw128_offset((uint32_t)row, (uint32_t)(cb / 8 + k))) =
+              make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) xv[q] = half ? __ldcg(sB + (size_t)(64 * part + cb + q) * D + row) : 0.f;
+        tmem_st32(tx + 64 * part + cb, xv);
+      }
+      tmem_st_wait();
     }
-    tmem_st_wait();
+    fence_proxy_async();
+    tc_fence_before();
+    bar_sync_named(1, NCONV);  // T_B tiles complete
+    mbar_arrive(bar_r1h);
+    const bool fx = mbar_wait_sleep(bar_xh, (uint32_t)(J + c - 1) & 1u, a.err);
+    tc_fence_after();
+    ok = ok && fx;
   }
-  fence_proxy_async();
-  tc_fence_before();
-  bar_sync_named(1, NCONV);  // T_B tiles complete
-  mbar_arrive(bar_r1h);
-  const bool fx = mbar_wait_sleep(bar_xh, (uint32_t)J & 1u, a.err);
-  tc_fence_after();
-  ok = ok && !bad && fx;
+  ok = ok && !bad;
   if (ok) conv_write_x(tx, unit_out(a, p, half));
   return ok;
 }
-// The MMA warp's part of a cut unit's head: X^T += X_A^T T_B^T on top of [0 | S_B]^T per half
-// (M = 128 n, N = 128 i, K = 128 j), hi.hi + hi.lo + lo.hi with T_B split like the chunk operands.
+// The MMA warp's part of a cut unit's head, once per published pair: X^T += X^T T_B^T on top of
+// [0 | S_B]^T per half (M = 128 n, N = 128 i, K = 128 j), hi.hi + hi.lo + lo.hi with T_B split like
+// the chunk operands.
 __device__ __noinline__ bool mma_compose_head(uint32_t tmem, uint32_t sb, uint64_t *bar_r1, uint64_t *bar_x, int J,
-                                              int *err) {
+                                              int n_fix, int *err) {
   const uint32_t id_f = idesc_f32acc(1, 1, 0, 0, 128, 128);
   const uint64_t dTH = sdesc_sw128(sb + FX_TBH, 16, 1024);
   const uint64_t dTL = sdesc_sw128(sb + FX_TBL, 16, 1024);
   const uint64_t dXL = sdesc_sw128(sb + OFF_XLO, 16, 1024);
-  const uint32_t par = (uint32_t)J & 1u;
-  for (int hf = 0; hf < 2; ++hf) {
-    if (!mbar_wait_cycles(&bar_r1[hf], par, err)) return false;
-    tc_fence_after();
+  for (int c = 0; c < n_fix; ++c) {
+    for (int hf = 0; hf < 2; ++hf) {
+      if (!mbar_wait_cycles(&bar_r1[hf], (uint32_t)(J + c) & 1u, err)) return false;
+      tc_fence_after();
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t ko = (uint64_t)(kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-      const uint64_t al = dXL + hf * 2048 + (kk >> 2) * 1024 + (kk & 3) * 2;
-      mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTH + ko, id_f, 1);
-      mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTL + ko, id_f, 1);
-      mma_f16(tmem + tm_x(hf), al, dTH + ko, id_f, 1);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ko = (uint64_t)(kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+        const uint64_t al = dXL + hf * 2048 + (kk >> 2) * 1024 + (kk & 3) * 2;
+        mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTH + ko, id_f, 1);
+        mma_f16_tmem_a(tmem + tm_x(hf), tmem + tm_xp(hf) + kk * 8, dTL + ko, id_f, 1);
+        mma_f16(tmem + tm_x(hf), al, dTH + ko, id_f, 1);
+      }
+      mma_commit(&bar_x[hf]);
     }
-    mma_commit(&bar_x[hf]);
   }
   return true;
 }
@@ -759,15 +770,15 @@ __global__ void __launch_bounds__(NT2, 1)
   const int part = (tid >> 7) & 1;  // which half of that lane's columns
   const int half = (tid >> 8) & 1;  // 0: T columns, 1: S columns
 
-  // This CTA's chunk steps J and whether it ends on a cut unit's head: from the schedule the prep
-  // kernel wrote, or with one unit per CTA straight from the unit's bounds.
-  int J = 0;
-  bool has_fix = false, bounds_ok = true;
+  // This CTA's chunk steps J and the pairs it composes onto a cut unit's head at the end: from the
+  // schedule the prep kernel wrote, or with one unit per CTA straight from the unit's bounds.
+  int J = 0, n_fix = 0;
+  bool bounds_ok = true;
   if (a.sched) {
     J = a.sched[2 * blockIdx.x];
     const int f = a.sched[2 * blockIdx.x + 1];
-    has_fix = (f & 1) != 0;
-    bounds_ok = (f & 2) == 0;
+    n_fix = f & 0xffff;
+    bounds_ok = (f & (1 << 30)) == 0;
   } else {
     int64_t beg, end;
     bounds_ok = seg_bounds(a, (int)(blockIdx.x / a.Hb), beg, end);
@@ -910,7 +921,7 @@ __global__ void __launch_bounds__(NT2, 1)
       bool ok = J == 0 || issue_u(0, std::integral_constant<int, 0>{});
       for (int j = 0; j < J && ok; ++j) ok = step(j);
       if constexpr (!T_ONLY)
-        if (ok && has_fix) ok = mma_compose_head(tmem, sb, bar_r1, bar_x, J, a.err);
+        if (ok && n_fix > 0) ok = mma_compose_head(tmem, sb, bar_r1, bar_x, J, n_fix, a.err);
       if (!ok) abort_flag = 1;
     }
     __syncwarp();
@@ -1322,12 +1333,18 @@ size_t bytes_per_head(int n_seg, int64_t max_len, bool want_o) {
 }
 
 // Pair slots of the split chain schedule, after the records: one (T, S) pair per chain CTA (at
-// most kSplitSlots CTAs), then a publish flag each and the CTAs' schedule (two ints each).
+// most kSplitSlots CTAs), then a publish flag each and the CTAs' schedule (two ints each).  With
+// fewer units than SMs a unit may be cut several times, into pieces of at least kMinPiece chunk
+// steps, so the slots are counted from the chunk steps as well.
 constexpr int kSplitSlots = 256;
+constexpr int kMinPiece = 8;
 constexpr size_t kSlotBytes = 2 * D * D * sizeof(float);
-int split_slots(long long units) { return (int)(units < kSplitSlots ? (units > 0 ? units : 0) : kSplitSlots); }
-size_t split_bytes(long long units) {
-  const int n = split_slots(units);
+int split_slots(long long units, long long steps) {
+  long long n = steps / kMinPiece > units ? steps / kMinPiece : units;
+  return (int)(n < kSplitSlots ? (n > 0 ? n : 0) : kSplitSlots);
+}
+size_t split_bytes(long long units, long long steps) {
+  const int n = split_slots(units, steps);
   return n ? (size_t)n * kSlotBytes + 3 * kSplitSlots * sizeof(int) : 0;  // + flags and schedule
 }
 
@@ -1364,7 +1381,9 @@ size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o) 
   size_t heads = WS_CAP / per;
   if (heads < 1) heads = 1;
   if (heads > (size_t)H) heads = (size_t)H;
-  return heads * per + (want_o ? 0 : split_bytes((long long)n_seg * (long long)heads));
+  const long long units = (long long)n_seg * (long long)heads;
+  const int64_t chunks = (max_len + C - 1) / C;
+  return heads * per + (want_o ? 0 : split_bytes(units, units * (chunks > 0 ? chunks : 1)));
 }
 
 // Runs the build over head blocks that fit the workspace: prep then chain for each block (and,
@@ -1419,7 +1438,8 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
   }
   // The split chain schedule needs its pair slots after the records and a cooperative launch.
   const size_t rec_end = (size_t)Hb * per;  // a multiple of 256 bytes
-  const bool split_room = !wo && ws_bytes >= rec_end + split_bytes((long long)r.n_seg * Hb);
+  const bool split_room =
+      !wo && ws_bytes >= rec_end + split_bytes((long long)r.n_seg * Hb, (long long)r.n_seg * Hb * a.max_chunks);
   const int resident = split_room ? chain_resident_ctas() : 0;
   for (int h0 = 0; h0 < r.H; h0 += Hb) {
     a.h0 = h0;
@@ -1434,16 +1454,26 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     a.sched = nullptr;
     a.n_flags = 0;
     long long g2 = units;
-    const int cap = resident < kSplitSlots ? resident : kSplitSlots;
+    const long long steps = units * a.max_chunks;
+    const int slots = split_slots(units, steps);
+    const int cap = resident < slots ? resident : slots;
+    // More units than resident CTAs: cap CTAs over equal shares of the chunk steps, each unit cut
+    // at most once.  Fewer: the same when it shortens the longest share by a quarter or more, the
+    // units then cut into pieces of at least kMinPiece steps.
+    long long q = 0;
     if (cap > 0 && units > cap) {
-      // more units than resident CTAs: cap CTAs, each an equal share of the chunk steps
-      const long long steps = units * a.max_chunks;
-      const long long q = (steps + cap - 1) / cap;
+      q = (steps + cap - 1) / cap;
+    } else if (cap > 0) {
+      const long long qm = (steps + cap - 1) / cap;
+      q = qm > kMinPiece ? qm : kMinPiece;
+      if (4 * q > 3 * (long long)a.max_chunks) q = 0;
+    }
+    if (q > 0) {
       if (q > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
       a.q_steps = (int)q;
       g2 = (steps + q - 1) / q;
       a.part = reinterpret_cast<float *>(a.ws + rec_end);
-      a.flags = reinterpret_cast<int *>(a.ws + rec_end + (size_t)split_slots(units) * kSlotBytes);
+      a.flags = reinterpret_cast<int *>(a.ws + rec_end + (size_t)slots * kSlotBytes);
       a.sched = a.flags + kSplitSlots;
       a.n_flags = (int)g2;
     }

@@ -125,6 +125,34 @@ def test_more_units_than_resident_ctas(family, gate_div):
             assert float(S[s].abs().max()) == 0.0
 
 
+@pytest.mark.parametrize("family,gate_div", [("delta", None), ("gated_delta", 1024.0)])
+def test_fewer_units_than_sms_cut_several_times(family, gate_div):
+    """Fewer (segment, head) units than SMs: the chain spreads each unit over several CTAs in pieces
+    of at least 8 chunks, and the CTA holding a unit's head composes the later pieces' published
+    pairs onto it in order.  Long ragged bodies give heads with up to seven pairs to compose;
+    a = 1 or slow decay keeps T_C large, so the composed T half is really checked."""
+    lens = [4096, 3001, 577, 0]
+    H = 2
+    tok, bounds, T, S = run_case(family, lens, H, key=31, gate_div=gate_div)
+    records = len(lens) * 64 * 49664 * H
+    ws = torch.empty(records, dtype=torch.uint8, device=DEV)
+    T1, S1 = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                      tok["beta"], family=family, ws=ws)
+    assert hy.stream_status() == 0
+    host = host_tokens(tok, list(range(H)))
+    eT = eS = 0.0
+    for s, (b, e) in enumerate(bounds):
+        for h in range(H):
+            Tr, Sr = ref_pair(family, host, h, b, e)
+            eT = max(eT, relerr(np64(T[s, h]), Tr))
+            if e > b:
+                eS = max(eS, relerr(np64(S[s, h]), Sr))
+                assert relerr(np64(S[s, h]), np64(S1[s, h])) <= 1e-4
+    print(f"{family} cut into pieces: max rel err T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+    assert torch.equal(T[3], torch.eye(128, device=DEV).expand(H, 128, 128))
+
+
 def test_tensor_core_path_agrees_with_recurrent_path(monkeypatch):
     lens = [300, 64, 5]
     H = 2

@@ -586,18 +586,28 @@ def main():
     d2h = S_host.numel() * 4 + o_host.numel() * 4
 
     # The request's k, v and gates go through the host-input build, which copies segment groups on a
-    # second stream while the earlier ones build; the seam tokens (0.7 MB) are copied first.
+    # second stream while the earlier ones build; the seam tokens (0.7 MB) are copied first.  Two
+    # sets of device input buffers alternate between requests, as in a serving loop: request i + 1's
+    # inputs cross the host link while request i finishes (its last group, assembly and readback);
+    # the copies of a set wait for the event recorded after the previous build that read it.
     bounds_host = torch.tensor(req.bounds_list, dtype=torch.int64)
     copy_stream = torch.cuda.Stream()
     seam_names = [n for n in host if n.startswith("seam_")]
+    dev_sets = [(req.k, req.v, req.alpha, req.beta, req.bounds),
+                tuple(torch.empty_like(t) for t in (req.k, req.v, req.alpha, req.beta, req.bounds))]
+    set_free = [torch.cuda.Event(), torch.cuda.Event()]
+    turn = [0]
 
     def e2e_step(ev):
+        i = turn[0] % 2
         for n in seam_names:
             getattr(req, n).copy_(host[n], non_blocking=True)
         hy.segment_build_batched_host(host["k"], host["v"], bounds_host, host["alpha"], host["beta"],
-                                      family=w.family, max_len=req.max_len,
-                                      dev=(req.k, req.v, req.alpha, req.beta, req.bounds), out=(req.T, req.S),
-                                      ws=req.ws, copy_stream=copy_stream)
+                                      family=w.family, max_len=req.max_len, dev=dev_sets[i], out=(req.T, req.S),
+                                      ws=req.ws, copy_stream=copy_stream,
+                                      ready_event=set_free[i] if turn[0] >= 2 else None)
+        set_free[i].record()
+        turn[0] += 1
         hy.assemble(req.T, req.S, req.idx, req.seam_k, req.seam_v, req.seam_a, req.seam_b, seam_q=req.seam_q,
                     family=w.family, out=req.S_out, o_out=req.o)
         S_host.copy_(req.S_out, non_blocking=True)

@@ -146,6 +146,11 @@ hypic_status hypic_segment_build_batched(const hypic_shape *shape, int32_t n_seg
  *                           hypic_build_workspace_bytes for the whole request).
  *   stream                  the build's stream; everything enqueued on it later sees the pairs.
  *   copy_stream             the copies' stream (null or equal to stream: no overlap).
+ *   ready_event             a cudaEvent_t after which nothing reads the device input buffers any
+ *                           more, or null: the copies then wait for all work already on stream.
+ *                           A caller that alternates two sets of device buffers passes the event
+ *                           it recorded after the earlier build of the same set, so that one
+ *                           request's copies run while the previous request still computes.
  * Asynchronous; events the library creates once per device order the two streams.  Calls on one
  * device are serialised on the host while they enqueue.
  */
@@ -155,7 +160,7 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *shape, int32_t 
                                               const float *beta_host, void *k_dev, void *v_dev, float *alpha_dev,
                                               float *beta_dev, int64_t *bounds_dev, float *T_out, float *S_out,
                                               void *ws, size_t ws_bytes, hypic_stream_t stream,
-                                              hypic_stream_t copy_stream);
+                                              hypic_stream_t copy_stream, void *ready_event);
 
 /*
  * Workspace bytes the build prefers for n_seg bodies of at most max_len tokens

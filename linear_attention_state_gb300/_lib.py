@@ -33,7 +33,7 @@ SIGNATURES = {
     "hypic_segment_build_batched": (_i32, [_SP, _i32, _i64p, _i64, _i64, _vp, _vp, _vp, _fp, _fp, _fp, _fp,
                                            _fp, _vp, _sz, _vp]),
     "hypic_segment_build_batched_host": (_i32, [_SP, _i32, _i64p, _i64, _i64, _vp, _vp, _fp, _fp, _vp, _vp, _fp,
-                                                _fp, _i64p, _fp, _fp, _vp, _sz, _vp, _vp]),
+                                                _fp, _i64p, _fp, _fp, _vp, _sz, _vp, _vp, _vp]),
     "hypic_build_workspace_bytes": (_sz, [_SP, _i32, _i64]),
     "hypic_build_workspace_bytes_outputs": (_sz, [_SP, _i32, _i64]),
     "hypic_segment_build_batched_noalloc": (_i32, [_SP, _i32, _i64p, _i64, _i64, _vp, _vp, _vp, _fp, _fp, _fp,

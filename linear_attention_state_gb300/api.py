@@ -147,13 +147,16 @@ def _host(t, name, dtype=None, allow_none=False):
 
 
 def segment_build_batched_host(k, v, bounds, alpha=None, beta=None, family="gated_delta", max_len=None,
-                               dev=None, out=None, ws=None, stream=None, copy_stream=None, device="cuda"):
+                               dev=None, out=None, ws=None, stream=None, copy_stream=None, ready_event=None,
+                               device="cuda"):
     """The batched build from host tensors (pinned memory: the copies overlap the build).
 
     k, v [n_tok, H, d], alpha/beta and bounds (int64 [n_seg, 2]) live on the host.  ``dev`` is a
     tuple of device buffers (k, v, alpha, beta, bounds) of the same shapes (allocated when None);
     the copies run on ``copy_stream`` (a new stream when None) while earlier segment groups build
-    on ``stream``.  Returns (T, S) on the device, ready on ``stream``."""
+    on ``stream``.  ``ready_event`` (a torch.cuda.Event) marks when nothing reads the ``dev`` buffers
+    any more; without it the copies wait for all work already on ``stream``.  Returns (T, S) on the
+    device, ready on ``stream``."""
     lib = L.load()
     _host(k, "k"), _host(v, "v", k.dtype), _host(bounds, "bounds", torch.int64)
     n_tok, H, d = k.shape
@@ -192,7 +195,8 @@ def segment_build_batched_host(k, v, bounds, alpha=None, beta=None, family="gate
                                               None if beta is None else ctypes.c_void_p(beta.data_ptr()),
                                               _p(k_d), _p(v_d), _p(a_d if alpha is not None else None),
                                               _p(b_d if beta is not None else None), _p(bn_d), _p(T), _p(S), _p(ws),
-                                              ws_bytes, _stream(stream), _stream(copy_stream))
+                                              ws_bytes, _stream(stream), _stream(copy_stream),
+                                              None if ready_event is None else ctypes.c_void_p(ready_event.cuda_event))
     L.check(st, "hypic_segment_build_batched_host")
     return T.view(_t_shape(family, (n_seg, H), d)), S
 

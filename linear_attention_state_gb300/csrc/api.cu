@@ -184,7 +184,8 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *sh, int32_t n_s
                                               const void *v_host, const float *alpha_host, const float *beta_host,
                                               void *k_dev, void *v_dev, float *alpha_dev, float *beta_dev,
                                               int64_t *bounds_dev, float *T_out, float *S_out, void *ws,
-                                              size_t ws_bytes, hypic_stream_t stream, hypic_stream_t copy_stream) {
+                                              size_t ws_bytes, hypic_stream_t stream, hypic_stream_t copy_stream,
+                                              void *ready_event) {
   hypic_status r = check_shape(sh);
   if (r != HYPIC_OK) return r;
   if (n_seg < 0 || max_len < 0 || n_tokens < 0) return HYPIC_EINVAL;
@@ -226,9 +227,11 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *sh, int32_t n_s
       if (cudaEventCreateWithFlags(&ev[dev][i], cudaEventDisableTiming) != cudaSuccess) return HYPIC_ECUDA;
     ev_ready[dev] = true;
   }
-  // The copies may overwrite the device buffers only after the work already on the compute
-  // stream (an earlier request reading them) is done.
-  if (cp != st) {
+  // The copies may overwrite the device buffers only once nothing reads them any more: after the
+  // caller's ready event, or else after all the work already on the compute stream.
+  if (ready_event) {
+    if (cudaStreamWaitEvent(cp, (cudaEvent_t)ready_event, 0) != cudaSuccess) return HYPIC_ECUDA;
+  } else if (cp != st) {
     if (cudaEventRecord(ev[dev][kMaxGroups], st) != cudaSuccess) return HYPIC_ECUDA;
     if (cudaStreamWaitEvent(cp, ev[dev][kMaxGroups], 0) != cudaSuccess) return HYPIC_ECUDA;
   }

@@ -176,7 +176,7 @@ def test_host_input_build_checks_bounds_on_the_host(lib):
     sh = L.shape(4, 128, "gated_delta", "bf16")
     p = _fake()
     bounds = (ctypes.c_int64 * 4)(0, 10, 10, 30)
-    args = [p] * 4 + [p] * 5 + [p, p, p, 1 << 20, None, None]
+    args = [p] * 4 + [p] * 5 + [p, p, p, 1 << 20, None, None, None]
     # a body past the token axis, and one longer than max_len: rejected before anything runs
     assert lib.hypic_segment_build_batched_host(ctypes.byref(sh), 2, bounds, 64, 20, *args) == L.HYPIC_EINVAL
     assert lib.hypic_segment_build_batched_host(ctypes.byref(sh), 2, bounds, 16, 30, *args) == L.HYPIC_EINVAL

@@ -293,35 +293,35 @@ __global__ void __launch_bounds__(NT, WO ? 4 : 6)
   }
   __syncthreads();
   if (ok_flag) {
-    // L_ts = b_t 2^(G_t - G_s) Gram_ts (s < t); Gram row t sits in lane 32(t/16) + t%16.
-    const int t = warp * 16 + lane;
-    const float Gt = lane < 16 ? sG[t] : 0.f;
-    const float bt = lane < 16 ? sBv[t] : 0.f;
-    const float be = lane < 16 ? bt * sE[t] : 0.f;
-#pragma unroll 1
-    for (int hb = 0; hb < C; hb += 32) {
-      float v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + hb, v);
-      if (lane < 16) {
-        if (separable) {
+    // L_ts = b_t 2^(G_t - G_s) Gram_ts (s < t).  Gram row t sits in lane 32 (t / 16) + t % 16; the
+    // 16x256b load spreads a warp's 16 rows over all its threads: rows ta and ta + 8, two columns
+    // of each group of eight.
+    const int ta = warp * 16 + (lane >> 2), tb = ta + 8, cq = 2 * (lane & 3);
+    float v[32];
+    tmem_ld16x256_x8(tmem + ((uint32_t)(warp * 32) << 16), v);
+    if (separable) {
+      const float ea = sBv[ta] * sE[ta], eb = sBv[tb] * sE[tb];
 #pragma unroll
-          for (int q = 0; q < 32; q += 4) {
-            const int sc = hb + q;
-            const float4 f4 = *reinterpret_cast<const float4 *>(sF + sc);
-            float4 o;
-            o.x = (sc + 0 < t) ? be * f4.x * v[q + 0] : 0.f;
-            o.y = (sc + 1 < t) ? be * f4.y * v[q + 1] : 0.f;
-            o.z = (sc + 2 < t) ? be * f4.z * v[q + 2] : 0.f;
-            o.w = (sc + 3 < t) ? be * f4.w * v[q + 3] : 0.f;
-            *reinterpret_cast<float4 *>(sL + t * LS + sc) = o;
-          }
-        } else {
+      for (int m = 0; m < 8; ++m) {
+        const int sc = 8 * m + cq;
+        const float2 f2 = *reinterpret_cast<const float2 *>(sF + sc);
+        *reinterpret_cast<float2 *>(sL + ta * LS + sc) =
+            make_float2(sc < ta ? ea * f2.x * v[4 * m] : 0.f, sc + 1 < ta ? ea * f2.y * v[4 * m + 1] : 0.f);
+        *reinterpret_cast<float2 *>(sL + tb * LS + sc) =
+            make_float2(sc < tb ? eb * f2.x * v[4 * m + 2] : 0.f, sc + 1 < tb ? eb * f2.y * v[4 * m + 3] : 0.f);
+      }
+    } else {
+      const float ba = sBv[ta], bb = sBv[tb], Ga = sG[ta], Gb = sG[tb];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int sc = hb + q;
-            sL[t * LS + sc] = (sc < t) ? bt * exp2f(Gt - sG[sc]) * v[q] : 0.f;
-          }
-        }
+      for (int m = 0; m < 8; ++m) {
+        const int sc = 8 * m + cq;
+        const float g0 = sG[sc], g1 = sG[sc + 1];
+        *reinterpret_cast<float2 *>(sL + ta * LS + sc) =
+            make_float2(sc < ta ? ba * exp2f(Ga - g0) * v[4 * m] : 0.f,
+                        sc + 1 < ta ? ba * exp2f(Ga - g1) * v[4 * m + 1] : 0.f);
+        *reinterpret_cast<float2 *>(sL + tb * LS + sc) =
+            make_float2(sc < tb ? bb * exp2f(Gb - g0) * v[4 * m + 2] : 0.f,
+                        sc + 1 < tb ? bb * exp2f(Gb - g1) * v[4 * m + 3] : 0.f);
       }
     }
   }

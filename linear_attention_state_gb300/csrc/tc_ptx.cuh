@@ -266,6 +266,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 lanes x 64 columns spread over the whole warp (the layout of an M = 64 accumulator, whose
+// rows fill 16 lanes of each warp's quarter): thread l gets lanes (base + l / 4) and
+// (base + 8 + l / 4) at columns 8 m + 2 (l % 4) and 8 m + 2 (l % 4) + 1, as
+// v[4 m] (first lane, first column), v[4 m + 1], v[4 m + 2] (second lane), v[4 m + 3], m = 0..7.
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : HYPIC_R4(0), HYPIC_R4(4), HYPIC_R4(8), HYPIC_R4(12), HYPIC_R4(16), HYPIC_R4(20), HYPIC_R4(24),
+        HYPIC_R4(28)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t r[64];
   asm volatile(

@@ -78,6 +78,20 @@ def test_slow_decay_keeps_T_large():
     assert eT <= TOL_BF16 and eS <= TOL_BF16
 
 
+def test_strong_decay_takes_per_entry_exponentials():
+    """Gates near 0.2 make a chunk's total decay exceed 2^-100, so the prep kernel forms every decay
+    factor of L as its own exponential instead of the separable product; T_C underflows to 0
+    (the tolerance floor covers it) and S must still match."""
+    lens = [64, 200, 1000, 37]
+    H = 2
+    tok, bounds, T, S = run_case("gated_delta", lens, H, key=41, gate_div=0.5)
+    a = tok["alpha"][bounds[2][0]:bounds[2][0] + 64]
+    assert float(torch.log2(a).sum(0).max()) < -100.0  # the chunk really is non-separable
+    eT, eS = check("gated_delta", tok, bounds, T, S, H)
+    print(f"strong decay: T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+
+
 def test_deltanet_four_segments_of_256():
     lens = [256, 256, 256, 256]
     H = 4

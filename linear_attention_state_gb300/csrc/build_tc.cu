@@ -363,34 +363,68 @@ __global__ void __launch_bounds__(NT, WO ? 4 : 6)
     return;
   }
 
-  // Diagonal 32 x 32 blocks of A by column-wise forward substitution (threads 0..63), written
-  // over the blocks of L they came from once every thread has read them.
-  float x[32];
-  const int base = (tid >> 5) * 32, cl = tid & 31;
-  if (tid < C) {
+  // Diagonal 16 x 16 blocks of A by column-wise forward substitution (threads 0..63, one column
+  // each), written over the blocks of L they came from once every thread has read them.
+  {
+    float x[16];
+    const int base = (tid >> 4) * 16, cl = tid & 15;
+    if (tid < C) {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) x[r] = (r == cl) ? 1.f : 0.f;
+      for (int r = 0; r < 16; ++r) x[r] = (r == cl) ? 1.f : 0.f;
 #pragma unroll
-    for (int r = 1; r < 32; ++r) {
-      const float *Lr = sL + (base + r) * LS + base;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      for (int r = 1; r < 16; ++r) {
+        const float *Lr = sL + (base + r) * LS + base;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int q = 0; q + 3 < r; q += 4) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(Lr + q);
-        a0 = fmaf(l4.x, x[q], a0);
-        a1 = fmaf(l4.y, x[q + 1], a1);
-        a2 = fmaf(l4.z, x[q + 2], a2);
-        a3 = fmaf(l4.w, x[q + 3], a3);
+        for (int q = 0; q + 3 < r; q += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(Lr + q);
+          a0 = fmaf(l4.x, x[q], a0);
+          a1 = fmaf(l4.y, x[q + 1], a1);
+          a2 = fmaf(l4.z, x[q + 2], a2);
+          a3 = fmaf(l4.w, x[q + 3], a3);
+        }
+#pragma unroll
+        for (int q = (r / 4) * 4; q < r; ++q) a0 = fmaf(Lr[q], x[q], a0);
+        if (r > cl) x[r] = -((a0 + a1) + (a2 + a3));
       }
+    }
+    __syncthreads();
+    if (tid < C) {
 #pragma unroll
-      for (int q = (r / 4) * 4; q < r; ++q) a0 = fmaf(Lr[q], x[q], a0);
-      if (r > cl) x[r] = -((a0 + a1) + (a2 + a3));
+      for (int r = 0; r < 16; ++r) sA[(base + r) * LS + base + cl] = x[r];
     }
   }
   __syncthreads();
-  if (tid < C) {
+  // Lower-left 16 x 16 quarter of each diagonal 32 x 32 block p (16-blocks a = 2p, b = 2p + 1):
+  // A_ba = -A_bb (L_ba A_aa).  Thread -> block p = tid / 64, row tid % 64 / 4, four columns; the
+  // product L_ba A_aa waits in the free upper-right region (rows 0..15, columns 32 + 16 p ..).
+  {
+    const int p = tid >> 6, r = (tid & 63) >> 2, c0 = 4 * (tid & 3);
+    const int o = 32 * p;  // the 32-block's first row and column
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) sA[(base + r) * LS + base + cl] = x[r];
+    for (int k = 0; k < 16; ++k) {
+      const float l = sL[(o + 16 + r) * LS + o + k];
+      const float4 a4 = *reinterpret_cast<const float4 *>(sA + (o + k) * LS + o + c0);
+      y.x = fmaf(l, a4.x, y.x);
+      y.y = fmaf(l, a4.y, y.y);
+      y.z = fmaf(l, a4.z, y.z);
+      y.w = fmaf(l, a4.w, y.w);
+    }
+    float *Y = sT + 16 * p;  // rows 0..15, columns 32 + 16 p + 0..15 of L's frame
+    *reinterpret_cast<float4 *>(Y + r * LS + c0) = y;
+    __syncthreads();
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float ab = sA[(o + 16 + r) * LS + o + 16 + k];
+      const float4 y4 = *reinterpret_cast<const float4 *>(Y + k * LS + c0);
+      z.x = fmaf(ab, y4.x, z.x);
+      z.y = fmaf(ab, y4.y, z.y);
+      z.z = fmaf(ab, y4.z, z.z);
+      z.w = fmaf(ab, y4.w, z.w);
+    }
+    *reinterpret_cast<float4 *>(sA + (o + 16 + r) * LS + o + c0) = make_float4(-z.x, -z.y, -z.z, -z.w);
   }
   __syncthreads();
   // T = L21 A11 and A21 = -A22 T (32 x 32 each): each thread owns a 2 x 4 output tile

@@ -38,7 +38,7 @@ FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and r
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 # dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
 # this workload, from the ncu capture summarised in profiles/build_tc_32h_d128_8x4096.md.
-BUILD_TC_TRAFFIC = 278_434_816 + 751_101_056 + 1_370_204_501 + 33_452_416
+BUILD_TC_TRAFFIC = 277_309_440 + 747_578_368 + 1_370_620_928 + 38_123_776
 # The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from the capture
 # summarised in profiles/build_decay_tc_32h_d128_64x512.md.
 DECAY_TC_TRAFFIC = {"scalar_const": 536_935_000 + 112_331_264, "diag": 1_073_959_000 + 122_754_304}

@@ -210,12 +210,13 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *sh, int32_t n_s
   const size_t row_b = (size_t)sh->H * sizeof(float);
   const int64_t tsz = hypic_t_size(sh);
   cudaStream_t st = (cudaStream_t)stream, cp = copy_stream ? (cudaStream_t)copy_stream : st;
-  // Groups of consecutive segments holding about an eighth of the body tokens each (at most
-  // kMaxGroups), so that the last group's build, which no copy hides, stays short.
+  // Groups of consecutive segments holding about an eighth of the body tokens each (at least 7/8
+  // of an eighth, so that equal bodies a seam shorter than the rest still form groups of one; at
+  // most kMaxGroups groups), so that the last group's build, which no copy hides, stays short.
   int64_t body_total = 0;
   for (int32_t i = 0; i < n_seg; ++i) body_total += seg_bounds_host[2 * i + 1] - seg_bounds_host[2 * i];
   constexpr int kMaxGroups = 16;
-  const int64_t target = body_total / 8 > 1 ? body_total / 8 : 1;
+  const int64_t target = body_total * 7 / 64 > 1 ? body_total * 7 / 64 : 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HYPIC_ECUDA;
   static std::mutex mu[kMaxDevices];

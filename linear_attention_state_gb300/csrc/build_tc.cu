@@ -449,8 +449,10 @@ __global__ void __launch_bounds__(NT, WO ? 4 : 6)
     *reinterpret_cast<float4 *>(sT + (r0 + 1) * LS + c0) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
     __syncthreads();
     float bcc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // A22 is lower triangular: rows r0, r0 + 1 of warp w (rows 8 w .. 8 w + 7) need k < 8 w + 8.
+    const int kmax = 8 * warp + 8;
 #pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < kmax; ++k) {
       const float a0 = sA[(32 + r0) * LS + 32 + k], a1 = sA[(33 + r0) * LS + 32 + k];
       const float4 b4 = *reinterpret_cast<const float4 *>(sT + k * LS + c0);
       bcc[0][0] = fmaf(a0, b4.x, bcc[0][0]);

@@ -17,14 +17,14 @@
 // Two kernels per block of heads:
 //   wy_prep_kernel  (one CTA per chunk and head, all chunks in parallel): the
 //     state-independent part.  TMA loads K; gates and their log-cumsum; Gram =
-//     K K^T on tcgen05 (M = 64); L; A = (I + L)^{-1} in fp32 by 2 x 2 blocked
-//     forward substitution; Wk^T = K^T (A diag(b gamma))^T on tcgen05 (K exact in
+//     K K^T on tcgen05 (M = 64); L; A = (I + L)^{-1} in fp32, blocked in two levels
+//     (16 x 16 diagonal blocks by forward substitution, then 32 x 32); Wk^T = K^T (A diag(b gamma))^T on tcgen05 (K exact in
 //     bf16, A diag(b gamma) split hi + lo).  Stored to the workspace as ready-made
 //     128-byte-swizzled operand tiles: Wk^T hi + lo, -A diag(b) hi + lo, and the
 //     per-token scales exp(G_C - G_t) and gamma_C.
-//   chain_tc_kernel (one CTA per segment and head, or with more of those than the GPU
-//     holds at once, one CTA per SM running an equal share of all chunk steps, cut
-//     segments rejoined by composing their two pairs): the state-dependent chain.  The
+//   chain_tc_kernel (one CTA per segment and head, or at most one CTA per SM running an
+//     equal share of all chunk steps, segments cut between CTAs rejoined by composing
+//     their pieces' pairs): the state-dependent chain.  The
 //     CTA keeps both 128 x 128 fp32 column halves of X (T and S, which evolve
 //     independently) in tensor memory for the whole segment, transposed.  Per chunk:
 //     TMA brings K, V and the chunk's record (double buffered); -U^T = V^T (-A diag(b))^T

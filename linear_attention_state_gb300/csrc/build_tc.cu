@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(NT, WO ? 4 : 6)
   if (ok_flag && tid == 0) {
     bulk_store(rec + WS_WH, sm + P_OFF_WT, 32768);
     bulk_store_commit();
-    bulk_store_wait_all();
+    bulk_store_wait_read();  // the shared source must outlive the copy; the CTA may then exit
   }
 }
 

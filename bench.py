@@ -143,6 +143,13 @@ class RequestStep:
         self.max_len = max(e - b for b, e in self.bounds_list)
         self.T = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
         self.S = torch.empty((w.n_seg, w.H, w.d, w.d), device=dev)
+        # Requests run as a serving loop would: request i's assembly (one CTA per head) runs on its
+        # own stream while request i + 1 builds, so the pairs alternate between two buffers and a
+        # build waits for the assembly that last read its buffer.
+        self.pairs = [(self.T, self.S), (torch.empty_like(self.T), torch.empty_like(self.S))]
+        self.asm_stream = torch.cuda.Stream(device=dev)
+        self.asm_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.turn = 0
         self.idx = torch.arange(w.n_seg, dtype=torch.int32, device=dev)[None]
         self.S_out = torch.empty((1, w.H, w.d, w.d), device=dev)
         self.o = torch.empty((1, w.n_seg - 1, w.w, w.H, w.d), device=dev)
@@ -159,17 +166,34 @@ class RequestStep:
         self.seam_head_tokens = (w.n_seg - 1) * w.w * w.H
 
     def step(self, ev=None):
+        import torch
         hy = self.hy
+        i = self.turn % 2
+        T, S = self.pairs[i]
+        cur = torch.cuda.current_stream()
+        if self.turn >= 2:
+            cur.wait_event(self.asm_done[i])
         if ev is not None:
             ev[0].record()
         hy.segment_build_batched(self.k, self.v, self.bounds, self.alpha, self.beta, family=self.w.family,
-                                 max_len=self.max_len, out=(self.T, self.S), ws=self.ws)
+                                 max_len=self.max_len, out=(T, S), ws=self.ws)
+        built = torch.cuda.Event()
+        built.record()
         if ev is not None:
             ev[1].record()
-        hy.assemble(self.T, self.S, self.idx, self.seam_k, self.seam_v, self.seam_a, self.seam_b,
-                    seam_q=self.seam_q, family=self.w.family, out=self.S_out, o_out=self.o)
-        if ev is not None:
-            ev[2].record()
+        self.asm_stream.wait_event(built)
+        with torch.cuda.stream(self.asm_stream):
+            hy.assemble(T, S, self.idx, self.seam_k, self.seam_v, self.seam_a, self.seam_b,
+                        seam_q=self.seam_q, family=self.w.family, out=self.S_out, o_out=self.o)
+            if ev is not None:
+                ev[2].record()
+            self.asm_done[i].record()
+        self.turn += 1
+
+    def join(self):
+        """Makes the current stream wait for the last assembly."""
+        import torch
+        torch.cuda.current_stream().wait_stream(self.asm_stream)
 
     def host_copies(self):
         """Pinned host copies of the step's inputs (for the end-to-end measurement)."""
@@ -177,7 +201,7 @@ class RequestStep:
         return {n: getattr(self, n).cpu().pin_memory() for n in names}
 
 
-def run_timed(fn, steps, warmup, sync_all, kernel_events=True):
+def run_timed(fn, steps, warmup, sync_all, kernel_events=True, finish=None):
     """Times `steps` calls of fn after `warmup` untimed ones, with CUDA events on the current stream.
 
     With kernel_events, fn records three events per step (before, between and after
@@ -186,12 +210,16 @@ def run_timed(fn, steps, warmup, sync_all, kernel_events=True):
     import torch
     for _ in range(warmup):
         fn(None)
+    if finish is not None:
+        finish()
     sync_all()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     start.record()
     for i in range(steps):
         fn(evs[i] if kernel_events else None)
+    if finish is not None:
+        finish()
     end.record()
     sync_all()
     total_ms = start.elapsed_time(end)
@@ -548,7 +576,7 @@ def main():
     req = RequestStep(w, dev)
     status0 = hy.stream_status()
     clocks = ClockSampler(local)
-    total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all)
+    total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all, finish=req.join)
     clk = clocks.stop()
     status = hy.stream_status()
     t = torch.tensor([total_ms], device=dev)
@@ -646,7 +674,9 @@ def main():
             "config": {"workload": w.name, "layers": w.layers, "heads": w.heads, "d": w.d, "segments": w.n_seg,
                        "segment_tokens": w.seg_len, "seam_w": w.w, "inputs": "bf16 q/k/v, fp32 gates and state",
                        "l2": "inputs larger than L2 (k+v 537 MB per step), no flush",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       "pipelining": "request i's assembly runs on a second stream while request i+1 builds "
+                                     "(pairs double-buffered); every step builds and assembles a whole request"},
             "build": {"body_head_tokens_per_s": req.body_head_tokens / avg_build_s, "ms": avg_build_s * 1e3},
             "assemble": {"compositions_per_s": req.compositions / avg_asm_s,
                          "seam_head_tokens_per_s": req.seam_head_tokens / avg_asm_s, "ms": avg_asm_s * 1e3},

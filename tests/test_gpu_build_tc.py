@@ -256,3 +256,62 @@ def test_build_from_host_inputs_matches_device_inputs():
         for h in range(H):
             Tr, Sr = ref_pair("gated_delta", hk, h, *bounds[s])
             assert relerr(np64(T2[s, h]), Tr) <= TOL_BF16 and relerr(np64(S2[s, h]), Sr) <= TOL_BF16
+
+
+@pytest.mark.parametrize("n_seg,H,seg_len", [(50, 4, 130), (2, 2, 2000)])
+def test_bad_bounds_in_the_split_chain_are_reported_without_waiting(n_seg, H, seg_len):
+    """One body running past the token axis, in a build whose chain cuts units between CTAs (more
+    units than SMs: cut once; fewer: cut several times).  The CTAs holding that unit stop at once
+    and raise their publish flags with a failure mark, so no neighbour's bounded wait has to run
+    out: the call reports HYPIC_EDEVICE quickly, and the next, valid build is clean and correct."""
+    import time
+    n = n_seg * seg_len
+    g = W.generator(DEV, 6400, n_seg)
+    tok = W.draw_tokens(g, n, H, 128, "gated_delta", "bf16", DEV, need_q=False)
+    good = [(i * seg_len, (i + 1) * seg_len) for i in range(n_seg)]
+    bad = list(good)
+    bad[n_seg // 2] = (bad[n_seg // 2][0], n + 64)  # past the token axis
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bad, device=DEV), tok["alpha"], tok["beta"],
+                             family="gated_delta", max_len=seg_len + 64)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert hy.stream_status() == hy._lib.HYPIC_EDEVICE
+    assert dt < 0.5, f"a bounded wait seems to have run out ({dt:.2f} s)"
+    T, S = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(good, device=DEV), tok["alpha"],
+                                    tok["beta"], family="gated_delta")
+    assert hy.stream_status() == 0
+    host = host_tokens(tok, list(range(H)))
+    for s_ in (0, n_seg // 2, n_seg - 1):
+        Tr, Sr = ref_pair("gated_delta", host, H - 1, *good[s_])
+        assert relerr(np64(S[s_, H - 1]), Sr) <= TOL_BF16
+        assert relerr(np64(T[s_, H - 1]), Tr) <= TOL_BF16
+
+
+def test_host_input_builds_in_a_serving_loop_with_ready_events():
+    """Four different requests through hypic_segment_build_batched_host, alternating between two sets
+    of device buffers: each request's copies wait only for the event recorded after the build that
+    last read its set, so they overlap the previous request's build.  Every request's pairs equal
+    those of the device-input build of the same tokens bit for bit."""
+    lens = [300, 64, 1000, 5, 700]
+    H = 4
+    reqs = [run_case("gated_delta", lens, H, key=50 + r) for r in range(4)]
+    n_tok = reqs[0][0]["k"].shape[0]
+    sets = [tuple(torch.empty_like(reqs[0][0][n]) for n in ("k", "v", "alpha", "beta")) +
+            (torch.empty(len(lens), 2, dtype=torch.int64, device=DEV),) for _ in range(2)]
+    free = [torch.cuda.Event(), torch.cuda.Event()]
+    copy_stream = torch.cuda.Stream()
+    out = []
+    for r, (tok, bounds, _, _) in enumerate(reqs):
+        host = {n: tok[n].cpu().pin_memory() for n in ("k", "v", "alpha", "beta")}
+        assert tok["k"].shape[0] == n_tok
+        T, S = hy.segment_build_batched_host(host["k"], host["v"], torch.tensor(bounds, dtype=torch.int64),
+                                             host["alpha"], host["beta"], family="gated_delta", dev=sets[r % 2],
+                                             copy_stream=copy_stream, ready_event=free[r % 2] if r >= 2 else None)
+        free[r % 2].record()
+        out.append((T, S, host))  # keep the pinned inputs alive until the copies have run
+    torch.cuda.synchronize()
+    assert hy.stream_status() == 0
+    for (tok, bounds, T0, S0), (T, S, _) in zip(reqs, out):
+        assert torch.equal(T, T0) and torch.equal(S, S0)

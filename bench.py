@@ -28,7 +28,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "segment tokens/s (build) and compositions/s, % tensor/HBM roofline, 1 GB300"
 
-# Algorithmic work per unit ("Measurement").
+# Algorithmic work per unit: the FLOP and bytes a direct implementation of each step needs.
 D = 128
 FLOP_PER_CHUNK_WY = 3 * 2 * 64 * 64 * D + 2 * 2 * 64 * D * (2 * D)  # G, U, W; W.X and K^T.R per 64-token chunk
 FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
@@ -37,13 +37,13 @@ FLOP_PER_HEAD_TOKEN_WY_O = (FLOP_PER_CHUNK_WY + 2 * 64 * D * D + 4 * 64 * 64 * D
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 # dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
-# this workload, from the ncu capture summarised in profiles/build_tc_32h_d128_8x4096.md.
+# this workload, from an ncu capture of the bench's own build launches.
 BUILD_TC_TRAFFIC = 277_309_440 + 747_578_368 + 1_370_620_928 + 38_123_776
-# The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from the capture
-# summarised in profiles/build_decay_tc_32h_d128_64x512.md.
+# The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from an ncu
+# capture of those launches.
 DECAY_TC_TRAFFIC = {"scalar_const": 536_935_000 + 112_331_264, "diag": 1_073_959_000 + 122_754_304}
 # The same for compose_tc_kernel on the full warm-cache workload (generator-drawn pool of 256 x 960
-# pairs, 64 requests x 16), from the one-pass capture in profiles/compose_tc_pool16_B64x8.md: the
+# pairs, 64 requests x 16), from a one-pass ncu capture of that launch: the
 # pool is re-read from L2, so DRAM traffic is far below the 128 KiB (fp32) / 64 KiB (bf16)
 # algorithmic bytes per composition.
 COMPOSE_TC_TRAFFIC = {"f32": 42_967_890_944 + 4_018_890_752, "bf16": 16_075_031_808 + 4_012_372_736}
@@ -481,14 +481,18 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
                              "bytes_per_composition": bytes_per_comp, "peak_source": peaks["source"]},
                 "status": hy.stream_status()}
 
+    # Algorithmic bytes per composition: the pair read (T_C and S_{C|0}) plus the request's final
+    # state, written once per chain of n compositions.
+    out_per_comp = D * D * 4 / pw.n
     res = None
     if storage in ("f32", "both"):
-        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION, pw.name, COMPOSE_TC_TRAFFIC["f32"])
+        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION + out_per_comp, pw.name, COMPOSE_TC_TRAFFIC["f32"])
     if storage in ("bf16", "both"):
         T_lp, S_lp = hy.pairs_to_bf16(pool_T, pool_S, family="gated_delta")
         del pool_T, pool_S
         torch.cuda.empty_cache()
-        lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2, pw.name + "_bf16pairs", COMPOSE_TC_TRAFFIC["bf16"])
+        lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2 + out_per_comp, pw.name + "_bf16pairs",
+                   COMPOSE_TC_TRAFFIC["bf16"])
         del T_lp, S_lp
         if res is None:
             res = lp

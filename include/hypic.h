@@ -319,7 +319,8 @@ typedef enum { HYPIC_ACT_IDENTITY = 0, HYPIC_ACT_SILU = 1 } hypic_activation;
  * i + rot_dim/2 (i < rot_dim/2) form a pair turned by delta * base^(-2i/rot_dim); dims >=
  * rot_dim pass through.  2 <= rot_dim <= d <= 512, rot_dim even, base > 1.  The angle is
  * reduced modulo 2 pi in double precision, the rotation applied in fp32 (bf16 outputs are
- * rounded to nearest even).  Errors: HYPIC_EINVAL (pointers, sizes), HYPIC_ECUDA.
+ * rounded to nearest even).  Errors: HYPIC_EINVAL (pointers, sizes), HYPIC_ECUDA; a staged copy
+ * that never lands (bounded wait) is recorded as HYPIC_ETIMEOUT for hypic_stream_status.
  */
 hypic_status hypic_rope_shift(int64_t n_rows, int32_t d, int32_t rot_dim, double base, int64_t delta,
                               hypic_dtype dtype, const void *K_in, void *K_out, hypic_stream_t stream);
@@ -329,7 +330,7 @@ hypic_status hypic_rope_shift(int64_t n_rows, int32_t d, int32_t rot_dim, double
  * index of S [n, H, d_k, d_v] fp32, in place; T_C is unchanged.  Exact only when the transition
  * commutes with the rotation, so only the scalar families are accepted (HYPIC_FAM_SCALAR_CONST,
  * HYPIC_FAM_SCALAR); others return HYPIC_EUNSUPPORTED.  Rotation as in hypic_rope_shift, with
- * rot_dim <= d_k.
+ * rot_dim <= d_k; errors as there.
  */
 hypic_status hypic_state_rerotate(const hypic_shape *shape, int64_t n, float *S_inout, int32_t rot_dim,
                                   double base, int64_t delta, hypic_stream_t stream);

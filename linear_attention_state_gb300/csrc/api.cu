@@ -448,7 +448,9 @@ hypic_status hypic_rope_shift(int64_t n_rows, int32_t d, int32_t rot_dim, double
   if (n_rows < 0 || !ok_rope(d, rot_dim, base) || !ok_dtype(dtype)) return HYPIC_EINVAL;
   if (n_rows == 0) return HYPIC_OK;
   if (!ok_ptr(K_in) || !ok_ptr(K_out)) return HYPIC_EINVAL;
-  return from_cuda(launch_rope_shift(K_in, K_out, n_rows, d, rot_dim, base, (long long)delta, dtype,
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  return from_cuda(launch_rope_shift(K_in, K_out, n_rows, d, rot_dim, base, (long long)delta, dtype, err,
                                      (cudaStream_t)stream));
 }
 
@@ -460,7 +462,9 @@ hypic_status hypic_state_rerotate(const hypic_shape *sh, int64_t n, float *S_ino
   if (n < 0 || !ok_rope(sh->d_k, rot_dim, base)) return HYPIC_EINVAL;
   if (n == 0 || sh->H == 0) return HYPIC_OK;
   if (!ok_ptr(S_inout)) return HYPIC_EINVAL;
-  return from_cuda(launch_state_rerotate(S_inout, n * sh->H, sh->d_k, sh->d_v, rot_dim, base, (long long)delta,
+  int *err = nullptr;
+  if (status_word(&err) != cudaSuccess) return HYPIC_ECUDA;
+  return from_cuda(launch_state_rerotate(S_inout, n * sh->H, sh->d_k, sh->d_v, rot_dim, base, (long long)delta, err,
                                          (cudaStream_t)stream));
 }
 

@@ -95,9 +95,9 @@ cudaError_t launch_pairs_to_bf16(const float *T, const float *S, void *T_lp, voi
 
 // Boundary patches (boundary.cu).
 cudaError_t launch_rope_shift(const void *in, void *out, int64_t rows, int d, int r, double base, long long delta,
-                              int dtype, cudaStream_t st);
+                              int dtype, int *err, cudaStream_t st);
 cudaError_t launch_state_rerotate(float *S, int64_t mats, int dk, int dv, int r, double base, long long delta,
-                                  cudaStream_t st);
+                                  int *err, cudaStream_t st);
 cudaError_t launch_conv_tail(const void *x, int64_t n_tokens, int C, int k, int n_seg, const int64_t *bounds,
                              void *tail, int dtype, int *err, cudaStream_t st);
 cudaError_t launch_conv_seam(const void *xs, const void *tail, const float *W, const float *bias, int B, int w, int C,

@@ -50,6 +50,35 @@ def test_rope_shift(dtype, d, rot, base, delta):
     assert torch.equal(K2, out)
 
 
+@pytest.mark.parametrize("dtype,rot", [(torch.float32, 96), (torch.bfloat16, 96), (torch.bfloat16, 100)])
+def test_rope_shift_many_rows(dtype, rot):
+    """Enough rows for several grid-stride passes of every CTA, with a ragged last pass (and, at
+    rot = 100 in bf16, rows that are not whole 16-byte groups): sampled rows against the oracle,
+    the pass-through dims bit for bit."""
+    d, delta, base = 128, 70_001, 1e6
+    K = randn((10007, 4, d), key=77 + rot, dtype=dtype)
+    out = hy.rope_shift(K, delta, rot_dim=rot, base=base)
+    assert hy.stream_status() == 0
+    fin, fout = K.reshape(-1, d), out.reshape(-1, d)
+    n = fin.shape[0]
+    rows = sorted({0, 1, n - 2, n - 1, *np.random.default_rng(5).integers(0, n, 200).tolist()})
+    ref = B.rope_shift(np64(fin[rows]), delta, rot, base)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert relerr(np64(fout[rows]), ref) <= tol
+    assert torch.equal(out[..., rot:], K[..., rot:])
+
+
+def test_state_rerotate_many_matrices():
+    """In place over 40 x 32 matrices (several grid-stride passes): sampled matrices against the
+    oracle."""
+    S = randn((40, 32, 128, 128), key=91)
+    S0 = S.clone()
+    hy.state_rerotate(S, 70_001, rot_dim=128, base=1e6, family="scalar")
+    assert hy.stream_status() == 0
+    for n, h in [(0, 0), (17, 5), (39, 31), (39, 30)]:
+        assert relerr(np64(S[n, h]), B.state_rerotate(np64(S0[n, h]), 70_001, 128, 1e6)) <= TOL_F32
+
+
 def test_rope_shift_makes_cached_keys_global():
     """Keys rotated at segment-local positions, shifted by the segment start, equal keys rotated
     at their global positions (computed by the oracle)."""

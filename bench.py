@@ -35,6 +35,7 @@ FLOP_PER_HEAD_TOKEN_WY = FLOP_PER_CHUNK_WY // 64                    # 180,224
 # with per-token outputs: + Q S_p (2 C d^2), Q K^T and M Wm (2 C^2 d each) per chunk
 FLOP_PER_HEAD_TOKEN_WY_O = (FLOP_PER_CHUNK_WY + 2 * 64 * D * D + 4 * 64 * 64 * D) // 64  # 245,760
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
+FLOP_PER_HEAD_TOKEN_KDA_RECURRENT = FLOP_PER_HEAD_TOKEN_RECURRENT + D * (2 * D)  # + the channel gate
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 # dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
 # this workload, from an ncu capture of the bench's own build launches.
@@ -283,7 +284,7 @@ def decay_build_measure(steps, warmup, dev, peaks):
     import linear_attention_state_gb300 as hy
     import workloads as W
     out = {}
-    for fam, w in W.DECAY_FAMILIES.items():
+    for fam, w in list(W.DECAY_FAMILIES.items()) + [("kda", W.KDA_BUILD)]:
         tok = w.draw_request(dev, need_q=False)
         bounds = torch.tensor(w.body_bounds(), device=dev)
         ws_bytes = hy.build_workspace_bytes(w.H, w.d, w.n_seg, w.seg_len, family=fam, in_dtype=w.in_dtype)
@@ -313,6 +314,14 @@ def decay_build_measure(steps, warmup, dev, peaks):
             fl = FLOP_PER_HEAD_TOKEN_WY * ht
             entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"]}
+        elif fam == "kda":
+            # token-by-token fp32 kernel (no chunked KDA build): fp32 FMA roofline
+            fl = FLOP_PER_HEAD_TOKEN_KDA_RECURRENT * ht
+            alu = fp32_simt_peak_tflops(peaks["sm_max_mhz"])
+            entry["roofline"] = {"bound": "alu", "achieved": fl / tb / 1e12, "peak": alu, "unit": "TFLOP/s",
+                                 "frac": fl / tb / 1e12 / alu, "kernel": "recurrent_kernel (fp32 SIMT)",
+                                 "flop_per_unit": FLOP_PER_HEAD_TOKEN_KDA_RECURRENT,
+                                 "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock"}
         else:
             per = 2 * w.d * 2 + {"scalar_const": 0, "scalar": 4, "diag": 4 * w.d}[fam]
             by = per * ht + w.n_seg * w.H * w.d * w.d * 4

@@ -173,6 +173,8 @@ DECAY_FAMILIES = {
     "diag": Workload("decay_diag_32h_d128_64x512", 3, 1, 32, 128, "bf16", "diag", 64, 512, 0, gate_div=16.0),
     "gated_delta": Workload("decay_gdn_32h_d128_64x512", 3, 1, 32, 128, "bf16", "gated_delta", 64, 512, 0),
 }
+# KDA (per-channel gate before the erase) on the decay-family shape, channel gates as the diagonal family's.
+KDA_BUILD = Workload("decay_kda_32h_d128_64x512", 3, 1, 32, 128, "bf16", "kda", 64, 512, 0, gate_div=16.0)
 LONG_MIXED = Workload("long_30x32_d128_128x1024", 4, 30, 32, 128, "bf16", "gated_delta", 128, 1024, 8,
                       extra={"n_cold": 32})
 

@@ -66,6 +66,11 @@ def test_rope_shift_many_rows(dtype, rot):
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
     assert relerr(np64(fout[rows]), ref) <= tol
     assert torch.equal(out[..., rot:], K[..., rot:])
+    # in place over the same rows: every block is read before any of its rows is written
+    K2 = K.clone()
+    hy.rope_shift(K2, delta, rot_dim=rot, base=base, out=K2)
+    assert hy.stream_status() == 0
+    assert torch.equal(K2, out)
 
 
 def test_state_rerotate_many_matrices():

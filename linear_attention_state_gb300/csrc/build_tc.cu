@@ -38,6 +38,7 @@
 // a ragged last chunk get b = 0 and a = 1, which makes them exact identity steps.
 #include <cuda_bf16.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "tc_ptx.cuh"
@@ -1424,6 +1425,33 @@ size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o) 
 
 // Runs the build over head blocks that fit the workspace: prep then chain for each block (and,
 // with per-token outputs, the S chain that emits them).
+// The outputs build runs its two chains (T half; S half with outputs) side by side: both read the
+// same records and write disjoint outputs, so the T-half chain goes to a side stream forked after
+// the prep kernel and joined back before the next head block's prep.  One side stream and two
+// events per device, created on first use; the enqueue holds a per-device lock so that calls from
+// several host threads do not interleave their fork and join.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+bool side_stream(int dev, SideStream **out, std::mutex **mu_out) {
+  static std::mutex mu[kMaxSideDevices];
+  static SideStream side[kMaxSideDevices];
+  static bool ready[kMaxSideDevices];
+  if (dev < 0 || dev >= kMaxSideDevices) return false;
+  std::lock_guard<std::mutex> g(mu[dev]);
+  if (!ready[dev]) {
+    if (cudaStreamCreateWithFlags(&side[dev].s, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&side[dev].fork, cudaEventDisableTiming) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&side[dev].join, cudaEventDisableTiming) != cudaSuccess) return false;
+    ready[dev] = true;
+  }
+  *out = &side[dev];
+  *mu_out = &mu[dev];
+  return true;
+}
+
 cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, cudaStream_t st) {
   const bool wo = r.o_out != nullptr;
   const size_t per = bytes_per_head(r.n_seg, r.seg.max_len, wo);
@@ -1472,6 +1500,14 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     e = cudaFuncSetAttribute(chain_so_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SO_SMEM);
     if (e != cudaSuccess) return e;
   }
+  SideStream *side = nullptr;
+  std::mutex *side_mu = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  if (wo) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !side_stream(dev, &side, &side_mu)) return cudaErrorInvalidResourceHandle;
+    side_lock = std::unique_lock<std::mutex>(*side_mu);
+  }
   // The split chain schedule needs its pair slots after the records and a cooperative launch.
   const size_t rec_end = (size_t)Hb * per;  // a multiple of 256 bytes
   const bool split_room =
@@ -1516,8 +1552,14 @@ cudaError_t launch_build_tc(const RecurrentArgs &r, void *ws, size_t ws_bytes, c
     if (wo) wy_prep_kernel<true><<<(unsigned)g1, NT, P_SMEM_O, st>>>(mk, mq, a);
     else wy_prep_kernel<false><<<(unsigned)g1, NT, P_SMEM, st>>>(mk, mq, a);
     if (wo) {
-      chain_tc_kernel<true><<<(unsigned)g2, NT2, SMEM_BYTES, st>>>(mk, mv, a);
+      if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(side->s, side->fork, 0)) != cudaSuccess) return e;
+      chain_tc_kernel<true><<<(unsigned)g2, NT2, SMEM_BYTES, side->s>>>(mk, mv, a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = cudaEventRecord(side->join, side->s)) != cudaSuccess) return e;
       chain_so_kernel<<<(unsigned)g2, SO_NT, SO_SMEM, st>>>(mk, mv, mq, a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess) return e;
     } else if (a.flags) {
       // CTAs wait on their neighbours: all must be resident together
       cudaLaunchConfig_t cfg = {};

@@ -18,7 +18,11 @@
  *   contiguous, 16-byte aligned, in the layout stated.  The library never
  *   allocates, frees or keeps a pointer after the call returns.
  * Execution: every call only enqueues work on `stream` (NULL = the legacy
- *   default stream) and returns; results are ready when the stream is.
+ *   default stream) and returns; results are ready when the stream is.  A call
+ *   may fork part of its work to a library-owned stream and join it back to
+ *   `stream` with events before returning (the build with per-token outputs
+ *   does); the ordering seen from `stream`, including under stream capture, is
+ *   unchanged.
  * Shapes: d_k == d_v in {16, 32, 64, 128}; H >= 0; counts >= 0.  An empty
  *   batch (H, B or n_seg == 0) is a no-op that returns HYPIC_OK.
  * Errors: arguments are checked on the host before anything is enqueued and

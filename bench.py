@@ -53,6 +53,9 @@ COMPOSE_TC_TRAFFIC = {"f32": 42_967_890_944 + 4_018_890_752, "bf16": 16_075_031_
 # writes counted during the launch are what L2 evicted before it ended (the rest follows later).
 BOUNDARY_TRAFFIC = {"rope_shift_32768x8x128_bf16": 67_140_864 + 15_822_080,
                     "state_rerotate_64x32_128x128_fp32": 134_249_472 + 72_236_032}
+# The same for the affine scan launch (compose_tc_kernel in scan mode) on the 64-pair, 960-head
+# workload, first launch of a one-pass ncu capture.
+SCAN_TRAFFIC = 8_456_816_128 + 8_021_051_904
 
 
 def load_peaks():
@@ -358,7 +361,8 @@ def scan_measure(steps, warmup, dev, peaks):
     by = n * H * (2 * d * d * 4) * 2  # read T and S, write both prefixes
     res = {"workload": f"scan_{n}x{H}heads_d{d}_fp32", "prefix_pairs_per_s": n * H / t, "ms": t * 1e3,
            "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": by / t / 1e9 / peaks["hbm_gbs"]}, "status": hy.stream_status()}
+                        "frac": by / t / 1e9 / peaks["hbm_gbs"], "traffic": SCAN_TRAFFIC},
+           "status": hy.stream_status()}
     del T, S
     torch.cuda.empty_cache()
     return res

@@ -53,6 +53,9 @@ COMPOSE_TC_TRAFFIC = {"f32": 42_967_890_944 + 4_018_890_752, "bf16": 16_075_031_
 # writes counted during the launch are what L2 evicted before it ended (the rest follows later).
 BOUNDARY_TRAFFIC = {"rope_shift_32768x8x128_bf16": 67_140_864 + 15_822_080,
                     "state_rerotate_64x32_128x128_fp32": 134_249_472 + 72_236_032}
+# The same for the build with per-token outputs (wy_prep_kernel<1>, the T-half chain_tc_kernel and
+# chain_so_kernel) on the 32k-token request, from a one-pass ncu capture of those launches.
+OUTPUTS_TC_TRAFFIC = 546_274_560 + 1_021_575_424 + 1_348_596_736 + 10_456_832 + 1_889_561_600 + 523_534_080
 # The same for the affine scan launch (compose_tc_kernel in scan mode) on the 64-pair, 960-head
 # workload, first launch of a one-pass ncu capture.
 SCAN_TRAFFIC = 8_456_816_128 + 8_021_051_904
@@ -401,7 +404,7 @@ def build_outputs_measure(steps, warmup, dev, peaks):
     res = {"workload": w.name + "_with_outputs", "build_ms": tb * 1e3, "body_head_tokens_per_s": ht / tb,
            "roofline": {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": fl / tb / 1e12 / peaks["bf16_tflops"], "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY_O,
-                        "traffic": None},
+                        "traffic": OUTPUTS_TC_TRAFFIC if os.environ.get("HYPIC_BUILD_PATH") != "recurrent" else None},
            "status": hy.stream_status()}
     del tok, ws, T, S, o
     torch.cuda.empty_cache()

@@ -149,6 +149,7 @@ class RequestStep:
         self.seam_v = tok["v"][pos].reshape(*shp, w.d).contiguous()
         self.seam_a = tok["alpha"][pos].reshape(shp).contiguous()
         self.seam_b = tok["beta"][pos].reshape(shp).contiguous()
+        self.q_full = tok["q"]  # kept for the parity check of the bench line
         del tok
         self.bounds_list = w.body_bounds()
         self.bounds = torch.tensor(self.bounds_list, dtype=torch.int64, device=dev)
@@ -242,20 +243,24 @@ def run_timed(fn, steps, warmup, sync_all, kernel_events=True, finish=None):
     return total_ms, k1, k2
 
 
-def cpu_baseline(w, n_heads, threads):
-    """The oracle, as it stands, on a sample of heads of the same request: pairs, seams, compose."""
+def cpu_baseline(w, n_heads, threads, tok=None):
+    """The oracle, as it stands, on a sample of heads of the same request: pairs, seams, compose.
+
+    tok: the request's inputs on the host (the device request copied back), so that the results
+    can be checked against the buffers the timed loop wrote; drawn on the host if None.  Returns
+    (tokens/s, seconds, {head: (T_C per segment, S per segment, seam outputs, composed S)})."""
     import numpy as np
 
     import oracle
-    tok = w.draw_request("cpu")
+    if tok is None:
+        tok = w.draw_request("cpu")
     heads = list(range(n_heads))
     bounds = w.body_bounds()
-    seam_pos = w.seam_positions()
 
     def one_head(h):
         f = lambda t: t[:, h].double().numpy()  # noqa: E731
         k, v, q, a, b = f(tok["k"]), f(tok["v"]), f(tok["q"]), f(tok["alpha"]), f(tok["beta"])
-        Ts, Ss = [], []
+        Ts, Ss, os_ = [], [], []
         for (b0, e0) in bounds:
             T, S = oracle.segment_pair(w.family, k[b0:e0], v[b0:e0], a[b0:e0], b[b0:e0])
             Ts.append(T.reshape(-1))
@@ -264,17 +269,41 @@ def cpu_baseline(w, n_heads, threads):
         for j in range(w.n_seg):
             if j >= 1 and w.w > 0:
                 s0 = j * w.seg_len
-                S, _ = oracle.run(w.family, k[s0:s0 + w.w], v[s0:s0 + w.w], a[s0:s0 + w.w], b[s0:s0 + w.w],
+                S, o = oracle.run(w.family, k[s0:s0 + w.w], v[s0:s0 + w.w], a[s0:s0 + w.w], b[s0:s0 + w.w],
                                   q=q[s0:s0 + w.w], S0=S)
+                os_.append(o)
             S = oracle.compose(w.family, Ts[j][None], Ss[j][None], S_init=S)
-        return S
+        return Ts, Ss, os_, S
 
     t0 = time.perf_counter()
-    oracle.parallel_map(one_head, heads, threads=threads)
+    res = oracle.parallel_map(one_head, heads, threads=threads)
     dt = time.perf_counter() - t0
-    del seam_pos
     tokens_equiv = w.n_seg * w.seg_len * w.layers * n_heads / w.H
-    return tokens_equiv / dt, dt
+    return tokens_equiv / dt, dt, dict(zip(heads, res))
+
+
+def request_parity(req, w, ref, tol):
+    """The timed loop's last request against the oracle on the sampled heads: relative Frobenius
+    error max(||gpu - ref|| / max(||ref||, 1e-30)) over heads and segments, for T_C, S_{C|0}, the
+    seam outputs and the composed state."""
+    import numpy as np
+
+    def rel(x, r):
+        return float(np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30))
+
+    T = req.T.double().cpu().numpy()
+    S = req.S.double().cpu().numpy()
+    So = req.S_out.double().cpu().numpy()
+    o = req.o.double().cpu().numpy()
+    err = {"T_C": 0.0, "S": 0.0, "seam_o": 0.0, "composed_S": 0.0}
+    for h, (Ts, Ss, os_, Sf) in ref.items():
+        for j in range(w.n_seg):
+            err["T_C"] = max(err["T_C"], rel(T[j, h].reshape(-1), Ts[j]))
+            err["S"] = max(err["S"], rel(S[j, h], Ss[j]))
+        for j, oj in enumerate(os_):
+            err["seam_o"] = max(err["seam_o"], rel(o[0, j, :, h], oj))
+        err["composed_S"] = max(err["composed_S"], rel(So[0, h], Sf))
+    return {"heads": len(ref), "max_rel_err": err, "tol": tol, "ok": all(e <= tol for e in err.values())}
 
 
 def decay_build_measure(steps, warmup, dev, peaks):
@@ -682,11 +711,17 @@ def main():
         compose = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
                                        args.compose_random, args.compose_storage)
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu:
         threads = os.cpu_count() or 1
         n_heads = min(w.H, max(1, threads))
-        v_cpu, dt = cpu_baseline(w, n_heads, threads)
+        torch.cuda.synchronize()
+        # the device request's own inputs, so the oracle also checks what the timed loop computed
+        host_tok = {"k": req.k[:, :n_heads].cpu(), "v": req.v[:, :n_heads].cpu(),
+                    "alpha": req.alpha[:, :n_heads].cpu(), "beta": req.beta[:, :n_heads].cpu(),
+                    "q": req.q_full[:, :n_heads].cpu()}
+        v_cpu, dt, ref = cpu_baseline(w, n_heads, threads, tok=host_tok)
+        parity = request_parity(req, w, ref, 2e-3 if w.in_dtype == "bf16" else 1e-5)
         cpu = {"value": v_cpu, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n_heads} of {w.H} heads of the same request, all 8 segments (pairs, seams, compose), "
                          f"float64, {dt:.1f} s wall"}
@@ -713,6 +748,7 @@ def main():
             "boundary_patches": bnd,
             "build_with_outputs": outs,
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": req.launches_per_step * args.steps,
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],

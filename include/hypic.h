@@ -205,13 +205,15 @@ size_t hypic_build_workspace_bytes_outputs(const hypic_shape *shape, int32_t n_s
  * It allocates nothing: where the build needs a workspace it uses a fixed
  * scratch array of HYPIC_NOALLOC_SCRATCH_BYTES that lives in the library, so
  * every GPU that loads the library holds that memory until the process exits.
- * Limit: one head's operand records must fit the scratch, i.e.
- * n_seg * ceil(max_len / 64) * 49,664 <= HYPIC_NOALLOC_SCRATCH_BYTES
- * (n_seg * ceil(max_len / 64) <= 1351); larger requests return HYPIC_ENOSPACE
- * before anything is enqueued.  More heads are processed in blocks that fit.
- * The first call on a device looks up the scratch array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture.  All calls on a device share the one scratch array:
+ * Limit: one head's operand records must fit the scratch.  Without outputs
+ * (o_out NULL) a record is 49,664 bytes per (64-token chunk, head):
+ * n_seg * ceil(max_len / 64) <= 1351.  With per-token outputs (q and o_out
+ * given) it is 66,560 bytes: n_seg * ceil(max_len / 64) <= 1008.  Larger
+ * requests return HYPIC_ENOSPACE before anything is enqueued.  More heads are
+ * processed in blocks that fit.  The first call on a device looks up the
+ * scratch array's device address (with that device current; a lookup that
+ * fails is tried again on the next call); make that first call before any
+ * stream capture.  All calls on a device share the one scratch array:
  * calls that overlap on the GPU (other streams, other host threads) race and
  * corrupt each other's results, so serialise them.  Nothing in the scratch has
  * to start at zero; every call writes each record before reading it.

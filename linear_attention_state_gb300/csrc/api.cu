@@ -13,21 +13,22 @@ __device__ int g_status_word;  // first device-side error since the last hypic_s
 
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices];
-std::once_flag g_status_once[kMaxDevices];
-cudaError_t g_status_err[kMaxDevices];
+std::mutex g_status_mu[kMaxDevices];
 
-// Device address of the status word on the current device (looked up once per device).
+// Device address of the status word on the current device.  Looked up with the device current;
+// only a successful lookup is kept, so a transient failure is retried on the next call.
 cudaError_t status_word(int **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_status_once[dev], [dev]() {
+  std::lock_guard<std::mutex> lock(g_status_mu[dev]);
+  if (!g_status_ptr[dev]) {
     void *p = nullptr;
-    g_status_err[dev] = cudaGetSymbolAddress(&p, g_status_word);
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
     g_status_ptr[dev] = static_cast<int *>(p);
-  });
-  if (g_status_err[dev] != cudaSuccess) return g_status_err[dev];
+  }
   *out = g_status_ptr[dev];
   return cudaSuccess;
 }

@@ -16,29 +16,30 @@ namespace hypic {
 namespace {
 
 constexpr size_t kScratchBytes = HYPIC_NOALLOC_SCRATCH_BYTES;  // per device
-constexpr size_t kRecordBytes = 49664;  // operand record of one (64-token chunk, head)
 
 static __device__ __align__(256) unsigned char g_build_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu[kMaxDevices];
 
 // Device address of the scratch array on the current device.  The host-side name
 // g_build_scratch is only a stand-in, never a device address, so the address is
-// looked up with cudaGetSymbolAddress once per device (with that device current).
+// looked up with cudaGetSymbolAddress (with the device current).  Only a successful
+// lookup is kept: a failed one (say, a first call made while a stream is being
+// captured) is tried again on the next call instead of failing every later call.
 cudaError_t scratch_ptr(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev]() {
+  std::lock_guard<std::mutex> lock(g_scratch_mu[dev]);
+  if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_build_scratch);
+    e = cudaGetSymbolAddress(&p, g_build_scratch);
+    if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+  }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
 }
@@ -53,14 +54,17 @@ extern "C" hypic_status hypic_segment_build_batched_noalloc(const hypic_shape *s
                                                             float *T_out, float *S_out, float *o_out,
                                                             hypic_stream_t stream) {
   if (!shape || n_seg < 0 || max_len < 0) return HYPIC_EINVAL;
+  // With per-token outputs (o_out given) the build keeps the larger record per (chunk, head).
+  const bool want_o = o_out != nullptr;
+  const size_t need = want_o ? hypic_build_workspace_bytes_outputs(shape, n_seg, max_len)
+                             : hypic_build_workspace_bytes(shape, n_seg, max_len);
   // Shapes whose build needs no workspace go straight through.
-  if (hypic_build_workspace_bytes(shape, n_seg, max_len) == 0)
+  if (need == 0)
     return hypic_segment_build_batched(shape, n_seg, seg_bounds, max_len, n_tokens, k, v, q, alpha, beta, T_out,
                                        S_out, o_out, nullptr, 0, stream);
   // The build works through the heads in blocks that fit the scratch; one head's
   // records must fit, which bounds n_seg * ceil(max_len / 64).
-  const size_t one_head = (size_t)n_seg * (size_t)((max_len + 63) / 64) * hypic::kRecordBytes;
-  if (one_head > hypic::kScratchBytes) return HYPIC_ENOSPACE;
+  if (hypic::build_tc_min_workspace(n_seg, max_len, want_o) > hypic::kScratchBytes) return HYPIC_ENOSPACE;
   void *scratch = nullptr;
   if (hypic::scratch_ptr(&scratch) != cudaSuccess) return HYPIC_ECUDA;
   return hypic_segment_build_batched(shape, n_seg, seg_bounds, max_len, n_tokens, k, v, q, alpha, beta, T_out,

@@ -22,6 +22,7 @@ import statistics
 import subprocess
 import sys
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -37,28 +38,49 @@ FLOP_PER_HEAD_TOKEN_WY_O = (FLOP_PER_CHUNK_WY + 2 * 64 * D * D + 4 * 64 * 64 * D
 FLOP_PER_HEAD_TOKEN_RECURRENT = 4 * D * (2 * D)                      # k.x and rank-1 update on [T|S]
 FLOP_PER_HEAD_TOKEN_KDA_RECURRENT = FLOP_PER_HEAD_TOKEN_RECURRENT + D * (2 * D)  # + the channel gate
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
-# dram__bytes_read.sum + dram__bytes_write.sum of one build (wy_prep_kernel + chain_tc_kernel) on
-# this workload, from an ncu capture of the bench's own build launches.
-BUILD_TC_TRAFFIC = 277_309_440 + 747_578_368 + 1_370_620_928 + 38_123_776
-# The same for build_decay_tc_kernel on the 64 x 512-token, 32-head decay workloads, from an ncu
-# capture of those launches.
-DECAY_TC_TRAFFIC = {"scalar_const": 536_935_000 + 112_331_264, "diag": 1_073_959_000 + 122_754_304}
-# The same for compose_tc_kernel on the full warm-cache workload (generator-drawn pool of 256 x 960
-# pairs, 64 requests x 16), from a one-pass ncu capture of that launch: the
-# pool is re-read from L2, so DRAM traffic is far below the 128 KiB (fp32) / 64 KiB (bf16)
-# algorithmic bytes per composition.
-COMPOSE_TC_TRAFFIC = {"f32": 42_967_890_944 + 4_018_890_752, "bf16": 16_075_031_808 + 4_012_372_736}
-# The same for the two boundary-patch launches (staged RoPE shift, staged state re-rotation) on the
-# boundary workloads, first launch of a one-pass ncu capture: the reads are the whole input; the
-# writes counted during the launch are what L2 evicted before it ended (the rest follows later).
-BOUNDARY_TRAFFIC = {"rope_shift_32768x8x128_bf16": 67_140_864 + 15_822_080,
-                    "state_rerotate_64x32_128x128_fp32": 134_249_472 + 72_236_032}
-# The same for the build with per-token outputs (wy_prep_kernel<1>, the T-half chain_tc_kernel and
-# chain_so_kernel) on the 32k-token request, from a one-pass ncu capture of those launches.
-OUTPUTS_TC_TRAFFIC = 546_274_560 + 1_021_575_424 + 1_348_596_736 + 10_456_832 + 1_889_561_600 + 523_534_080
-# The same for the affine scan launch (compose_tc_kernel in scan mode) on the 64-pair, 960-head
-# workload, first launch of a one-pass ncu capture.
-SCAN_TRAFFIC = 8_456_816_128 + 8_021_051_904
+
+# Captured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch, from the ncu
+# captures summarised under profiles/.  Each entry carries the digest of the kernel sources it was
+# captured on (sha1 of the listed csrc files, first 12 hex digits) and the commit of the capture;
+# the bench reports a figure only while those sources are unchanged, and null once they differ.
+TRAFFIC = {
+    # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request
+    "build_tc": {"bytes": None, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
+    "build_outputs_tc": {"bytes": 5_339_999_232, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
+                         "commit": "2fc0e60"},
+    # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads
+    "decay_scalar_const": {"bytes": None, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": None,
+                           "commit": None},
+    "decay_diag": {"bytes": None, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    # compose_tc_kernel on the warm-cache workload (fp32 and bf16 pools), scaled from a reduced head count
+    "compose_f32": {"bytes": None, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    "compose_bf16": {"bytes": None, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    # compose_tc_kernel in scan mode, 64 pairs x 960 heads
+    "scan": {"bytes": 16_477_868_032, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b", "commit": "36258c6"},
+    # staged RoPE shift and state re-rotation
+    "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",
+                                    "commit": "ae9cc2f"},
+    "state_rerotate_64x32_128x128_fp32": {"bytes": 206_485_504, "src": ("boundary.cu",), "digest": "59ea01fe4941",
+                                          "commit": "ae9cc2f"},
+}
+
+
+def src_digest(names) -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_attention_state_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def traffic(key):
+    """Captured DRAM bytes of one launch, or None when not captured on the current sources."""
+    t = TRAFFIC[key]
+    if t["bytes"] is None or t["digest"] != src_digest(t["src"]):
+        return None
+    return t["bytes"]
 
 
 def load_peaks():
@@ -362,7 +384,7 @@ def decay_build_measure(steps, warmup, dev, peaks):
             by = per * ht + w.n_seg * w.H * w.d * w.d * 4
             entry["roofline"] = {"bound": "hbm", "achieved": by / tb / 1e9, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": by / tb / 1e9 / peaks["hbm_gbs"],
-                                 "bytes_per_head_token": per, "traffic": DECAY_TC_TRAFFIC.get(fam),
+                                 "bytes_per_head_token": per, "traffic": traffic("decay_" + fam),
                                  "kernel": "build_decay_tc_kernel"}
         entry["status"] = hy.stream_status()
         out[fam] = entry
@@ -393,7 +415,7 @@ def scan_measure(steps, warmup, dev, peaks):
     by = n * H * (2 * d * d * 4) * 2  # read T and S, write both prefixes
     res = {"workload": f"scan_{n}x{H}heads_d{d}_fp32", "prefix_pairs_per_s": n * H / t, "ms": t * 1e3,
            "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": by / t / 1e9 / peaks["hbm_gbs"], "traffic": SCAN_TRAFFIC},
+                        "frac": by / t / 1e9 / peaks["hbm_gbs"], "traffic": traffic("scan")},
            "status": hy.stream_status()}
     del T, S
     torch.cuda.empty_cache()
@@ -433,7 +455,7 @@ def build_outputs_measure(steps, warmup, dev, peaks):
     res = {"workload": w.name + "_with_outputs", "build_ms": tb * 1e3, "body_head_tokens_per_s": ht / tb,
            "roofline": {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": fl / tb / 1e12 / peaks["bf16_tflops"], "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY_O,
-                        "traffic": OUTPUTS_TC_TRAFFIC if os.environ.get("HYPIC_BUILD_PATH") != "recurrent" else None},
+                        "traffic": traffic("build_outputs_tc") if os.environ.get("HYPIC_BUILD_PATH") != "recurrent" else None},
            "status": hy.stream_status()}
     del tok, ws, T, S, o
     torch.cuda.empty_cache()
@@ -470,7 +492,7 @@ def boundary_measure(steps, warmup, dev, peaks):
         out[name] = {"ms": avg * 1e3, "roofline": {"bound": "hbm", "achieved": nbytes / avg / 1e9,
                                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                                     "frac": nbytes / avg / 1e9 / peaks["hbm_gbs"],
-                                                    "traffic": BOUNDARY_TRAFFIC[name]}}
+                                                    "traffic": traffic(name)}}
     out["status"] = hy.stream_status()
     del K, K_out, S
     torch.cuda.empty_cache()
@@ -510,7 +532,7 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
     out = torch.empty((pw.B, H, d, d), device=dev)
     comps = pw.B * pw.n * H
 
-    def timed(pT, pS, bytes_per_comp, name, traffic):
+    def timed(pT, pS, bytes_per_comp, name, traffic_bytes):
         torch.cuda.synchronize()
 
         def fn(ev):
@@ -528,7 +550,9 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
                 "ms_per_step": total_ms / steps,
                 "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"],
-                             "traffic": traffic if (pool is None and n is None) else None,
+                             "traffic": traffic_bytes if (pool is None and n is None) else None,
+                             "dram_frac": (traffic_bytes / avg / 1e9 / peaks["hbm_gbs"]
+                                           if traffic_bytes is not None and pool is None and n is None else None),
                              "bytes_per_composition": bytes_per_comp, "peak_source": peaks["source"]},
                 "status": hy.stream_status()}
 
@@ -537,13 +561,13 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
     out_per_comp = D * D * 4 / pw.n
     res = None
     if storage in ("f32", "both"):
-        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION + out_per_comp, pw.name, COMPOSE_TC_TRAFFIC["f32"])
+        res = timed(pool_T, pool_S, BYTES_PER_COMPOSITION + out_per_comp, pw.name, traffic("compose_f32"))
     if storage in ("bf16", "both"):
         T_lp, S_lp = hy.pairs_to_bf16(pool_T, pool_S, family="gated_delta")
         del pool_T, pool_S
         torch.cuda.empty_cache()
         lp = timed(T_lp, S_lp, BYTES_PER_COMPOSITION // 2 + out_per_comp, pw.name + "_bf16pairs",
-                   COMPOSE_TC_TRAFFIC["bf16"])
+                   traffic("compose_bf16"))
         del T_lp, S_lp
         if res is None:
             res = lp
@@ -552,6 +576,248 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
     else:
         del pool_T, pool_S
     torch.cuda.empty_cache()
+    return res
+
+
+def t_path_parity(dev, threads):
+    """The build on DeltaNet bodies (a = 1, 32 heads, 2 x 4096 tokens), whose T_C stays far above the
+    fp32 range where the headline workload's T_C underflows: T_C and S_{C|0} of sampled heads against
+    the oracle, so the line also checks the T half of the build."""
+    import numpy as np
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import oracle
+    import workloads as W
+    H, d, L_, nseg = 32, 128, 4096, 2
+    g = W.generator(dev, 5151, 0)
+    tok = W.draw_tokens(g, nseg * L_, H, d, "delta", "bf16", dev, need_q=False)
+    bounds = [(j * L_, (j + 1) * L_) for j in range(nseg)]
+    T, S = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=dev), None, tok["beta"],
+                                    family="delta", max_len=L_)
+    status = hy.stream_status()
+    heads = [0, 13, 31]
+    hk, hv, hb = (tok[x][:, heads].double().cpu().numpy() for x in ("k", "v", "beta"))
+    Tg = T[:, heads].double().cpu().numpy()
+    Sg = S[:, heads].double().cpu().numpy()
+    units = [(i, j) for i in range(len(heads)) for j in range(nseg)]
+
+    def ref(u):
+        i, j = u
+        b, e = bounds[j]
+        return oracle.segment_pair("delta", hk[b:e, i], hv[b:e, i], None, hb[b:e, i])
+
+    res = oracle.parallel_map(ref, units, threads=threads)
+    eT = eS = 0.0
+    tmin = float("inf")
+    for (i, j), (Tr, Sr) in zip(units, res):
+        eT = max(eT, float(np.linalg.norm(Tg[j, i].reshape(d, d) - Tr) / max(np.linalg.norm(Tr), 1e-30)))
+        eS = max(eS, float(np.linalg.norm(Sg[j, i] - Sr) / max(np.linalg.norm(Sr), 1e-30)))
+        tmin = min(tmin, float(np.linalg.norm(Tr)))
+    del tok, T, S
+    return {"workload": f"delta_{H}h_d{d}_{nseg}x{L_}", "heads": heads, "max_rel_err": {"T_C": eT, "S": eS},
+            "min_ref_T_C_norm": tmin, "tol": 2e-3, "ok": max(eT, eS) <= 2e-3, "status": status}
+
+
+def long_mixed_measure(steps, warmup, dev, peaks, threads, cpu=True):
+    """Long mixed request: 30 layers x 32 heads (960 layer-heads), d = 128, bf16 inputs, 128 segments x
+    1024 tokens (131,072 tokens); 32 cold segments built in the step, 96 arriving as cached fp32 pairs
+    (built beforehand, untimed); seam window w = 8 on every inner segment, with outputs.
+
+    One step = the cold builds (one batched launch over all layers) + the assembly (seams and 128
+    compositions per layer-head, one launch).  A secondary schedule runs the same work layer by layer
+    as a real stack would, a build and an assembly per layer (60 launches).  The oracle runs the step's
+    work for three sampled layer-heads on the host cores (cpu_baseline; its cached pairs oracle-built
+    beforehand, untimed) and the step's outputs are checked against it."""
+    import numpy as np
+    import torch
+
+    import linear_attention_state_gb300 as hy
+    import oracle
+    import workloads as W
+    w = W.LONG_MIXED
+    H, d, n, Ls, ww, hpl = w.H, w.d, w.n_seg, w.seg_len, w.w, w.heads
+    cold = W.long_mixed_cold(w)
+    cold_set = set(cold)
+    cached = [j for j in range(n) if j not in cold_set]
+    slot = {j: i for i, j in enumerate(cached + cold)}  # cached pairs first, the cold builds last
+    nc, nh = len(cached), len(cold)
+    bf = torch.bfloat16
+    pool_T = torch.empty((n, H, d, d), device=dev)
+    pool_S = torch.empty((n, H, d, d), device=dev)
+    ck = torch.empty((nh * Ls, H, d), dtype=bf, device=dev)
+    cv = torch.empty_like(ck)
+    ca = torch.empty((nh * Ls, H), device=dev)
+    cb = torch.empty_like(ca)
+    sk = torch.empty((1, n - 1, ww, H, d), dtype=bf, device=dev)
+    sv, sq = torch.empty_like(sk), torch.empty_like(sk)
+    sa = torch.empty((1, n - 1, ww, H), device=dev)
+    sb = torch.empty_like(sa)
+    ws1 = torch.empty(hy.build_workspace_bytes(H, d, 1, Ls), dtype=torch.uint8, device=dev)
+    cbounds = []
+    for j in range(n):
+        tok = w.draw_segment(j, dev)
+        lo = 0 if j == 0 else ww
+        if j >= 1:
+            sk[0, j - 1], sv[0, j - 1], sq[0, j - 1] = tok["k"][:ww], tok["v"][:ww], tok["q"][:ww]
+            sa[0, j - 1], sb[0, j - 1] = tok["alpha"][:ww], tok["beta"][:ww]
+        if j in cold_set:
+            c = cold.index(j)
+            ck[c * Ls:(c + 1) * Ls], cv[c * Ls:(c + 1) * Ls] = tok["k"], tok["v"]
+            ca[c * Ls:(c + 1) * Ls], cb[c * Ls:(c + 1) * Ls] = tok["alpha"], tok["beta"]
+            cbounds.append((c * Ls + lo, (c + 1) * Ls))
+        else:
+            i = slot[j]
+            hy.segment_build_batched(tok["k"][lo:], tok["v"][lo:], torch.tensor([[0, Ls - lo]], device=dev),
+                                     tok["alpha"][lo:], tok["beta"][lo:], family=w.family, max_len=Ls,
+                                     out=(pool_T[i:i + 1], pool_S[i:i + 1]), ws=ws1)
+        del tok
+    del ws1
+    cb_dev = torch.tensor(cbounds, dtype=torch.int64, device=dev)
+    ws_c = torch.empty(hy.build_workspace_bytes(H, d, nh, Ls), dtype=torch.uint8, device=dev)
+    idx = torch.tensor([[slot[j] for j in range(n)]], dtype=torch.int32, device=dev)
+    S_out = torch.empty((1, H, d, d), device=dev)
+    o = torch.empty((1, n - 1, ww, H, d), device=dev)
+    Tc, Sc = pool_T[nc:], pool_S[nc:]
+
+    def step(ev):
+        if ev is not None:
+            ev[0].record()
+        hy.segment_build_batched(ck, cv, cb_dev, ca, cb, family=w.family, max_len=Ls, out=(Tc, Sc), ws=ws_c)
+        if ev is not None:
+            ev[1].record()
+        hy.assemble(pool_T, pool_S, idx, sk, sv, sa, sb, seam_q=sq, family=w.family, out=S_out, o_out=o)
+        if ev is not None:
+            ev[2].record()
+
+    total_ms, kb, ka = run_timed(step, steps, warmup, torch.cuda.synchronize)
+    status = hy.stream_status()
+    step_s = total_ms / 1e3 / steps
+    tb, ta = sum(kb) / len(kb) / 1e3, sum(ka) / len(ka) / 1e3
+    build_ht = sum(e - b for b, e in cbounds) * H
+    comps = n * H
+    seam_ht = (n - 1) * ww * H
+    fl = FLOP_PER_HEAD_TOKEN_WY * build_ht
+    # assembly bytes: the pairs read, the seam tokens (q, k, v bf16 and two fp32 gates) read, their
+    # outputs written (fp32), the final state written
+    asm_bytes = comps * BYTES_PER_COMPOSITION + seam_ht * (3 * d * 2 + 8 + d * 4) + H * d * d * 4
+    res = {"workload": w.name, "cold_segments": nh, "cached_segments": nc,
+           "request_tokens_per_s": n * Ls / step_s, "ms_per_step": step_s * 1e3,
+           "build": {"ms": tb * 1e3, "body_head_tokens_per_s": build_ht / tb,
+                     "roofline": {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
+                                  "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"],
+                                  "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY, "units_per_launch": build_ht}},
+           "assemble": {"ms": ta * 1e3, "compositions_per_s": comps / ta, "seam_head_tokens_per_s": seam_ht / ta,
+                        "roofline": {"bound": "hbm", "achieved": asm_bytes / ta / 1e9, "peak": peaks["hbm_gbs"],
+                                     "unit": "GB/s", "frac": asm_bytes / ta / 1e9 / peaks["hbm_gbs"],
+                                     "bytes_per_step": asm_bytes}},
+           "status": status}
+    sample_heads = [0, 17 * hpl + 9, 29 * hpl + 31]
+    S_g = S_out[0, sample_heads].double().cpu().numpy()
+    o_g = o[0, :, :, sample_heads].double().cpu().numpy()           # [n-1, w, 3, d]
+    Tc_g = Tc[:, sample_heads].double().cpu().numpy()
+    Sc_g = Sc[:, sample_heads].double().cpu().numpy()
+
+    # Secondary schedule: layer by layer, a build of that layer's cold segments and its assembly.
+    del ws_c
+    per_layer = []
+    for layer in range(w.layers):
+        hs = slice(layer * hpl, (layer + 1) * hpl)
+        lp_T, lp_S = pool_T[:, hs].contiguous(), pool_S[:, hs].contiguous()
+        per_layer.append({"k": ck[:, hs].contiguous(), "v": cv[:, hs].contiguous(), "a": ca[:, hs].contiguous(),
+                          "b": cb[:, hs].contiguous(), "T": lp_T, "S": lp_S,
+                          "sk": sk[:, :, :, hs].contiguous(), "sv": sv[:, :, :, hs].contiguous(),
+                          "sq": sq[:, :, :, hs].contiguous(), "sa": sa[:, :, :, hs].contiguous(),
+                          "sb": sb[:, :, :, hs].contiguous(), "S_out": torch.empty((1, hpl, d, d), device=dev),
+                          "o": torch.empty((1, n - 1, ww, hpl, d), device=dev)})
+    del pool_T, pool_S, ck, cv, ca, cb, Tc, Sc
+    torch.cuda.empty_cache()
+    ws_l = torch.empty(hy.build_workspace_bytes(hpl, d, nh, Ls), dtype=torch.uint8, device=dev)
+
+    def serial(ev):
+        if ev is not None:
+            ev[0].record()
+        for L_ in per_layer:
+            hy.segment_build_batched(L_["k"], L_["v"], cb_dev, L_["a"], L_["b"], family=w.family, max_len=Ls,
+                                     out=(L_["T"][nc:], L_["S"][nc:]), ws=ws_l)
+            hy.assemble(L_["T"], L_["S"], idx, L_["sk"], L_["sv"], L_["sa"], L_["sb"], seam_q=L_["sq"],
+                        family=w.family, out=L_["S_out"], o_out=L_["o"])
+        if ev is not None:
+            ev[1].record()
+            ev[2].record()
+
+    s_ms, _, _ = run_timed(serial, steps, min(warmup, 3), torch.cuda.synchronize)
+    s_step = s_ms / 1e3 / steps
+    res["per_layer_serial"] = {"launches": 2 * w.layers, "ms_per_step": s_step * 1e3,
+                               "request_tokens_per_s": n * Ls / s_step, "status": hy.stream_status()}
+    # the serial schedule computes the same request state as the batched one (the build's chain
+    # schedule differs with the head count, so the two agree to rounding, not bit for bit)
+    dev_err = 0.0
+    for i, h in enumerate(sample_heads):
+        x = per_layer[h // hpl]["S_out"][0, h % hpl].double().cpu().numpy()
+        dev_err = max(dev_err, float(np.linalg.norm(x - S_g[i]) / max(np.linalg.norm(S_g[i]), 1e-30)))
+    res["per_layer_serial"]["max_rel_diff_vs_batched"] = dev_err
+    del per_layer, ws_l
+    torch.cuda.empty_cache()
+    if not cpu:
+        return res
+
+    # Oracle on the host: the step's work for the sampled layer-heads (cold builds + assembly), and the
+    # step's outputs against it.  Inputs are the device draws of those heads, copied to the host.
+    host = {key: [] for key in ("k", "q", "v", "alpha", "beta")}
+    for j in range(n):
+        t = w.draw_segment(j, dev, heads=sample_heads)
+        for key in host:
+            host[key].append(t[key].double().cpu().numpy())
+        del t
+    fam = w.family
+
+    def body(i, j):
+        lo = 0 if j == 0 else ww
+        return tuple(host[x][j][lo:, i] for x in ("k", "v", "alpha", "beta"))
+
+    cached_units = [(i, j) for i in range(len(sample_heads)) for j in cached]
+    pairs = dict(zip(cached_units, oracle.parallel_map(lambda u: oracle.segment_pair(fam, *body(*u)), cached_units,
+                                                       threads=threads)))
+    cold_units = [(i, j) for i in range(len(sample_heads)) for j in cold]
+    t0 = time.perf_counter()
+    pairs.update(zip(cold_units, oracle.parallel_map(lambda u: oracle.segment_pair(fam, *body(*u)), cold_units,
+                                                     threads=threads)))
+
+    def assemble_ref(i):
+        S = np.zeros((d, d))
+        outs = []
+        for j in range(n):
+            if j >= 1:
+                S, oj = oracle.run(fam, host["k"][j][:ww, i], host["v"][j][:ww, i], host["alpha"][j][:ww, i],
+                                   host["beta"][j][:ww, i], q=host["q"][j][:ww, i], S0=S)
+                outs.append(oj)
+            T, S0 = pairs[(i, j)]
+            S = oracle.compose(fam, T[None], S0[None], S_init=S)
+        return S, outs
+
+    ref = oracle.parallel_map(assemble_ref, list(range(len(sample_heads))), threads=threads)
+    dt = time.perf_counter() - t0
+
+    def rel(x, r):
+        return float(np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30))
+
+    err = {"cold_T_C": 0.0, "cold_S": 0.0, "seam_o": 0.0, "composed_S": 0.0}
+    for i in range(len(sample_heads)):
+        for c, j in enumerate(cold):
+            Tr, Sr = pairs[(i, j)]
+            err["cold_T_C"] = max(err["cold_T_C"], rel(Tc_g[c, i], Tr))
+            err["cold_S"] = max(err["cold_S"], rel(Sc_g[c, i], Sr))
+        Sf, outs = ref[i]
+        err["composed_S"] = max(err["composed_S"], rel(S_g[i], Sf))
+        for jj, oj in enumerate(outs):
+            err["seam_o"] = max(err["seam_o"], rel(o_g[jj, :, i], oj))
+    res["parity"] = {"layer_heads": sample_heads, "max_rel_err": err, "tol": 2e-3,
+                     "ok": all(v <= 2e-3 for v in err.values())}
+    frac = len(sample_heads) / H
+    res["cpu_baseline"] = {"value": n * Ls * frac / dt, "unit": "request tokens/s", "cores": threads, "kind": "oracle",
+                           "sample": f"{len(sample_heads)} of {H} layer-heads: {nh} cold builds + the assembly "
+                                     f"({n - 1} seam windows, {n} compositions), float64, {dt:.1f} s wall"}
     return res
 
 
@@ -577,6 +843,9 @@ def main():
                     help="time only the affine scan (profiling aid; prints its own line)")
     ap.add_argument("--boundary-only", action="store_true",
                     help="time only the boundary patches (profiling aid; prints its own line)")
+    ap.add_argument("--long-only", action="store_true",
+                    help="time only the long mixed request (profiling aid; prints its own line)")
+    ap.add_argument("--no-long", action="store_true", help="skip the long mixed request")
     ap.add_argument("--outputs-only", action="store_true",
                     help="time only the build with per-token outputs (profiling aid; prints its own line)")
     args = ap.parse_args()
@@ -628,12 +897,21 @@ def main():
             print(json.dumps({"metric": what, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                               "result": res}))
         return
+    if args.long_only:
+        res = long_mixed_measure(args.steps, args.warmup, dev, peaks, os.cpu_count() or 1,
+                                 cpu=rank == 0 and world == 1 and not args.no_cpu)
+        if rank == 0:
+            print(json.dumps({"metric": "long mixed request", "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "result": res}))
+        return
     req = RequestStep(w, dev)
     status0 = hy.stream_status()
     clocks = ClockSampler(local)
     total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all, finish=req.join)
     clk = clocks.stop()
     status = hy.stream_status()
+    # what the timed loop wrote, kept for the parity check (the end-to-end loop below reuses the buffers)
+    snap = types.SimpleNamespace(T=req.T.clone(), S=req.S.clone(), S_out=req.S_out.clone(), o=req.o.clone())
     t = torch.tensor([total_ms], device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -656,7 +934,7 @@ def main():
         flops = FLOP_PER_HEAD_TOKEN_WY * req.body_head_tokens
         pk = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": flops / avg_build_s / 1e12, "peak": pk, "unit": "TFLOP/s",
-                "frac": flops / avg_build_s / 1e12 / pk, "traffic": BUILD_TC_TRAFFIC,
+                "frac": flops / avg_build_s / 1e12 / pk, "traffic": traffic("build_tc"),
                 "kernel": "build: wy_prep_kernel + chain_tc_kernel (chunked WY, tcgen05)",
                 "peak_source": f"{peaks['source']} dense bf16 (burst)",
                 "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY, "units_per_launch": req.body_head_tokens}
@@ -698,22 +976,23 @@ def main():
 
     e2e_ms, _, _ = run_timed(e2e_step, args.steps, min(args.warmup, 3), sync_all, kernel_events=False)
     e2e_value = req.tokens * world / (e2e_ms / 1e3 / args.steps)
+    del dev_sets, host
 
-    decay = scan = bnd = outs = None
+    threads = os.cpu_count() or 1
+    decay = scan = bnd = outs = compose = longm = None
     if not args.no_compose:
         outs = build_outputs_measure(args.steps, args.warmup, dev, peaks)
         decay = decay_build_measure(args.steps, args.warmup, dev, peaks)
         scan = scan_measure(args.steps, args.warmup, dev, peaks)
         bnd = boundary_measure(args.steps, args.warmup, dev, peaks)
-    compose = None
-    if not args.no_compose:
-        del host
         compose = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
                                        args.compose_random, args.compose_storage)
+    if not args.no_long:
+        longm = long_mixed_measure(args.steps, args.warmup, dev, peaks, threads,
+                                   cpu=rank == 0 and world == 1 and not args.no_cpu)
 
-    cpu = parity = None
+    cpu = parity = t_par = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        threads = os.cpu_count() or 1
         n_heads = min(w.H, max(1, threads))
         torch.cuda.synchronize()
         # the device request's own inputs, so the oracle also checks what the timed loop computed
@@ -721,10 +1000,12 @@ def main():
                     "alpha": req.alpha[:, :n_heads].cpu(), "beta": req.beta[:, :n_heads].cpu(),
                     "q": req.q_full[:, :n_heads].cpu()}
         v_cpu, dt, ref = cpu_baseline(w, n_heads, threads, tok=host_tok)
-        parity = request_parity(req, w, ref, 2e-3 if w.in_dtype == "bf16" else 1e-5)
+        parity = request_parity(snap, w, ref, 2e-3 if w.in_dtype == "bf16" else 1e-5)
         cpu = {"value": v_cpu, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n_heads} of {w.H} heads of the same request, all 8 segments (pairs, seams, compose), "
                          f"float64, {dt:.1f} s wall"}
+        if os.environ.get("HYPIC_BUILD_PATH") != "recurrent":
+            t_par = t_path_parity(dev, threads)
 
     dtype = "f32" if os.environ.get("HYPIC_BUILD_PATH") == "recurrent" else "bf16"
     if rank == 0:
@@ -732,12 +1013,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "config": {"workload": w.name, "layers": w.layers, "heads": w.heads, "d": w.d, "segments": w.n_seg,
-                       "segment_tokens": w.seg_len, "seam_w": w.w, "inputs": "bf16 q/k/v, fp32 gates and state",
-                       "l2": "inputs larger than L2 (k+v 537 MB per step), no flush",
-                       "parallelism": f"replicas x{world}",
-                       "pipelining": "request i's assembly runs on a second stream while request i+1 builds "
-                                     "(pairs double-buffered); every step builds and assembles a whole request"},
+            "config": bench_config(w, world),
             "build": {"body_head_tokens_per_s": req.body_head_tokens / avg_build_s, "ms": avg_build_s * 1e3},
             "assemble": {"compositions_per_s": req.compositions / avg_asm_s,
                          "seam_head_tokens_per_s": req.seam_head_tokens / avg_asm_s, "ms": avg_asm_s * 1e3},
@@ -747,26 +1023,76 @@ def main():
             "affine_scan": scan,
             "boundary_patches": bnd,
             "build_with_outputs": outs,
+            "long_mixed": longm,
             "cpu_baseline": cpu,
             "parity": parity,
+            "parity_t_path": t_par,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": req.launches_per_step * args.steps,
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"], "window": "warm-up and timed steps"},
             "device_status": [status0, status],
         }
+        line["summary"] = summary(line)
         print(json.dumps(line))
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
 
 
+def bench_config(w, world):
+    """The workload of the headline line (both arms print the same)."""
+    return {"workload": w.name, "layers": w.layers, "heads": w.heads, "d": w.d, "segments": w.n_seg,
+            "segment_tokens": w.seg_len, "seam_w": w.w, "inputs": "bf16 q/k/v, fp32 gates and state",
+            "l2": "inputs larger than L2 (k+v 537 MB per step), no flush",
+            "parallelism": f"replicas x{world}",
+            "pipelining": "request i's assembly runs on a second stream while request i+1 builds "
+                          "(pairs double-buffered); every step builds and assembles a whole request"}
+
+
+def summary(line):
+    """The headline figures in a few hundred bytes, printed last in the JSON line."""
+    def r(x, n=3):
+        return None if x is None else float(f"{x:.{n}g}")
+
+    def g(d, *keys):
+        for k in keys:
+            if d is None:
+                return None
+            d = d.get(k) if isinstance(d, dict) else None
+        return d
+
+    cp = line.get("compose_pool")
+    dec = line.get("decay_builds") or {}
+    lm = line.get("long_mixed")
+    return {
+        "tok_per_s": r(line["value"]), "e2e_tok_per_s": r(line["e2e"]["value"]),
+        "build_ms": r(line["build"]["ms"]), "build_tensor_frac": r(line["roofline"]["frac"]),
+        "assemble_ms": r(line["assemble"]["ms"]),
+        "compose_f32": {"comp_per_s": r(g(cp, "compositions_per_s")), "hbm_frac": r(g(cp, "roofline", "frac")),
+                        "dram_frac": r(g(cp, "roofline", "dram_frac"))},
+        "compose_bf16": {"comp_per_s": r(g(cp, "bf16_pool", "compositions_per_s")),
+                         "hbm_frac": r(g(cp, "bf16_pool", "roofline", "frac")),
+                         "dram_frac": r(g(cp, "bf16_pool", "roofline", "dram_frac"))},
+        "scan_hbm_frac": r(g(line.get("affine_scan"), "roofline", "frac")),
+        "decay_frac": {f: r(g(dec, f, "roofline", "frac")) for f in dec},
+        "outputs_build_tensor_frac": r(g(line.get("build_with_outputs"), "roofline", "frac")),
+        "long_mixed": {"tok_per_s": r(g(lm, "request_tokens_per_s")),
+                       "build_tensor_frac": r(g(lm, "build", "roofline", "frac")),
+                       "assemble_hbm_frac": r(g(lm, "assemble", "roofline", "frac")),
+                       "serial_tok_per_s": r(g(lm, "per_layer_serial", "request_tokens_per_s"))},
+        "parity_ok": {"request": g(line.get("parity"), "ok"), "t_path": g(line.get("parity_t_path"), "ok"),
+                      "long_mixed": g(lm, "parity", "ok")},
+    }
+
+
 def run_reference(args, w, rank, world):
-    """Reference arm: the float64 oracle on the host cores, K timed steps of a bounded sample."""
+    """Reference arm: the float64 oracle on every host core, K timed steps of a bounded sample of the
+    same request (half the heads on 16 cores), in the headline line's format and config."""
     if rank != 0:
         return
     threads = os.cpu_count() or 1
-    n_heads = min(w.H, max(1, threads // 4))
+    n_heads = min(w.H, max(1, threads))
     for _ in range(args.warmup):
         cpu_baseline(w, 1, 1)
     t0 = time.perf_counter()
@@ -777,9 +1103,10 @@ def run_reference(args, w, rank, world):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "sample": f"{n_heads} of {w.H} heads per step"},
+            "config": bench_config(w, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n_heads} of {w.H} heads of the request per step"},
+                             "sample": f"{n_heads} of {w.H} heads of the request per step, {threads} threads; "
+                                       "tokens/s scaled to the whole request"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

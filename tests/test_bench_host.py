@@ -56,3 +56,37 @@ def test_parity_floor_keeps_underflowed_transitions_quiet():
     tiny = {h: ([np.full(16, 1e-154) for _ in range(3)], Ss, os_, Sf) for h, (_, Ss, os_, Sf) in ref.items()}
     p = bench.request_parity(req, wl, tiny, 2e-3)
     assert p["max_rel_err"]["T_C"] < 1e-100 and p["ok"]
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_captured_on(monkeypatch):
+    """A captured DRAM figure carries the digest of its kernel sources; once they change, the line
+    reports null instead of a stale number."""
+    entry = {"bytes": 123, "src": ("build_tc.cu",), "digest": bench.src_digest(("build_tc.cu",)), "commit": "x"}
+    monkeypatch.setitem(bench.TRAFFIC, "build_tc", entry)
+    assert bench.traffic("build_tc") == 123
+    monkeypatch.setitem(bench.TRAFFIC, "build_tc", dict(entry, digest="000000000000"))
+    assert bench.traffic("build_tc") is None
+    monkeypatch.setitem(bench.TRAFFIC, "build_tc", dict(entry, bytes=None))
+    assert bench.traffic("build_tc") is None
+
+
+def test_summary_is_compact_and_tolerates_missing_legs():
+    import json
+    line = {"value": 45977012.07, "e2e": {"value": 11924399.0}, "build": {"ms": 0.70312},
+            "roofline": {"frac": 0.13812345}, "assemble": {"ms": 0.105},
+            "compose_pool": {"compositions_per_s": 3.6e7, "roofline": {"frac": 0.718, "dram_frac": 0.25},
+                             "bf16_pool": {"compositions_per_s": 6.3e7, "roofline": {"frac": 0.65, "dram_frac": None}}},
+            "decay_builds": {"scalar_const": {"roofline": {"frac": 0.703}}}, "affine_scan": None,
+            "build_with_outputs": None, "long_mixed": None, "parity": {"ok": True}, "parity_t_path": None}
+    s = bench.summary(line)
+    assert s["build_tensor_frac"] == 0.138 and s["compose_f32"]["dram_frac"] == 0.25
+    assert s["scan_hbm_frac"] is None and s["long_mixed"]["tok_per_s"] is None
+    assert s["parity_ok"] == {"request": True, "t_path": None, "long_mixed": None}
+    assert len(json.dumps(s)) < 900
+
+
+def test_both_arms_print_the_same_config():
+    import workloads as W
+    assert bench.bench_config(W.BUILD_32K, 1) == bench.bench_config(W.BUILD_32K, 1)
+    src = open(bench.__file__).read()
+    assert src.count('"config": bench_config(w, world)') == 2

@@ -74,6 +74,18 @@ def test_ragged_bodies(family):
 
 
 @pytest.mark.parametrize("family", FAMS)
+def test_several_units_per_cta_with_empty_and_ragged_bodies(family):
+    """More units than SMs, so every CTA walks several (segment, head) units and reads each next
+    unit's bounds and gates ahead of time, across empty, one-token and ragged bodies."""
+    lens = [0, 1, 37, 64, 65, 130, 300]
+    H = 48  # 336 units over at most 152 CTAs
+    tok, bounds, T, S = run_case(family, lens, H, key=40 + FAMS.index(family))
+    eT, eS = check(family, tok, bounds, T, S, H)
+    print(f"{family} several units per CTA: max rel err T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+
+
+@pytest.mark.parametrize("family", FAMS)
 def test_last_chunk_runs_past_the_token_axis(family):
     # the final body ends at the last token and its length is not a multiple of 64, so the
     # tensor-map loads of its last chunk read past the axis (zero fill)

@@ -367,10 +367,15 @@ def decay_build_measure(steps, warmup, dev, peaks):
         ht = w.n_seg * w.seg_len * w.H
         entry = {"build_head_tokens_per_s": ht / tb, "build_ms": tb * 1e3,
                  "compose_ms": tc * 1e3, "compositions_per_s": w.n_seg * w.H / tc}
-        if fam == "gated_delta":
+        recurrent = os.environ.get("HYPIC_BUILD_PATH") == "recurrent"
+        if fam == "gated_delta" or (fam == "kda" and not recurrent):
+            # chunked WY count (the per-channel decay of KDA leaves the products' shapes unchanged)
             fl = FLOP_PER_HEAD_TOKEN_WY * ht
             entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
-                                 "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"]}
+                                 "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"],
+                                 "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY,
+                                 "kernel": ("kda_prep_kernel + chain_kda_kernel" if fam == "kda" else
+                                            "wy_prep_kernel + chain_tc_kernel")}
         elif fam == "kda":
             # token-by-token fp32 kernel (no chunked KDA build): fp32 FMA roofline
             fl = FLOP_PER_HEAD_TOKEN_KDA_RECURRENT * ht

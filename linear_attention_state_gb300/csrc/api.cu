@@ -87,6 +87,9 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
                    !force_recurrent();
   if (tc && (ws_bytes < build_tc_min_workspace(n_seg, seg.max_len, o_out != nullptr) || !ok_ptr(ws)))
     return HYPIC_ENOSPACE;
+  const bool ktc = tokens && build_kda_tc_supported(sh->d_k, sh->family, sh->in_dtype, o_out != nullptr) &&
+                   !force_recurrent();
+  if (ktc && (ws_bytes < build_kda_tc_min_workspace(n_seg, seg.max_len) || !ok_ptr(ws))) return HYPIC_ENOSPACE;
   int *err = nullptr;
   cudaError_t e = status_word(&err);
   if (e != cudaSuccess) return HYPIC_ECUDA;
@@ -103,6 +106,7 @@ hypic_status build_common(const hypic_shape *sh, int32_t n_seg, const SegMap &se
   a.o_out = o_out;
   a.err = err;
   if (tc) return from_cuda(launch_build_tc(a, ws, ws_bytes, st));
+  if (ktc) return from_cuda(launch_build_kda_tc(a, ws, ws_bytes, st));
   if (dtc) return from_cuda(launch_build_decay_tc(a, st));
   return from_cuda(launch_recurrent(a, st));
 }
@@ -138,6 +142,8 @@ const char *hypic_strerror(hypic_status s) {
 
 size_t hypic_build_workspace_bytes(const hypic_shape *sh, int32_t n_seg, int64_t max_len) {
   if (check_shape(sh) != HYPIC_OK || n_seg <= 0 || max_len <= 0) return 0;
+  if (build_kda_tc_supported(sh->d_k, sh->family, sh->in_dtype, false))
+    return build_kda_tc_workspace_bytes(sh->H, n_seg, max_len);
   if (!build_tc_supported(sh->d_k, sh->family, sh->in_dtype, false)) return 0;
   return build_tc_workspace_bytes(sh->H, n_seg, max_len, false);
 }

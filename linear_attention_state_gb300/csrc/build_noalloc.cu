@@ -64,7 +64,10 @@ extern "C" hypic_status hypic_segment_build_batched_noalloc(const hypic_shape *s
                                        S_out, o_out, nullptr, 0, stream);
   // The build works through the heads in blocks that fit the scratch; one head's
   // records must fit, which bounds n_seg * ceil(max_len / 64).
-  if (hypic::build_tc_min_workspace(n_seg, max_len, want_o) > hypic::kScratchBytes) return HYPIC_ENOSPACE;
+  const size_t one_head = (shape->family == HYPIC_FAM_KDA && !want_o)
+                              ? hypic::build_kda_tc_min_workspace(n_seg, max_len)
+                              : hypic::build_tc_min_workspace(n_seg, max_len, want_o);
+  if (one_head > hypic::kScratchBytes) return HYPIC_ENOSPACE;
   void *scratch = nullptr;
   if (hypic::scratch_ptr(&scratch) != cudaSuccess) return HYPIC_ECUDA;
   return hypic_segment_build_batched(shape, n_seg, seg_bounds, max_len, n_tokens, k, v, q, alpha, beta, T_out,

@@ -60,6 +60,13 @@ size_t build_tc_workspace_bytes(int H, int n_seg, int64_t max_len, bool want_o);
 size_t build_tc_min_workspace(int n_seg, int64_t max_len, bool want_o);          // one head
 cudaError_t launch_build_tc(const RecurrentArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
 
+// Chunked tcgen05 build for the KDA family (d = 128, bf16 inputs, no per-token outputs): per-(chunk,
+// head) operand records in the workspace, processed over blocks of heads that fit.
+bool build_kda_tc_supported(int D, int fam, int in_dtype, bool want_o);
+size_t build_kda_tc_workspace_bytes(int H, int n_seg, int64_t max_len);  // preferred size
+size_t build_kda_tc_min_workspace(int n_seg, int64_t max_len);           // one head
+cudaError_t launch_build_kda_tc(const RecurrentArgs &a, void *ws, size_t ws_bytes, cudaStream_t st);
+
 // Tensor-core build for the scalar and diagonal decay families (d = 128, bf16 inputs, no
 // per-token outputs): one accumulating GEMM per (segment, head), no workspace.
 bool build_decay_tc_supported(int D, int fam, int in_dtype, bool want_o);

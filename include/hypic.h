@@ -179,7 +179,12 @@ hypic_status hypic_segment_build_batched_host(const hypic_shape *shape, int32_t 
  * cooperative launch), segments cut between CTAs (once when U exceeds the SMs,
  * into pieces of at least 8 chunks when there are fewer units) are rejoined by
  * composing their pieces' pairs in the kernel.  Without that room each unit gets
- * its own CTA; results agree to rounding either way.  The
+ * its own CTA; results agree to rounding either way.  The KDA family at d = 128
+ * with bf16 inputs (pairs only) keeps an 82,432-byte record per (64-token chunk,
+ * head) -- W_k^T, -A diag(b) and the per-channel decayed keys in hi and lo
+ * pieces plus the chunk's channel decays -- so any size holding one head's
+ * records (n_seg * ceil(max_len / 64) * 82,432 bytes) works; its preferred size
+ * covers all heads up to about 4 GiB and has no split-schedule area.  The
  * workspace is caller-owned device memory, 16-byte aligned, and must not be used
  * by anything else until the stream reaches the end of the call.
  */
@@ -208,7 +213,8 @@ size_t hypic_build_workspace_bytes_outputs(const hypic_shape *shape, int32_t n_s
  * Limit: one head's operand records must fit the scratch.  Without outputs
  * (o_out NULL) a record is 49,664 bytes per (64-token chunk, head):
  * n_seg * ceil(max_len / 64) <= 1351.  With per-token outputs (q and o_out
- * given) it is 66,560 bytes: n_seg * ceil(max_len / 64) <= 1008.  Larger
+ * given) it is 66,560 bytes: n_seg * ceil(max_len / 64) <= 1008.  The KDA
+ * family's records are 82,432 bytes: n_seg * ceil(max_len / 64) <= 814.  Larger
  * requests return HYPIC_ENOSPACE before anything is enqueued.  More heads are
  * processed in blocks that fit.  The first call on a device looks up the
  * scratch array's device address (with that device current; a lookup that

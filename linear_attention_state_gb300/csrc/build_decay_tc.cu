@@ -44,18 +44,23 @@ constexpr int NT = 320;
 constexpr uint32_t BAR_CONV = 1, BAR_EPI = 2;
 
 // Stage layout (1024-aligned): K / Khat hi [2 boxes of 64 t x 64 i, SW128] at 0, V at 16384,
-// gates [64 t][128 i] fp32 (diagonal) at 32768, whose first 16 KB later take Khat lo
-// (scalar families: Khat lo only).  After the stages: the store's row buffer.
+// gates [64 t][128 i] fp32 (diagonal) at 32768, whose first 16 KB later take Khat lo.  The scalar
+// families keep Khat (hi and lo) in tensor memory instead, as the MMA's A operand, so their stage
+// is the 32 KB of K and V and six stages fit.  After the stages: the store's row buffer.
 template <bool DIAG>
 struct Cfg {
-  static constexpr uint32_t STAGE = DIAG ? 65536u : 49152u;
-  static constexpr int NS = DIAG ? 3 : 4;
+  static constexpr uint32_t STAGE = DIAG ? 65536u : 32768u;
+  static constexpr int NS = DIAG ? 3 : 6;
   static constexpr uint32_t TX = DIAG ? 65536u : 32768u;
   static constexpr uint32_t OFF_OUT = STAGE * NS;
   static constexpr uint32_t SMEM = OFF_OUT + 128 * 144 + 1024;
 };
 constexpr uint32_t OFF_V = 16384, OFF_G = 32768;
 constexpr uint32_t OUT_STRIDE = 144;  // one padded row of a 32-column block of S, in bytes
+// Tensor memory: two accumulators (columns 0 and 128); scalar families: KB buffers of Khat^T pieces
+// (lanes = key channels, 32 columns of token pairs each for hi, then lo) from column 256.
+constexpr int KB = 3;
+constexpr uint32_t TM_KH = 256;
 
 struct DecayArgs {
   int H, n_seg;
@@ -113,6 +118,7 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr int NS = G::NS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[NS], bar_conv[NS], bar_empty[NS], bar_acc_full[2], bar_acc_empty[2];
+  __shared__ uint64_t bar_kfree[KB];  // scalar families: the MMAs have read a Khat buffer
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ float s_f[2][C];  // scalar families: factors of the current chunk (double buffered)
@@ -131,11 +137,13 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&bar_acc_full[i], 1);
       mbar_init(&bar_acc_empty[i], 128);
     }
+    for (int i = 0; i < KB; ++i) mbar_init(&bar_kfree[i], 1);
     mbar_fence_init();
     abort_flag = 0;
   }
+  constexpr uint32_t TM_ALLOC = DIAG ? 256 : 512;
   if (warp == 0) {
-    tmem_alloc(&tmem_slot, 256);
+    tmem_alloc(&tmem_slot, TM_ALLOC);
     tmem_relinquish();
   }
   __syncthreads();
@@ -180,7 +188,8 @@ __global__ void __launch_bounds__(NT, 1)
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_f32acc(1, 1, 1, 1, 128, 128);  // A = Khat^T, B = V, both MN-major
+      // A = Khat^T (MN-major in shared memory, or from tensor memory for the scalar families), B = V
+      const uint32_t idesc = DIAG ? idesc_f32acc(1, 1, 1, 1, 128, 128) : idesc_f32acc(1, 1, 0, 1, 128, 128);
       int j = 0, m = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
@@ -196,13 +205,20 @@ __global__ void __launch_bounds__(NT, 1)
           }
           tc_fence_after();
           const uint32_t kb = sb + st * G::STAGE;
+          const uint32_t kt = tmem + TM_KH + (uint32_t)(j % KB) * 64;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bv = sdesc_sw128(kb + OFF_V + kk * 2048, 8192, 1024);
-            mma_f16(tmem + acc * 128, sdesc_sw128(kb + kk * 2048, 8192, 1024), bv, idesc, (q | kk) != 0);
-            mma_f16(tmem + acc * 128, sdesc_sw128(kb + OFF_G + kk * 2048, 8192, 1024), bv, idesc, 1);
+            if constexpr (DIAG) {
+              mma_f16(tmem + acc * 128, sdesc_sw128(kb + kk * 2048, 8192, 1024), bv, idesc, (q | kk) != 0);
+              mma_f16(tmem + acc * 128, sdesc_sw128(kb + OFF_G + kk * 2048, 8192, 1024), bv, idesc, 1);
+            } else {
+              mma_f16_tmem_a(tmem + acc * 128, kt + kk * 8, bv, idesc, (q | kk) != 0);
+              mma_f16_tmem_a(tmem + acc * 128, kt + 32 + kk * 8, bv, idesc, 1);
+            }
           }
           mma_commit(&bar_empty[st]);
+          if constexpr (!DIAG) mma_commit(&bar_kfree[j % KB]);
           last_commit = j;
           if (q == U.nch - 1) mma_commit(&bar_acc_full[acc]);
         }
@@ -271,6 +287,41 @@ __global__ void __launch_bounds__(NT, 1)
         }
         bar_sync_named(BAR_CONV, 128);
 
+        if constexpr (!DIAG) {
+          // (2) Khat^T row i = f_t k_ti over the chunk's tokens, hi and lo pieces into tensor
+          // memory (lane i, token pairs per column) once the MMAs of chunk j - KB have read the buffer.
+          const int buf = j % KB;
+          const bool kfree = j < KB || wait_or_abort(&bar_kfree[buf], (uint32_t)((j / KB - 1) & 1), &abort_flag, a.err);
+          if (bar_or_named(BAR_CONV, 128, !kfree)) {  // one decision for all converters
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const int i = tid;
+          const uint8_t *kcol = base + (uint32_t)(i >> 6) * 8192u + (uint32_t)(i & 7) * 2u;
+          const uint32_t ck = (uint32_t)((i & 63) >> 3);
+          const float *ft = s_f[j & 1];
+          float hw[32], lw[32];
+#pragma unroll
+          for (int t = 0; t < C; t += 2) {
+            const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t, ck)));
+            const float k1 =
+                __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t + 1, ck)));
+            const float x0 = ft[t] * k0, x1 = ft[t + 1] * k1;
+            const __nv_bfloat162 hp = __floats2bfloat162_rn(x0, x1);
+            const float2 hf = __bfloat1622float2(hp);
+            const __nv_bfloat162 lp = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+            hw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
+            lw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
+          }
+          const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+          tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64, hw);
+          tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64 + 32, lw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bar_conv[st]);
+          continue;
+        }
         // (2) Khat = f * k: hi over K in place, lo into the lo slot.  On the diagonal path the
         // lo slot overlaps the factor tile, so all factors are read before any lo is written.
         uint32_t lo_w[8][4];
@@ -377,7 +428,7 @@ __global__ void __launch_bounds__(NT, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, TM_ALLOC);
 }
 
 int sm_count() {

@@ -44,18 +44,27 @@ BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S
 # captured on (sha1 of the listed csrc files, first 12 hex digits) and the commit of the capture;
 # the bench reports a figure only while those sources are unchanged, and null once they differ.
 TRAFFIC = {
-    # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request
-    "build_tc": {"bytes": None, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
+    "build_tc": {"bytes": 2_431_883_776, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
+                 "commit": "edc1dcb"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
     "build_outputs_tc": {"bytes": 5_339_999_232, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
                          "commit": "2fc0e60"},
-    # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads
-    "decay_scalar_const": {"bytes": None, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": None,
-                           "commit": None},
-    "decay_diag": {"bytes": None, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
-    # compose_tc_kernel on the warm-cache workload (fp32 and bf16 pools), scaled from a reduced head count
-    "compose_f32": {"bytes": None, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
-    "compose_bf16": {"bytes": None, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": None, "commit": None},
+    # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
+    "decay_scalar_const": {"bytes": 645_460_138, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
+                           "digest": "5f8476ae66e0", "commit": "edc1dcb"},
+    "decay_diag": {"bytes": 1_193_407_829, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "5f8476ae66e0",
+                   "commit": "edc1dcb"},
+    # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
+    "decay_kda": {"bytes": 3_970_323_882, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9bf23969ba4a",
+                  "commit": "edc1dcb"},
+    # compose_tc_kernel on the warm-cache workload (fp32 and bf16 pools): captured at 4 layers
+    # (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each head's pool entries
+    # and requests are independent, the grid head-major)
+    "compose_f32": {"bytes": 46_900_577_280, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b",
+                    "commit": "edc1dcb"},
+    "compose_bf16": {"bytes": 20_228_006_400, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b",
+                     "commit": "edc1dcb"},
     # compose_tc_kernel in scan mode, 64 pairs x 960 heads
     "scan": {"bytes": 16_477_868_032, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b", "commit": "36258c6"},
     # staged RoPE shift and state re-rotation
@@ -374,6 +383,7 @@ def decay_build_measure(steps, warmup, dev, peaks):
             entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"],
                                  "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY,
+                                 "traffic": traffic("decay_kda") if fam == "kda" else None,
                                  "kernel": ("kda_prep_kernel + chain_kda_kernel" if fam == "kda" else
                                             "wy_prep_kernel + chain_tc_kernel")}
         elif fam == "kda":
@@ -504,7 +514,8 @@ def boundary_measure(steps, warmup, dev, peaks):
     return out
 
 
-def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False, storage="both"):
+def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pairs=False, storage="both",
+                         layers=None):
     """Warm-cache composition: 30 layers x 32 heads, pool of 256 pairs, 64 requests x 16 segments.
 
     storage "f32": fp32 pairs (128 KiB per composition); "bf16": the same pairs rounded to bf16
@@ -517,9 +528,9 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
     import linear_attention_state_gb300 as hy
     import workloads as W
     pw = W.COMPOSE_POOL
-    if pool is not None or n is not None:
-        pw = dataclasses.replace(pw, pool=pool or pw.pool, n=n or pw.n,
-                                 name=f"compose_30x32_d128_pool{pool or pw.pool}_B{pw.B}x{n or pw.n}")
+    if pool is not None or n is not None or layers is not None:
+        pw = dataclasses.replace(pw, pool=pool or pw.pool, n=n or pw.n, layers=layers or pw.layers,
+                                 name=f"compose_{layers or pw.layers}x32_d128_pool{pool or pw.pool}_B{pw.B}x{n or pw.n}")
     H, d, P = pw.H, pw.d, pw.pool
     if random_pairs:
         pool_T, pool_S = W.random_pairs(P, H, d, dev, key=3)
@@ -555,9 +566,10 @@ def compose_pool_measure(steps, warmup, dev, peaks, pool=None, n=None, random_pa
                 "ms_per_step": total_ms / steps,
                 "roofline": {"bound": "hbm", "achieved": bytes_ / avg / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": bytes_ / avg / 1e9 / peaks["hbm_gbs"],
-                             "traffic": traffic_bytes if (pool is None and n is None) else None,
+                             "traffic": traffic_bytes if (pool is None and n is None and layers is None) else None,
                              "dram_frac": (traffic_bytes / avg / 1e9 / peaks["hbm_gbs"]
-                                           if traffic_bytes is not None and pool is None and n is None else None),
+                                           if traffic_bytes is not None and pool is None and n is None
+                                           and layers is None else None),
                              "bytes_per_composition": bytes_per_comp, "peak_source": peaks["source"]},
                 "status": hy.stream_status()}
 
@@ -840,6 +852,10 @@ def main():
     ap.add_argument("--compose-pool", type=int, default=None, help="pool entries per head (default 256)")
     ap.add_argument("--compose-n", type=int, default=None, help="segments per request (default 16)")
     ap.add_argument("--compose-random", action="store_true", help="generator-drawn pairs instead of built ones")
+    ap.add_argument("--compose-layers", type=int, default=None,
+                    help="layers of 32 heads in the composition measurement (default 30; fewer for profiling)")
+    ap.add_argument("--build-only", action="store_true",
+                    help="time only the headline request's build and assembly loop (profiling aid)")
     ap.add_argument("--compose-storage", default="both", choices=["both", "f32", "bf16"],
                     help="pair storage of the composition measurement (fp32, bf16 or both)")
     ap.add_argument("--decay-only", action="store_true",
@@ -886,7 +902,7 @@ def main():
 
     if args.compose_only:
         res = compose_pool_measure(args.steps, args.warmup, dev, peaks, args.compose_pool, args.compose_n,
-                                   args.compose_random, args.compose_storage)
+                                   args.compose_random, args.compose_storage, args.compose_layers)
         if rank == 0:
             print(json.dumps({"metric": "compositions/s", "value": res["compositions_per_s"] * world,
                               "unit": "compositions/s", "n_gpus": world, "steps": args.steps,
@@ -911,6 +927,14 @@ def main():
         return
     req = RequestStep(w, dev)
     status0 = hy.stream_status()
+    if args.build_only:
+        total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all, finish=req.join)
+        if rank == 0:
+            print(json.dumps({"metric": "build and assembly loop", "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+                              "build_ms": sum(k_build) / len(k_build), "assemble_ms": sum(k_asm) / len(k_asm),
+                              "status": hy.stream_status()}))
+        return
     clocks = ClockSampler(local)
     total_ms, k_build, k_asm = run_timed(req.step, args.steps, args.warmup, sync_all, finish=req.join)
     clk = clocks.stop()

@@ -37,6 +37,8 @@ using namespace tc;
 constexpr int D = 128;
 constexpr int NT = 256;
 constexpr int R = 64;  // rows of the column each thread owns
+constexpr int SG = 8;  // seam tokens per group (one coalesced load, one shared-memory pass)
+constexpr int NL = SG * D / NT;  // each thread's share of one token tensor of a group
 
 // fp32 pairs
 constexpr uint32_t OFF_TST = 0;                 // T staging, fp32, 4 boxes [128 i][32 k] swizzled
@@ -218,8 +220,41 @@ __global__ void __launch_bounds__(NT, 1)
   const Tin *SV = static_cast<const Tin *>(a.seam_v);
   const Tin *SQ = static_cast<const Tin *>(a.seam_q);
   uint32_t ph = 0;
+  const bool kda = a.fam == HYPIC_FAM_KDA;
+  const bool want_o = a.o_out != nullptr;
+  // Tokens [t0, t0 + SG) of the seam window that follows composition step `st`, this thread's share.
+  auto load_seam = [&](int st, int t0, float (&lk)[NL], float (&lv)[NL], float (&lq)[NL], float (&lg)[NL],
+                       float &la, float &lb) {
+    const int ng = a.w - t0 < SG ? a.w - t0 : SG;
+    const size_t tok0 = ((size_t)b * (a.n - 1) + st) * a.w + t0;
+    la = 1.f;
+    lb = 0.f;
+    if (tid < ng) {
+      const size_t tok = tok0 + tid;
+      la = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
+      lb = a.seam_beta[tok * H + h];
+    }
+#pragma unroll
+    for (int it = 0; it < NL; ++it) {
+      const int e = tid + it * NT, t = e / D, i = e % D;
+      lk[it] = lv[it] = lq[it] = 0.f;
+      lg[it] = 1.f;
+      if (t < ng) {
+        const size_t g = ((tok0 + t) * H + h) * D + i;
+        lk[it] = ld_tok<Tin>(SK, g);
+        lv[it] = ld_tok<Tin>(SV, g);
+        lq[it] = want_o ? ld_tok<Tin>(SQ, g) : 0.f;
+        lg[it] = kda ? a.seam_alpha[g] : 1.f;
+      }
+    }
+  };
 
   for (int step = 0; step < a.n; ++step) {
+    // The first token group of the seam window after this step is loaded now: the state lives in
+    // tensor memory until the epilogue, so these registers are free, and the loads' latency hides
+    // behind the step's T split and products.
+    float pk[NL], pv[NL], pq[NL], pg[NL], pa = 1.f, pb = 0.f;
+    if (a.w > 0 && step + 1 < a.n) load_seam(step, 0, pk, pv, pq, pg, pa, pb);
     // (1) T of this step: fp32 staging -> three bf16 B pieces [128 i][128 k], K-major, swizzled.
     // Thread (row i, half) converts k in [64 half, 64 half + 64).  bf16 pairs: already in place.
     if (tid == 0) {
@@ -338,9 +373,6 @@ __global__ void __launch_bounds__(NT, 1)
       // one warp per token forms q . k, and each token then needs a single barrier, the partial
       // sums k . y and q . y of the two row halves alternating between two slots.
       if (a.w > 0) {
-        constexpr int SG = 8;
-        const bool kda = a.fam == HYPIC_FAM_KDA;
-        const bool want_o = a.o_out != nullptr;
         float *sK = sS0;               // [SG][D]
         float *sQ = sK + SG * D;       // [SG][D]
         float *sV = sQ + SG * D;       // [SG][D]
@@ -354,24 +386,21 @@ __global__ void __launch_bounds__(NT, 1)
           const int ng = a.w - t0 < SG ? a.w - t0 : SG;
           const size_t tok0 = ((size_t)b * (a.n - 1) + step) * a.w + t0;
           {
-            // all of the group's loads are issued before the first store (one memory latency)
-            constexpr int NL = SG * D / NT;
-            float lk[NL], lv[NL], lq[NL], lg[NL], la = 1.f, lb = 0.f;
-            if (tid < ng) {
-              const size_t tok = tok0 + tid;
-              la = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
-              lb = a.seam_beta[tok * H + h];
-            }
+            // the first group was loaded at the top of the step; later groups load here, all of a
+            // group's loads issued before the first store (one memory latency)
+            float lk[NL], lv[NL], lq[NL], lg[NL], la, lb;
+            if (t0 == 0) {
 #pragma unroll
-            for (int it = 0; it < NL; ++it) {
-              const int e = tid + it * NT, t = e / D, i = e % D;
-              if (t < ng) {
-                const size_t g = ((tok0 + t) * H + h) * D + i;
-                lk[it] = ld_tok<Tin>(SK, g);
-                lv[it] = ld_tok<Tin>(SV, g);
-                lq[it] = want_o ? ld_tok<Tin>(SQ, g) : 0.f;
-                lg[it] = kda ? a.seam_alpha[g] : 1.f;
+              for (int it = 0; it < NL; ++it) {
+                lk[it] = pk[it];
+                lv[it] = pv[it];
+                lq[it] = pq[it];
+                lg[it] = pg[it];
               }
+              la = pa;
+              lb = pb;
+            } else {
+              load_seam(step, t0, lk, lv, lq, lg, la, lb);
             }
 #pragma unroll
             for (int it = 0; it < NL; ++it) {

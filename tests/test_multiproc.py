@@ -93,3 +93,54 @@ def test_two_gloo_ranks_build_their_shards():
         assert np.array_equal(np.array(merged[i][0]), T)
         assert np.array_equal(np.array(merged[i][1]), S)
     assert torch.distributed.is_available()
+
+
+def _combine_worker(rank, world, port, combine_rank, out):
+    from linear_attention_state_gb300.shard import CombinePlan, combine_pairs
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    plan = CombinePlan(LENS, world, combine_rank)
+    mine = plan.segments_of(rank)
+    pairs = [_pair(i) for i in mine]
+    # [k, H = 1, d, d] per rank: this rank's segments in plan order (k may be 0)
+    T_local = torch.tensor(np.array([p[0] for p in pairs]).reshape(len(mine), 1, D, D))
+    S_local = torch.tensor(np.array([p[1] for p in pairs]).reshape(len(mine), 1, D, D))
+    T_slots = S_slots = None
+    if rank == combine_rank:
+        T_slots = torch.full((len(LENS), 1, D, D), float("nan"), dtype=torch.float64)
+        S_slots = torch.full((len(LENS), 1, D, D), float("nan"), dtype=torch.float64)
+    combine_pairs(plan, rank, T_local, S_local, T_slots, S_slots)
+    if rank == combine_rank:
+        out.put((T_slots.tolist(), S_slots.tolist(), plan.owner))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,combine_rank", [(2, 0), (3, 2)])
+def test_cold_segments_scatter_and_combine_into_slots(world, combine_rank):
+    """Cold segments built on the ranks LPT assigns them to arrive, by point-to-point transfers,
+    in the combine rank's preallocated slots in request order, bit for bit."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_combine_worker, args=(r, world, port, combine_rank, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    T_slots, S_slots, owner = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert len(set(owner)) == world  # every rank built something
+    for i in range(len(LENS)):
+        T, S = _pair(i)
+        assert np.array_equal(np.array(T_slots[i][0]), T)
+        assert np.array_equal(np.array(S_slots[i][0]), S)
+
+
+def test_combine_plan_checks():
+    from linear_attention_state_gb300.shard import CombinePlan
+    with pytest.raises(ValueError):
+        CombinePlan(LENS, 2, combine_rank=2)
+    plan = CombinePlan(LENS, 3, combine_rank=1)
+    assert sorted(i for r in range(3) for i in plan.segments_of(r)) == list(range(len(LENS)))

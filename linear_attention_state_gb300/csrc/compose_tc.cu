@@ -26,6 +26,8 @@
 // hi.T + mid.T + lo.T remain, and S_{C|0} is staged in bf16 and added in fp32.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -52,6 +54,8 @@ constexpr uint32_t SMEM_BYTES16 = OFF_S016 + 32768 + 1024;
 
 constexpr uint32_t TM_D = 0;    // accumulator D = S_new^T: lanes j, columns i
 constexpr uint32_t TM_A = 128;  // three A pieces of S^T, 64 columns each (two bf16 per column)
+constexpr uint32_t TM_DOT = 320;  // seam windows: k_t . S_j and q_t . S_j (16 columns)
+constexpr uint32_t SEAM_BT = 24576;  // seam windows: the dot products' B tile, within the S0 staging
 constexpr uint32_t TM_COLS = 512;
 
 struct ComposeTcArgs {
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(NT, 1)
     compose_tc_kernel(const __grid_constant__ CUtensorMap mapT, const __grid_constant__ CUtensorMap mapS,
                       ComposeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_t[2], bar_s, bar_m;  // bar_t[1]: second T buffer (bf16 pairs)
+  __shared__ uint64_t bar_t[2], bar_s, bar_m, bar_d;  // bar_t[1]: second T buffer (bf16 pairs)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,6 +170,7 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(&bar_t[1], 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_m, 1);
+    mbar_init(&bar_d, 1);
     mbar_fence_init();
     abort_flag = 0;
     prefetch_tmap(&mapT);
@@ -220,6 +225,9 @@ __global__ void __launch_bounds__(NT, 1)
   const Tin *SV = static_cast<const Tin *>(a.seam_v);
   const Tin *SQ = static_cast<const Tin *>(a.seam_q);
   uint32_t ph = 0;
+  uint32_t dph = 0;  // phase of bar_d (one completion per seam token group)
+  // bf16 seam tokens are exact B operands: their dot products with the state run on the tensor core
+  constexpr bool TCD = std::is_same<Tin, __nv_bfloat16>::value;
   const bool kda = a.fam == HYPIC_FAM_KDA;
   const bool want_o = a.o_out != nullptr;
   // Tokens [t0, t0 + SG) of the seam window that follows composition step `st`, this thread's share.
@@ -430,6 +438,48 @@ __global__ void __launch_bounds__(NT, 1)
             float *sGam = sM + SG * SG; // [SG]: gamma_t
             float *sF = sGam + SG;      // [SG]: D_last,s
             float *sU = sF + SG;        // [2 halves][SG][D]: partial k_t . x, then q_t . x
+            if constexpr (TCD) {
+              // u_t = k_t . S_j and p_t = q_t . S_j for every column j at once: D = S^T [K; Q]^T
+              // (M = 128 columns j, N = 16, K = 128 rows i) against the state's exact three A pieces,
+              // written to tensor memory now; B holds k_t in rows 0..7 and q_t in rows 8..15 (exact
+              // bf16, zero past the group), K-major and swizzled.  The warps form the Gram meanwhile.
+              uint8_t *bt = reinterpret_cast<uint8_t *>(sS0) + SEAM_BT;
+              {
+                const int r = tid >> 4, c = tid & 15, t = r & 7;
+                const bool isq = r >= SG;
+                float v8[8];
+                const bool live = t < ng && (!isq || want_o);
+                const float *src = (isq ? sQ : sK) + t * D + 8 * c;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v8[e] = live ? src[e] : 0.f;
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 p2 = __floats2bfloat162_rn(v8[2 * e], v8[2 * e + 1]);
+                  w4[e] = *reinterpret_cast<const uint32_t *>(&p2);
+                }
+                *reinterpret_cast<uint4 *>(bt + (c >> 3) * 2048 + sw128_offset((uint32_t)r, (uint32_t)(c & 7))) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+              write_pieces();
+              fence_proxy_async();
+              tc_fence_before();
+              __syncthreads();
+              if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id16 = idesc_f32acc(1, 1, 0, 0, 128, 16);
+                const uint32_t bb = smem_u32(bt);
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {
+#pragma unroll
+                  for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_tmem_a(tmem + TM_DOT, tmem + TM_A + (2 - pr) * 64 + kk * 8,
+                                   sdesc_sw128(bb + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), id16,
+                                   (pr | kk) != 0);
+                }
+                mma_commit(&bar_d);
+              }
+            }
             if (warp < ng) {
               // warp t: (k_t . k_s) and (q_t . k_s) for s < ng, and row t of the decay products
               const int t = warp, ln = tid & 31;
@@ -479,6 +529,37 @@ __global__ void __launch_bounds__(NT, 1)
                 }
               }
             }
+            float wv[SG];
+            if constexpr (TCD) {
+              float dd[16];
+              int got = 1;
+              if ((tid & 31) == 0) got = mbar_wait_cycles(&bar_d, dph, a.err) ? 1 : 0;
+              __syncwarp();
+              if (!__shfl_sync(0xffffffffu, got, 0)) abort_flag = 1;
+              tc_fence_after();
+              tmem_ld16(tmem + lane_base + TM_DOT, dd);
+              __syncthreads();  // the Gram's rows are complete
+#pragma unroll
+              for (int t = 0; t < SG; ++t) {
+                if (t < ng) {
+                  float acc = sB[t] * (sV[t * D + j] - sGam[t] * dd[t]);
+#pragma unroll
+                  for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sL[t * SG + s2], wv[s2], acc);
+                  wv[t] = acc;
+                }
+              }
+              if (want_o && half == 0) {
+#pragma unroll
+                for (int t = 0; t < SG; ++t) {
+                  if (t < ng) {
+                    float o = sGam[t] * dd[SG + t];
+#pragma unroll
+                    for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t * SG + s2], wv[s2], o);
+                    a.o_out[((tok0 + t) * H + h) * D + j] = o;
+                  }
+                }
+              }
+            } else {
             // partial dot products of this thread's 64 rows
             {
               float u[SG];
@@ -502,7 +583,6 @@ __global__ void __launch_bounds__(NT, 1)
                 if (t < ng) sU[(half * SG + t) * D + j] = u[t];
             }
             __syncthreads();
-            float wv[SG];
             {
               float uk[SG];
 #pragma unroll
@@ -551,6 +631,7 @@ __global__ void __launch_bounds__(NT, 1)
                   }
                 }
               }
+            }
             }
             // x <- gamma_last x + sum_s D_last,s w_s k_s
             {
@@ -625,6 +706,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
           }
           __syncthreads();  // the group's tokens are consumed
+          if (TCD && !kda) dph ^= 1u;
         }
         fence_proxy_async();  // the buffer is refilled by TMA next
         __syncthreads();
@@ -642,6 +724,7 @@ __global__ void __launch_bounds__(NT, 1)
   }
   if (abort_flag && tid == 0) {
     mbar_wait_cycles(&bar_m, ph, nullptr, 200000000LL);
+    if (TCD) mbar_wait_cycles(&bar_d, dph, nullptr, 200000000LL);
     mbar_wait_cycles(&bar_t[0], PB ? 0u : ph, nullptr, 200000000LL);
     if (PB) {
       mbar_wait_cycles(&bar_t[0], 1u, nullptr, 200000000LL);

@@ -55,6 +55,7 @@ constexpr uint32_t SMEM_BYTES16 = OFF_S016 + 32768 + 1024;
 constexpr uint32_t TM_D = 0;    // accumulator D = S_new^T: lanes j, columns i
 constexpr uint32_t TM_A = 128;  // three A pieces of S^T, 64 columns each (two bf16 per column)
 constexpr uint32_t TM_DOT = 320;  // seam windows: k_t . S_j and q_t . S_j (16 columns)
+constexpr uint32_t TM_C = 336;    // seam windows: three pieces of the update's coefficients (24 columns)
 constexpr uint32_t SEAM_BT = 24576;  // seam windows: the dot products' B tile, within the S0 staging
 constexpr uint32_t TM_COLS = 512;
 
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(NT, 1)
     compose_tc_kernel(const __grid_constant__ CUtensorMap mapT, const __grid_constant__ CUtensorMap mapS,
                       ComposeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_t[2], bar_s, bar_m, bar_d;  // bar_t[1]: second T buffer (bf16 pairs)
+  __shared__ uint64_t bar_t[2], bar_s, bar_m, bar_d, bar_u;  // bar_t[1]: second T buffer (bf16 pairs)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(&bar_s, 1);
     mbar_init(&bar_m, 1);
     mbar_init(&bar_d, 1);
+    mbar_init(&bar_u, 1);
     mbar_fence_init();
     abort_flag = 0;
     prefetch_tmap(&mapT);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(NT, 1)
   const Tin *SV = static_cast<const Tin *>(a.seam_v);
   const Tin *SQ = static_cast<const Tin *>(a.seam_q);
   uint32_t ph = 0;
-  uint32_t dph = 0;  // phase of bar_d (one completion per seam token group)
+  uint32_t dph = 0;  // phase of bar_d and bar_u (one completion each per seam token group)
   // bf16 seam tokens are exact B operands: their dot products with the state run on the tensor core
   constexpr bool TCD = std::is_same<Tin, __nv_bfloat16>::value;
   const bool kda = a.fam == HYPIC_FAM_KDA;
@@ -634,7 +636,53 @@ __global__ void __launch_bounds__(NT, 1)
             }
             }
             // x <- gamma_last x + sum_s D_last,s w_s k_s
-            {
+            if constexpr (TCD) {
+              // On the tensor core: D = C^T K over the group's tokens (K = 16, the rows past the
+              // group contribute zero), A = C^T with C_s[j] = D_last,s w_s[j] in its exact three-way
+              // split (tensor memory, written by one thread per column), B = the key rows of the dot
+              // products' B tile read as an MN-major operand (rows s, columns i).
+              const float gl = sGam[ng - 1];
+              if (half == 0) {
+                float c0[8], c1[8], c2[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const int s0 = 2 * q, s1 = 2 * q + 1;
+                  const float ca = (s0 < SG && s0 < ng) ? sF[s0] * wv[s0 < SG ? s0 : 0] : 0.f;
+                  const float cb = (s1 < SG && s1 < ng) ? sF[s1] * wv[s1 < SG ? s1 : 0] : 0.f;
+                  uint32_t w0, w1, w2;
+                  split3_pair(ca, cb, w0, w1, w2);
+                  c0[q] = __uint_as_float(w0);
+                  c1[q] = __uint_as_float(w1);
+                  c2[q] = __uint_as_float(w2);
+                }
+                tmem_st8(tmem + lane_base + TM_C, c0);
+                tmem_st8(tmem + lane_base + TM_C + 8, c1);
+                tmem_st8(tmem + lane_base + TM_C + 16, c2);
+                tmem_st_wait();
+              }
+              tc_fence_before();
+              __syncthreads();
+              if (tid == 0) {
+                tc_fence_after();
+                const uint32_t idU = idesc_f32acc(1, 1, 0, 1, 128, 128);
+                const uint64_t bK = sdesc_sw128(smem_u32(reinterpret_cast<uint8_t *>(sS0) + SEAM_BT), 2048, 1024);
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) mma_f16_tmem_a(tmem + TM_D, tmem + TM_C + (2 - pr) * 8, bK, idU, pr > 0);
+                mma_commit(&bar_u);
+              }
+              int got = 1;
+              if ((tid & 31) == 0) got = mbar_wait_cycles(&bar_u, dph, a.err) ? 1 : 0;
+              __syncwarp();
+              if (!__shfl_sync(0xffffffffu, got, 0)) abort_flag = 1;
+              tc_fence_after();
+#pragma unroll
+              for (int hb = 0; hb < R; hb += 32) {
+                float dv[32];
+                tmem_ld32(tmem + lane_base + TM_D + i0 + hb, dv);
+#pragma unroll
+                for (int r = 0; r < 32; ++r) x[hb + r] = fmaf(gl, x[hb + r], dv[r]);
+              }
+            } else {
               const float gl = sGam[ng - 1];
               float cs[SG];
 #pragma unroll
@@ -724,7 +772,10 @@ __global__ void __launch_bounds__(NT, 1)
   }
   if (abort_flag && tid == 0) {
     mbar_wait_cycles(&bar_m, ph, nullptr, 200000000LL);
-    if (TCD) mbar_wait_cycles(&bar_d, dph, nullptr, 200000000LL);
+    if (TCD) {
+      mbar_wait_cycles(&bar_d, dph, nullptr, 200000000LL);
+      mbar_wait_cycles(&bar_u, dph, nullptr, 200000000LL);
+    }
     mbar_wait_cycles(&bar_t[0], PB ? 0u : ph, nullptr, 200000000LL);
     if (PB) {
       mbar_wait_cycles(&bar_t[0], 1u, nullptr, 200000000LL);

@@ -1,0 +1,310 @@
+// Pipelined tensor-core composition over pairs stored in bf16 (delta families, d = 128, no seam
+// windows): S <- T_C S + S_{C|0} applied in prompt order (HYPIC reading notes, Method 2, paper
+// Eq. (6)), with the cached pairs in 16-bit storage (Method 3, Table 3 sizes).
+//
+// The product is the transposed one the unpipelined chain uses, D = S_new^T = S^T T^T (M = 128
+// columns j in the TMEM lanes, N = 128 rows i, K = 128), A = S^T as three exact bf16 pieces in
+// tensor memory, B = T (exact bf16) straight from its TMA tile, three products (A piece x T),
+// accumulated smallest first.  Thread (j, h) owns rows 64h .. 64h + 63 of column j: its epilogue
+// reads output rows 64h.. (N half h) and writes the A pieces of contraction half h of the next
+// step.  A step issues its products in this order:
+//     lo and mid pieces, contraction half 0     (waits for half 0's pieces of the last step)
+//     lo and mid pieces, contraction half 1     (waits for half 1's pieces)
+//     hi piece, output half 0 (N = 64)  -> commit e0
+//     hi piece, output half 1 (N = 64)  -> commit e1
+// so half 0's epilogue runs beside the last products, and the next step's first products beside
+// half 1's epilogue.  For that the accumulator and the hi piece are double buffered by step
+// parity (the lo and mid pieces are no longer read once e0 has fired): 2 x 128 + 64 + 64 + 2 x 64
+// = 512 columns.  The epilogue loads its S_{C|0} rows while it waits, and T and S_{C|0} arrive by
+// TMA two steps ahead (three buffers).  A dedicated warp issues the MMAs and the copies; the
+// epilogue threads signal it through mbarriers.
+#include <cuda_bf16.h>
+
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace hypic {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int NE = 256;       // epilogue threads: column j = tid & 127, row half h = tid >> 7
+constexpr int NTH = NE + 32;  // + the control warp (MMA issue and TMA)
+constexpr int R = 64;         // rows of a column each epilogue thread owns
+constexpr int NBUF = 3;       // T and S_{C|0} buffers
+constexpr uint32_t BUF_T = 32768;   // T: two k-blocks of [128 i][64 k] bf16, K-major, 128-byte swizzle
+constexpr uint32_t BUF_S = 32768;   // S_{C|0}: [128 i][128 j] bf16, row-major
+constexpr uint32_t OFF_T = 0, OFF_S = NBUF * BUF_T;
+constexpr uint32_t SMEM_BYTES = OFF_S + NBUF * BUF_S + 1024;
+// Tensor memory: the accumulator D and the hi piece of S^T (two buffers each, by step parity),
+// the mid and lo pieces.
+constexpr uint32_t TM_D = 0, TM_MID = 256, TM_LO = 320, TM_HI = 384, TM_COLS = 512;
+
+struct PipeArgs {
+  int H, B, n;
+  const int32_t *idx;
+  int64_t pool_size;
+  const float *S_init;
+  float *S_out;
+  int *err;
+};
+
+// Exact three-way split of two fp32 values into bf16 pieces, two per 32-bit word (hi keeps the
+// sign, the exponent and the top 7 stored bits; the remainder is exact in fp32 and is split the
+// same way; the last remainder has at most 8 significant bits, so x = hi + mid + lo exactly).
+__device__ __forceinline__ void split3(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const float ra = a - __uint_as_float(ua & 0xFFFF0000u), rb = b - __uint_as_float(ub & 0xFFFF0000u);
+  const uint32_t ura = __float_as_uint(ra), urb = __float_as_uint(rb);
+  const float la = ra - __uint_as_float(ura & 0xFFFF0000u), lb = rb - __uint_as_float(urb & 0xFFFF0000u);
+  p0 = __byte_perm(ua, ub, 0x7632);
+  p1 = __byte_perm(ura, urb, 0x7632);
+  p2 = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
+}
+
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__global__ void __launch_bounds__(NTH, 1)
+    compose_pipe_kernel(const __grid_constant__ CUtensorMap mapT, const __grid_constant__ CUtensorMap mapS,
+                        PipeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_t[NBUF], bar_s[NBUF];
+  __shared__ uint64_t bar_e[2];        // MMA commits: output half 0 done, all done
+  __shared__ uint64_t bar_a[2];        // epilogue of half h done (its A pieces written)
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = a.H, n = a.n;
+  const int b = blockIdx.x % a.B, h = blockIdx.x / a.B;  // head-major: one head's requests together
+
+  if (tid == 0) {
+    for (int i = 0; i < NBUF; ++i) {
+      mbar_init(&bar_t[i], 1);
+      mbar_init(&bar_s[i], 1);
+    }
+    mbar_init(&bar_e[0], 1);
+    mbar_init(&bar_e[1], 1);
+    mbar_init(&bar_a[0], NE / 2);
+    mbar_init(&bar_a[1], NE / 2);
+    mbar_fence_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+  const size_t base_bh = ((size_t)b * H + h) * D * D;
+  const int j = tid & (D - 1), half = (tid >> 7) & 1, i0 = half * R;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  float x[R];
+  if (tid < NE) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) x[r] = a.S_init ? a.S_init[base_bh + (size_t)(i0 + r) * D + j] : 0.f;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // This thread's rows i0 .. i0 + 63 of column j as A pieces (contraction half `half`) of the step
+  // with parity p.
+  auto write_pieces = [&](uint32_t p) {
+#pragma unroll
+    for (int c0 = 0; c0 < R; c0 += 16) {
+      uint32_t p0[8], p1[8], p2[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) split3(x[c0 + 2 * q], x[c0 + 2 * q + 1], p0[q], p1[q], p2[q]);
+      const uint32_t col = tmem + lane_base + (uint32_t)(i0 + c0) / 2;
+      st8(col + TM_HI + p * 64, p0);
+      st8(col + TM_MID, p1);
+      st8(col + TM_LO, p2);
+    }
+    tmem_st_wait();
+  };
+  if (tid < NE && n > 0) write_pieces(0);
+  tc_fence_before();
+  __syncthreads();
+
+  if (warp == NE / 32) {
+    // ---- control warp: lane 0 issues every copy and MMA -------------------------------------
+    if ((tid & 31) == 0) {
+      tc_fence_after();
+      prefetch_tmap(&mapT);
+      prefetch_tmap(&mapS);
+      int loads = 0, commits = 0;
+      auto entry = [&](int s) -> int64_t {
+        int64_t p = a.idx ? (int64_t)a.idx[(size_t)b * n + s] : (int64_t)s;
+        if (p < 0 || p >= a.pool_size) {
+          set_error(a.err, HYPIC_EDEVICE);
+          p = 0;
+        }
+        return p;
+      };
+      auto load = [&](int s) {
+        const int bs = s % NBUF;
+        const int row = (int)((entry(s) * H + h) * D);
+        mbar_arrive_expect_tx(&bar_t[bs], BUF_T);
+        tma_load_2d(sm + OFF_T + bs * BUF_T, &mapT, &bar_t[bs], 0, row);
+        tma_load_2d(sm + OFF_T + bs * BUF_T + 16384, &mapT, &bar_t[bs], 64, row);
+        mbar_arrive_expect_tx(&bar_s[bs], BUF_S);
+        tma_load_2d(sm + OFF_S + bs * BUF_S, &mapS, &bar_s[bs], 0, row);
+        ++loads;
+      };
+      const uint32_t id128 = idesc_f32acc(1, 1, 0, 0, 128, 128), id64 = idesc_f32acc(1, 1, 0, 0, 128, 64);
+      // Products of the A piece at column `pc` with T over contraction half kh (four k-blocks of
+      // 16) into D.
+      auto prod = [&](uint32_t dt, int bs, uint32_t pc, int kh, bool first) {
+        const uint32_t tb = sb + OFF_T + bs * BUF_T + kh * 16384;
+        const uint32_t ak = tmem + pc + kh * 32;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_tmem_a(dt, ak + kk * 8, sdesc_sw128(tb + kk * 32, 16, 1024), id128, (first && kk == 0) ? 0u : 1u);
+      };
+      // The hi piece's products for output half nh (rows 64 nh .. of T), both contraction halves.
+      auto prod_hi = [&](uint32_t dt, int bs, uint32_t hc, int nh) {
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+          const uint32_t tb = sb + OFF_T + bs * BUF_T + kh * 16384 + nh * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_tmem_a(dt + nh * 64, tmem + hc + kh * 32 + kk * 8, sdesc_sw128(tb + kk * 32, 16, 1024), id64, 1u);
+        }
+      };
+      bool pending = false;  // products issued since the last commit
+      for (int s = 0; s < n && s < NBUF - 1; ++s) load(s);
+      for (int s = 0; s < n; ++s) {
+        const int bs = s % NBUF;
+        const uint32_t pp = (uint32_t)(s - 1) & 1u;
+        const uint32_t dt = tmem + TM_D + (uint32_t)(s & 1) * 128;
+        bool ok = mbar_wait_cycles(&bar_t[bs], (uint32_t)(s / NBUF) & 1u, a.err);
+        if (ok && s > 0) ok = mbar_wait_cycles(&bar_a[0], pp, a.err);
+        if (!ok || abort_flag) {
+          abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t hc = TM_HI + (uint32_t)(s & 1) * 64;
+        prod(dt, bs, TM_LO, 0, true);
+        prod(dt, bs, TM_MID, 0, false);
+        pending = true;
+        if (s > 0 && !mbar_wait_cycles(&bar_a[1], pp, a.err)) {
+          abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        // step s - 1 is consumed whole: its buffers take step s + NBUF - 1
+        if (s + NBUF - 1 < n) load(s + NBUF - 1);
+        prod(dt, bs, TM_LO, 1, false);
+        prod(dt, bs, TM_MID, 1, false);
+        prod_hi(dt, bs, hc, 0);
+        mma_commit(&bar_e[0]);
+        prod_hi(dt, bs, hc, 1);
+        mma_commit(&bar_e[1]);
+        pending = false;
+        ++commits;
+      }
+      if (pending) {
+        mma_commit(&bar_e[1]);
+        ++commits;
+      }
+      // Drain (bounded): every copy issued has landed and every product has completed before the
+      // block's shared and tensor memory go away.
+      if (commits > 0) mbar_wait_cycles(&bar_e[1], (uint32_t)(commits - 1) & 1u, nullptr, 200000000LL);
+      for (int s = loads - NBUF > 0 ? loads - NBUF : 0; s < loads; ++s) {
+        mbar_wait_cycles(&bar_t[s % NBUF], (uint32_t)(s / NBUF) & 1u, nullptr, 200000000LL);
+        mbar_wait_cycles(&bar_s[s % NBUF], (uint32_t)(s / NBUF) & 1u, nullptr, 200000000LL);
+      }
+    }
+  } else {
+    // ---- epilogue threads: output half `half`, rows i0 .. i0 + 63 of column j ------------------
+    const __nv_bfloat16 *s0 = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_S) + (size_t)i0 * D + j;
+    // x = this thread's rows of S_{C|0} of step s (loaded while the products run)
+    auto load_s0 = [&](int s) -> bool {
+      int ok = 1;
+      if ((tid & 31) == 0) {
+        ok = !abort_flag && mbar_wait_cycles(&bar_s[s % NBUF], (uint32_t)(s / NBUF) & 1u, a.err);
+        if (!ok) abort_flag = 1;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      const __nv_bfloat16 *sc = s0 + (size_t)(s % NBUF) * (BUF_S / 2);
+#pragma unroll
+      for (int r = 0; r < R; ++r) x[r] = __bfloat162float(sc[(size_t)r * D]);
+      return true;
+    };
+    bool live = n > 0 ? load_s0(0) : true;
+    // bounded wait of the warp on one of the commit barriers
+    auto wait_e = [&](int k, int s) -> bool {
+      int ok = 1;
+      if ((tid & 31) == 0) {
+        ok = !abort_flag && mbar_wait_cycles(&bar_e[k], (uint32_t)s & 1u, a.err);
+        if (!ok) abort_flag = 1;
+      }
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    for (int s = 0; s < n && live; ++s) {
+      if (!wait_e(half, s)) {
+        live = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem + lane_base + TM_D + (uint32_t)(s & 1) * 128 + i0;
+#pragma unroll
+      for (int hb = 0; hb < R; hb += 32) {
+        float dv[32];
+        tmem_ld32(dt + hb, dv);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[hb + r] += dv[r];
+      }
+      if (s + 1 < n) {
+        write_pieces((uint32_t)(s + 1) & 1u);
+        fence_proxy_async();  // the S_{C|0} buffer is refilled by TMA after this arrival
+        tc_fence_before();
+        mbar_arrive(&bar_a[half]);
+        live = load_s0(s + 1);
+      }
+    }
+    if (live && !abort_flag) {
+      float *out = a.S_out + base_bh;
+#pragma unroll
+      for (int r = 0; r < R; ++r) out[(size_t)(i0 + r) * D + j] = x[r];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+}  // namespace
+
+// Pairs in bf16, no seam window and no scan: the pipelined composition above.
+cudaError_t launch_compose_pipe(const CUtensorMap &mT, const CUtensorMap &mS, int H, int B, int n,
+                                const int32_t *idx, int64_t pool_size, const float *S_init, float *S_out, int *err,
+                                cudaStream_t st) {
+  PipeArgs a{};
+  a.H = H;
+  a.B = B;
+  a.n = n;
+  a.idx = idx;
+  a.pool_size = pool_size;
+  a.S_init = S_init;
+  a.S_out = S_out;
+  a.err = err;
+  const long long blocks = (long long)B * H;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(compose_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  compose_pipe_kernel<<<(unsigned)blocks, NTH, SMEM_BYTES, st>>>(mT, mS, a);
+  return cudaGetLastError();
+}
+
+}  // namespace hypic

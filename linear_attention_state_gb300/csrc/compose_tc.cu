@@ -805,6 +805,10 @@ cudaError_t launch_one(const CUtensorMap &mT, const CUtensorMap &mS, const Compo
   return cudaGetLastError();
 }
 
+cudaError_t launch_compose_pipe(const CUtensorMap &mT, const CUtensorMap &mS, int H, int B, int n,
+                                const int32_t *idx, int64_t pool_size, const float *S_init, float *S_out, int *err,
+                                cudaStream_t st);
+
 cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
   const uint64_t rows = (uint64_t)c.pool_size * c.H * D;
   if (rows >= ((uint64_t)1 << 31)) return cudaErrorInvalidValue;
@@ -830,6 +834,8 @@ cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  if (pb && !c.scan && c.w == 0)
+    return launch_compose_pipe(mT, mS, c.H, c.B, c.n, c.idx, c.pool_size, c.S_init, c.S_out, c.err, st);
   ComposeTcArgs a{};
   a.H = c.H;
   a.B = c.B;

@@ -88,6 +88,29 @@ def test_compose_over_bf16_pool(family, d):
         assert worst <= TOL_F32, worst
 
 
+def test_long_chains_over_bf16_pool():
+    """Chains of 1, 2, 3 and 41 steps over a bf16 pool, so every load buffer and signal of the
+    pipelined composition is reused many times and the short chains end before the pipeline
+    fills, against the oracle composing the same stored values."""
+    P, H, d = 13, 2, 128
+    T, S = random_pool("delta", P, H, d, key=123)
+    T_lp, S_lp = hy.pairs_to_bf16(T, S, family="delta")
+    Th, Sh = np64(T_lp), np64(S_lp)
+    g = np.random.default_rng(7)
+    for n in (1, 2, 3, 41):
+        idx = torch.tensor(g.integers(0, P, size=(3, n)), dtype=torch.int32)
+        S_init = torch.randn((3, H, d, d), device=DEV, generator=W.generator(DEV, 46, n))
+        out = hy.compose(T_lp, S_lp, idx.to(DEV), S_init=S_init, family="delta")
+        assert hy.stream_status() == 0
+        worst = 0.0
+        for b in range(3):
+            for h in range(H):
+                ids = idx[b].tolist()
+                ref = oracle.compose("delta", Th[ids, h].reshape(n, -1), Sh[ids, h], S_init=np64(S_init[b, h]))
+                worst = max(worst, relerr(np64(out[b, h]), ref))
+        assert worst <= TOL_F32, (n, worst)
+
+
 def test_bf16_pool_differs_from_fp32_pool_by_the_storage_rounding():
     """Composing the rounded pool differs from composing the fp32 pool by the storage rounding
     (about 2^-9 relative per stored value), not by anything larger."""

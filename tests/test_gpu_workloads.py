@@ -178,6 +178,29 @@ def test_compose_full_size_random_pairs():
     assert worst <= TOL_F32
 
 
+def test_compose_full_size_bf16_pool():
+    """The bench's bf16-pool launch: 30 x 32 heads, pool of 256 pairs stored in bf16, 64 requests x
+    16; sampled chains against the oracle composing the same stored values."""
+    pw = W.COMPOSE_POOL
+    pool_T, pool_S = W.random_pairs(pw.pool, pw.H, pw.d, DEV, key=17)
+    T_lp, S_lp = hy.pairs_to_bf16(pool_T, pool_S, family="gated_delta")
+    del pool_T, pool_S
+    idx = pw.request_indices(DEV)
+    out = hy.compose(T_lp, S_lp, idx, family="gated_delta")
+    assert hy.stream_status() == 0
+    g = np.random.default_rng(6)
+    worst = 0.0
+    idx_h = idx.cpu()
+    for _ in range(12):
+        b, h = int(g.integers(pw.B)), int(g.integers(pw.H))
+        ids = idx_h[b].tolist()
+        ref = oracle.compose("gated_delta", np64(T_lp[ids, h]).reshape(pw.n, -1), np64(S_lp[ids, h]))
+        worst = max(worst, relerr(np64(out[b, h]), ref))
+    print(f"compose full size bf16 pool: {worst:.2e}")
+    del T_lp, S_lp
+    assert worst <= TOL_F32
+
+
 def test_long_mixed_full_size_sampled_heads():
     """30 x 32 heads, 128 segments x 1024 tokens, 96 cached + 32 cold, w = 8 on every inner segment."""
     w = W.LONG_MIXED

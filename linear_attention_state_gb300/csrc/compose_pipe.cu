@@ -283,6 +283,277 @@ __global__ void __launch_bounds__(NTH, 1)
   }
 }
 
+// ---- fp32 pairs: compose and the affine scan -------------------------------------------------
+// With fp32 pairs T is not an exact bf16 operand: each step splits it into three exact bf16
+// B pieces (hi, mid, lo), and the product takes the six terms (A piece a, B piece b) with
+// a + b <= 2, smallest first.  The 256 epilogue threads also split T: warp w takes rows
+// w, w + 8, .., lane l columns 4l .. 4l + 3 (one coalesced 512-byte row per warp and load), and
+// they split the next step's T while this step's products run, into the other of two B buffers
+// (2 x 96 KB of shared memory).  S_{C|0} comes straight from global memory into the registers
+// of the thread that adds it, loaded while the products run.  A step issues
+//     the five smaller terms over contraction half 0   (waits for half 0's A pieces)
+//     the five smaller terms over contraction half 1   (waits for half 1's A pieces)
+//     hi.hi, output half 0 (N = 64)  -> commit e0
+//     hi.hi, output half 1 (N = 64)  -> commit e1, and the step's B buffer is free
+// as the bf16-pair kernel does.  In scan mode (one block per head and column half of the
+// augmented state [T | S], as the unpipelined chain has it) every step's state is written out.
+constexpr uint32_t BUF_B = 3 * 32768;          // B pieces of one T: hi, mid, lo x two k-blocks
+constexpr uint32_t SMEM32 = 2 * BUF_B + 1024;  // two buffers by step parity
+
+struct Pipe32Args {
+  int H, B, n;
+  const int32_t *idx;
+  int64_t pool_size;
+  const float *pool_T, *pool_S;
+  const float *S_init;
+  float *S_out;
+  int scan;
+  float *T_rec, *S_rec;
+  int *err;
+};
+
+__global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_b[2];  // the B pieces of the step with this parity are written
+  __shared__ uint64_t bar_f[2];  // the products of the step with this parity are done
+  __shared__ uint64_t bar_e[2];  // MMA commits: output half 0 done, all done
+  __shared__ uint64_t bar_a[2];  // epilogue of half h done (its A pieces written)
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = a.H, n = a.n;
+  int b, h;
+  bool isT = false;  // scan: the T half (starts at I, no addend)
+  if (a.scan) {
+    isT = (blockIdx.x & 1) == 0;
+    h = blockIdx.x >> 1;
+    b = 0;
+  } else {
+    b = blockIdx.x % a.B;
+    h = blockIdx.x / a.B;
+  }
+  const bool addend = !isT;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_b[i], NE);
+      mbar_init(&bar_f[i], 1);
+      mbar_init(&bar_e[i], 1);
+      mbar_init(&bar_a[i], NE / 2);
+    }
+    mbar_fence_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+  const size_t base_bh = ((size_t)b * H + h) * D * D;
+  const int j = tid & (D - 1), half = (tid >> 7) & 1, i0 = half * R;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  float x[R];
+  if (tid < NE) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int i = i0 + r;
+      if (a.scan) x[r] = (isT && i == j) ? 1.f : 0.f;
+      else x[r] = a.S_init ? a.S_init[base_bh + (size_t)i * D + j] : 0.f;
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  auto entry = [&](int s) -> int64_t {
+    int64_t p = a.idx ? (int64_t)a.idx[(size_t)b * n + s] : (int64_t)s;
+    if (p < 0 || p >= a.pool_size) {
+      set_error(a.err, HYPIC_EDEVICE);
+      p = 0;
+    }
+    return p;
+  };
+
+  if (warp == NE / 32) {
+    // ---- control warp: lane 0 issues every MMA ------------------------------------------------
+    if ((tid & 31) == 0) {
+      tc_fence_after();
+      int commits = 0;
+      const uint32_t id128 = idesc_f32acc(1, 1, 0, 0, 128, 128), id64 = idesc_f32acc(1, 1, 0, 0, 128, 64);
+      bool pending = false;
+      for (int s = 0; s < n; ++s) {
+        const int bb = s & 1;
+        const uint32_t pp = (uint32_t)(s - 1) & 1u;
+        const uint32_t dt = tmem + TM_D + (uint32_t)bb * 128;
+        const uint32_t ac[3] = {tmem + TM_HI + (uint32_t)bb * 64, tmem + TM_MID, tmem + TM_LO};
+        const uint32_t bt = sb + (uint32_t)bb * BUF_B;
+        bool ok = mbar_wait_cycles(&bar_b[bb], (uint32_t)(s >> 1) & 1u, a.err);
+        if (ok && s > 0) ok = mbar_wait_cycles(&bar_a[0], pp, a.err);
+        if (!ok || abort_flag) {
+          abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        // the five smaller terms (A piece pa, B piece pb), smallest first
+        const int pa[5] = {2, 1, 0, 1, 0}, pb[5] = {0, 1, 2, 0, 1};
+#pragma unroll 1
+        for (int kh = 0; kh < 2; ++kh) {
+          if (kh == 1) {
+            if (s > 0 && !mbar_wait_cycles(&bar_a[1], pp, a.err)) {
+              abort_flag = 1;
+              break;
+            }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int t = 0; t < 5; ++t) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_tmem_a(dt, ac[pa[t]] + kh * 32 + kk * 8,
+                             sdesc_sw128(bt + pb[t] * 32768 + kh * 16384 + kk * 32, 16, 1024), id128,
+                             (kh | t | kk) != 0);
+          }
+          pending = true;
+        }
+        if (abort_flag) break;
+        // hi.hi by output half
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_tmem_a(dt + nh * 64, ac[0] + kh * 32 + kk * 8,
+                             sdesc_sw128(bt + kh * 16384 + nh * 8192 + kk * 32, 16, 1024), id64, 1u);
+          }
+          mma_commit(&bar_e[nh]);
+        }
+        mma_commit(&bar_f[bb]);
+        pending = false;
+        ++commits;
+      }
+      if (pending) {
+        mma_commit(&bar_e[1]);
+        ++commits;
+      }
+      if (commits > 0) mbar_wait_cycles(&bar_e[1], (uint32_t)(commits - 1) & 1u, nullptr, 200000000LL);
+    }
+  } else {
+    // ---- epilogue and split threads -------------------------------------------------------------
+    // This thread's rows i0 .. i0 + 63 of column j as A pieces (contraction half `half`) of the
+    // step with parity p.
+    auto write_pieces = [&](uint32_t p) {
+#pragma unroll
+      for (int c0 = 0; c0 < R; c0 += 16) {
+        uint32_t p0[8], p1[8], p2[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) split3(x[c0 + 2 * q], x[c0 + 2 * q + 1], p0[q], p1[q], p2[q]);
+        const uint32_t col = tmem + lane_base + (uint32_t)(i0 + c0) / 2;
+        st8(col + TM_HI + p * 64, p0);
+        st8(col + TM_MID, p1);
+        st8(col + TM_LO, p2);
+      }
+      tmem_st_wait();
+    };
+    // T of step s as three B pieces in buffer s & 1 (K-major [128 i][64 k] blocks, 128-byte
+    // swizzle): warp w, rows w + 8 r; lane l, columns 4l .. 4l + 3.
+    auto split_T = [&](int s) {
+      const float *Tg = a.pool_T + ((size_t)entry(s) * H + h) * D * D;
+      uint8_t *bt = sm + (size_t)(s & 1) * BUF_B;
+      const int l = tid & 31;
+      const uint32_t kb = (uint32_t)l >> 4, chunk = ((uint32_t)l & 15u) >> 1, sub = ((uint32_t)l & 1u) * 8u;
+      float4 v[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) v[r] = reinterpret_cast<const float4 *>(Tg + (size_t)(warp + 8 * r) * D)[l];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        uint32_t p0a, p1a, p2a, p0b, p1b, p2b;
+        split3(v[r].x, v[r].y, p0a, p1a, p2a);
+        split3(v[r].z, v[r].w, p0b, p1b, p2b);
+        const uint32_t off = kb * 16384u + sw128_offset((uint32_t)(warp + 8 * r), chunk) + sub;
+        *reinterpret_cast<uint2 *>(bt + off) = make_uint2(p0a, p0b);
+        *reinterpret_cast<uint2 *>(bt + 32768 + off) = make_uint2(p1a, p1b);
+        *reinterpret_cast<uint2 *>(bt + 65536 + off) = make_uint2(p2a, p2b);
+      }
+      fence_proxy_async();  // the pieces are read by the MMAs
+    };
+    // x = this thread's rows of S_{C|0} of step s (or zero in the T half of a scan)
+    auto load_s0 = [&](int s) {
+      if (addend) {
+        const float *Sg = a.pool_S + ((size_t)entry(s) * H + h) * D * D + (size_t)i0 * D + j;
+#pragma unroll
+        for (int r = 0; r < R; ++r) x[r] = Sg[(size_t)r * D];
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) x[r] = 0.f;
+      }
+    };
+    auto wait_warp = [&](uint64_t *bar, uint32_t parity) -> bool {
+      int ok = 1;
+      if ((tid & 31) == 0) {
+        ok = !abort_flag && mbar_wait_cycles(bar, parity, a.err);
+        if (!ok) abort_flag = 1;
+      }
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    bool live = true;
+    if (n > 0) {
+      write_pieces(0);
+      split_T(0);
+      tc_fence_before();
+      mbar_arrive(&bar_b[0]);
+      load_s0(0);
+    }
+    for (int s = 0; s < n && live; ++s) {
+      if (s + 1 < n) {
+        // the other B buffer was last read by the products of step s - 1
+        if (s >= 1 && !wait_warp(&bar_f[(s + 1) & 1], (uint32_t)((s - 1) >> 1) & 1u)) {
+          live = false;
+          break;
+        }
+        split_T(s + 1);
+        mbar_arrive(&bar_b[(s + 1) & 1]);
+      }
+      if (!wait_warp(&bar_e[half], (uint32_t)s & 1u)) {
+        live = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem + lane_base + TM_D + (uint32_t)(s & 1) * 128 + i0;
+#pragma unroll
+      for (int hb = 0; hb < R; hb += 32) {
+        float dv[32];
+        tmem_ld32(dt + hb, dv);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[hb + r] += dv[r];
+      }
+      if (a.scan) {
+        float *rec = (isT ? a.T_rec : a.S_rec) + ((size_t)s * H + h) * D * D + (size_t)i0 * D + j;
+#pragma unroll
+        for (int r = 0; r < R; ++r) rec[(size_t)r * D] = x[r];
+      }
+      if (s + 1 < n) {
+        write_pieces((uint32_t)(s + 1) & 1u);
+        tc_fence_before();
+        mbar_arrive(&bar_a[half]);
+        load_s0(s + 1);
+      }
+    }
+    if (live && !abort_flag && !a.scan) {
+      float *out = a.S_out + base_bh;
+#pragma unroll
+      for (int r = 0; r < R; ++r) out[(size_t)(i0 + r) * D + j] = x[r];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
 }  // namespace
 
 // Pairs in bf16, no seam window and no scan: the pipelined composition above.
@@ -304,6 +575,35 @@ cudaError_t launch_compose_pipe(const CUtensorMap &mT, const CUtensorMap &mS, in
   cudaError_t e = cudaFuncSetAttribute(compose_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   compose_pipe_kernel<<<(unsigned)blocks, NTH, SMEM_BYTES, st>>>(mT, mS, a);
+  return cudaGetLastError();
+}
+
+// Pairs in fp32, no seam window: the pipelined composition or, with scan set, the affine scan
+// (T_rec and S_rec receive every prefix).
+cudaError_t launch_compose_pipe32(int H, int B, int n, const int32_t *idx, int64_t pool_size, const float *pool_T,
+                                  const float *pool_S, const float *S_init, float *S_out, int scan, float *T_rec,
+                                  float *S_rec, int *err, cudaStream_t st) {
+  Pipe32Args a{};
+  a.H = H;
+  a.B = B;
+  a.n = n;
+  a.idx = idx;
+  a.pool_size = pool_size;
+  a.pool_T = pool_T;
+  a.pool_S = pool_S;
+  a.S_init = S_init;
+  a.S_out = S_out;
+  a.scan = scan;
+  a.T_rec = T_rec;
+  a.S_rec = S_rec;
+  a.err = err;
+  const long long blocks = scan ? (long long)H * 2 : (long long)B * H;
+  if (blocks <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(pool_T) & 15) != 0) return cudaErrorInvalidValue;  // rows read as float4
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(compose_pipe32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM32);
+  if (e != cudaSuccess) return e;
+  compose_pipe32_kernel<<<(unsigned)blocks, NTH, SMEM32, st>>>(a);
   return cudaGetLastError();
 }
 

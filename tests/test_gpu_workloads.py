@@ -201,6 +201,23 @@ def test_compose_full_size_bf16_pool():
     assert worst <= TOL_F32
 
 
+def test_affine_scan_full_size_sampled_heads():
+    """The bench's scan launch: 64 fp32 pairs x 960 heads; every prefix of sampled heads against the
+    oracle."""
+    n, H, d = 64, 960, 128
+    T, S = W.random_pairs(n, H, d, DEV, key=11)
+    Tp, Sp = hy.affine_scan(T, S, family="gated_delta")
+    assert hy.stream_status() == 0
+    worst = 0.0
+    for h in (0, 1, 479, 959):
+        Tr, Sr = oracle.affine_scan("gated_delta", np64(T[:, h]).reshape(n, -1), np64(S[:, h]))
+        for i in range(n):
+            worst = max(worst, relerr(np64(Tp[i, h]), Tr[i].reshape(d, d)), relerr(np64(Sp[i, h]), Sr[i]))
+    print(f"affine scan full size: {worst:.2e}")
+    del T, S, Tp, Sp
+    assert worst <= TOL_F32
+
+
 def test_long_mixed_full_size_sampled_heads():
     """30 x 32 heads, 128 segments x 1024 tokens, 96 cached + 32 cold, w = 8 on every inner segment."""
     w = W.LONG_MIXED

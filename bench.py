@@ -16,6 +16,7 @@ independent request (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import functools
 import json
 import os
 import statistics
@@ -58,15 +59,17 @@ TRAFFIC = {
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
     "decay_kda": {"bytes": 3_970_323_882, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9bf23969ba4a",
                   "commit": "edc1dcb"},
-    # compose_tc_kernel on the warm-cache workload (fp32 and bf16 pools): captured at 4 layers
-    # (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each head's pool entries
-    # and requests are independent, the grid head-major)
-    "compose_f32": {"bytes": 46_900_577_280, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b",
-                    "commit": "edc1dcb"},
-    "compose_bf16": {"bytes": 20_228_006_400, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b",
-                     "commit": "edc1dcb"},
-    # compose_tc_kernel in scan mode, 64 pairs x 960 heads
-    "scan": {"bytes": 16_477_868_032, "src": ("compose_tc.cu", "tc_ptx.cuh"), "digest": "a0c842cc4b9b", "commit": "36258c6"},
+    # compose_pipe32_kernel / compose_pipe_kernel on the warm-cache workload (fp32 and bf16 pools):
+    # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each
+    # head's pool entries and requests are independent, the grid head-major)
+    "compose_f32": {"bytes": 46_612_121_600, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"),
+                    "digest": "1492692e731a", "commit": "1234e70"},
+    "compose_bf16": {"bytes": 19_925_423_360, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"),
+                     "digest": "1492692e731a", "commit": "1234e70"},
+    # compose_pipe32_kernel in scan mode, 64 pairs: captured at 128 heads (--scan-heads 128) and
+    # scaled by 7.5 to 960 heads
+    "scan": {"bytes": 15_815_274_880, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"), "digest": "1492692e731a",
+             "commit": "1234e70"},
     # staged RoPE shift and state re-rotation
     "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",
                                     "commit": "ae9cc2f"},
@@ -408,13 +411,14 @@ def decay_build_measure(steps, warmup, dev, peaks):
     return out
 
 
-def scan_measure(steps, warmup, dev, peaks):
-    """Affine scan of 64 pairs per head over 960 heads (d = 128, fp32): prefix pairs/s."""
+def scan_measure(steps, warmup, dev, peaks, heads=None):
+    """Affine scan of 64 pairs per head over 960 heads (d = 128, fp32): prefix pairs/s.  `heads`
+    runs a reduced case (fewer heads, same per-head work) for counter captures."""
     import torch
 
     import linear_attention_state_gb300 as hy
     import workloads as W
-    n, H, d = 64, 960, 128
+    n, H, d = 64, heads or 960, 128
     T, S = W.random_pairs(n, H, d, dev, key=11)
 
     def fn(ev):
@@ -860,6 +864,8 @@ def main():
                     help="pair storage of the composition measurement (fp32, bf16 or both)")
     ap.add_argument("--decay-only", action="store_true",
                     help="time only the decay-family builds (profiling aid; prints its own line)")
+    ap.add_argument("--scan-heads", type=int, default=None,
+                    help="heads of the scan measurement (default 960; fewer for counter captures)")
     ap.add_argument("--scan-only", action="store_true",
                     help="time only the affine scan (profiling aid; prints its own line)")
     ap.add_argument("--boundary-only", action="store_true",
@@ -910,7 +916,7 @@ def main():
         return
     if args.decay_only or args.scan_only or args.boundary_only or args.outputs_only:
         fn, what = ((decay_build_measure, "decay-family builds") if args.decay_only else
-                    (scan_measure, "affine scan") if args.scan_only else
+                    (functools.partial(scan_measure, heads=args.scan_heads), "affine scan") if args.scan_only else
                     (build_outputs_measure, "build with outputs") if args.outputs_only else
                     (boundary_measure, "boundary patches"))
         res = fn(args.steps, args.warmup, dev, peaks)

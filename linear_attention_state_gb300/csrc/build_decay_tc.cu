@@ -13,10 +13,13 @@
 // The kernel is persistent (one CTA per SM, units dealt round-robin) and warp-specialised,
 // so the chunk stream through shared memory never stops at a unit boundary:
 //   warp 8  (producer)  TMA: K, V (and the diagonal family's gates) into NS stages;
-//   warps 0-3 (convert) suffix factors in fp32 (diagonal: one thread per key channel scans
-//                       down the chunk in place over the gate tile; scalar: a warp scan), then
-//                       Khat = f * k split into bf16 hi (over K) + lo (over the gate tile or
-//                       its own slot); V is exact in bf16; T_C at the end of each unit;
+//   warps 0-3 (convert) diagonal: suffix factors in fp32 (one thread per key channel scans down
+//                       the chunk in place over the gate tile), then Khat = f * k split into
+//                       bf16 hi (over K) + lo (over the gate tile); T_C at the end of each unit.
+//                       Scalar: Khat^T = (f * k)^T split hi + lo into tensor memory, with the
+//                       factors from warp 10;
+//   warp 10 (scalar)    the chunk's suffix factors (a warp scan over the gates), one chunk ahead
+//                       of the converters (double buffered), and T_C at the end of each unit;
 //   warp 9  (MMA)       S += Khat_hi^T V + Khat_lo^T V (M = N = 128, K = 64 per chunk) into
 //                       one of two TMEM accumulators, alternating per unit;
 //   warps 4-7 (store)   accumulator -> registers -> padded shared rows -> whole-line stores,
@@ -40,7 +43,6 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NT = 320;
 constexpr uint32_t BAR_CONV = 1, BAR_EPI = 2;
 
 // Stage layout (1024-aligned): K / Khat hi [2 boxes of 64 t x 64 i, SW128] at 0, V at 16384,
@@ -49,6 +51,7 @@ constexpr uint32_t BAR_CONV = 1, BAR_EPI = 2;
 // is the 32 KB of K and V and six stages fit.  After the stages: the store's row buffer.
 template <bool DIAG>
 struct Cfg {
+  static constexpr int NT = DIAG ? 320 : 352;  // the scalar families add the factor warp
   static constexpr uint32_t STAGE = DIAG ? 65536u : 32768u;
   static constexpr int NS = DIAG ? 3 : 6;
   static constexpr uint32_t TX = DIAG ? 65536u : 32768u;
@@ -111,7 +114,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 }
 
 template <bool DIAG>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(Cfg<DIAG>::NT, 1)
     build_decay_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                           const __grid_constant__ CUtensorMap mapA, DecayArgs a) {
   using G = Cfg<DIAG>;
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(NT, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[NS], bar_conv[NS], bar_empty[NS], bar_acc_full[2], bar_acc_empty[2];
   __shared__ uint64_t bar_kfree[KB];  // scalar families: the MMAs have read a Khat buffer
+  __shared__ uint64_t bar_fac_full[2], bar_fac_empty[2];  // scalar families: factors written / read
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ float s_f[2][C];  // scalar families: factors of the current chunk (double buffered)
@@ -138,6 +142,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&bar_acc_empty[i], 128);
     }
     for (int i = 0; i < KB; ++i) mbar_init(&bar_kfree[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_fac_full[i], 32);
+      mbar_init(&bar_fac_empty[i], 128);
+    }
     mbar_fence_init();
     abort_flag = 0;
   }
@@ -226,152 +234,177 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ---------------- converters (tid = key channel) ----------------
+  } else if (!DIAG && warp < 4) {
+    // ---------------- scalar converters (tid = key channel) ----------------
+    // Khat^T row i = f_t k_ti over the chunk's tokens, hi and lo pieces into tensor memory (lane i,
+    // token pairs per column) once the MMAs of chunk j - KB have read the buffer.  No block-wide
+    // barrier: every wait is the thread's own, so a role that stops leaves no one at a barrier.
     int j = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    bool stop = false;
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
       const Unit U = unit_of(a, u);
       if (!U.ok) {
         if (tid == 0) set_error(a.err, HYPIC_EDEVICE);
         continue;
       }
-      float carry = 1.f;  // product of the gates passed: channel tid (diagonal) or the head's
-      float gc = 1.f;     // scalar_const: the head's gate
-      if (!DIAG && a.fam == HYPIC_FAM_SCALAR_CONST) gc = a.alpha[U.h];
-      bool stop = false;
       for (int q = 0; q < U.nch; ++q, ++j) {
-        const int st = j % NS;
-        uint8_t *base = sm + st * G::STAGE;
-        const int64_t t0 = U.beg + (int64_t)(U.nch - 1 - q) * C;
-        const int nvalid = (int)((U.end - t0) < C ? (U.end - t0) : C);
-        const bool ok = wait_or_abort(&bar_full[st], (uint32_t)((j / NS) & 1), &abort_flag, a.err);
-        if (bar_or_named(BAR_CONV, 128, !ok)) {
+        const int st = j % NS, fb = j & 1, buf = j % KB;
+        const uint8_t *base = sm + st * G::STAGE;
+        if (!wait_or_abort(&bar_full[st], (uint32_t)((j / NS) & 1), &abort_flag, a.err) ||
+            !wait_or_abort(&bar_fac_full[fb], (uint32_t)((j >> 1) & 1), &abort_flag, a.err) ||
+            (j >= KB && !wait_or_abort(&bar_kfree[buf], (uint32_t)((j / KB - 1) & 1), &abort_flag, a.err))) {
           stop = true;
           break;
         }
-        // (1) suffix factors
-        if (DIAG) {
-          float *g = reinterpret_cast<float *>(base + OFF_G);
-          float acc = carry;
-#pragma unroll 8
-          for (int t = C - 1; t >= 0; --t) {
-            const float gv = g[t * D + tid];
-            const bool v = t < nvalid;
-            g[t * D + tid] = v ? acc : 0.f;
-            acc = v ? acc * gv : acc;
-          }
-          carry = acc;
-        } else if (warp == 0) {
-          // lane l owns tokens 2l and 2l + 1
-          const int ta = 2 * lane, tb = 2 * lane + 1;
-          float g0 = 1.f, g1 = 1.f;
-          if (a.fam == HYPIC_FAM_SCALAR_CONST) {
-            g0 = ta < nvalid ? gc : 1.f;
-            g1 = tb < nvalid ? gc : 1.f;
-          } else {
-            if (ta < nvalid) g0 = a.alpha[(t0 + ta) * a.H + U.h];
-            if (tb < nvalid) g1 = a.alpha[(t0 + tb) * a.H + U.h];
-          }
-          float suf = g0 * g1;  // inclusive suffix product over lanes >= lane
+        tc_fence_after();
+        const int i = tid;
+        const uint8_t *kcol = base + (uint32_t)(i >> 6) * 8192u + (uint32_t)(i & 7) * 2u;
+        const uint32_t ck = (uint32_t)((i & 63) >> 3);
+        const float *ft = s_f[fb];
+        float hw[32], lw[32];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_down_sync(0xffffffffu, suf, o);
-            if (lane + o < 32) suf *= y;
-          }
-          float after = __shfl_down_sync(0xffffffffu, suf, 1);
-          if (lane == 31) after = 1.f;
-          const float total = __shfl_sync(0xffffffffu, suf, 0);
-          s_f[j & 1][tb] = tb < nvalid ? carry * after : 0.f;
-          s_f[j & 1][ta] = ta < nvalid ? carry * after * g1 : 0.f;
-          carry *= total;
+        for (int t = 0; t < C; t += 2) {
+          const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t, ck)));
+          const float k1 =
+              __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t + 1, ck)));
+          const float x0 = ft[t] * k0, x1 = ft[t + 1] * k1;
+          const __nv_bfloat162 hp = __floats2bfloat162_rn(x0, x1);
+          const float2 hf = __bfloat1622float2(hp);
+          const __nv_bfloat162 lp = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+          hw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
+          lw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
         }
-        bar_sync_named(BAR_CONV, 128);
-
-        if constexpr (!DIAG) {
-          // (2) Khat^T row i = f_t k_ti over the chunk's tokens, hi and lo pieces into tensor
-          // memory (lane i, token pairs per column) once the MMAs of chunk j - KB have read the buffer.
-          const int buf = j % KB;
-          const bool kfree = j < KB || wait_or_abort(&bar_kfree[buf], (uint32_t)((j / KB - 1) & 1), &abort_flag, a.err);
-          if (bar_or_named(BAR_CONV, 128, !kfree)) {  // one decision for all converters
+        mbar_arrive(&bar_fac_empty[fb]);  // the factors are in registers
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64, hw);
+        tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64 + 32, lw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_conv[st]);
+      }
+    }
+  } else if (!DIAG && warp == 10) {
+    // ---------------- scalar factors, one chunk ahead of the converters ----------------
+    // f_t = product of the gates after token t within the segment (0 past its end); lane l owns
+    // tokens 2l and 2l + 1 of the chunk.
+    int j = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      const Unit U = unit_of(a, u);
+      if (!U.ok) continue;
+      float carry = 1.f;  // product of the gates of the chunks already passed
+      const float gc = a.fam == HYPIC_FAM_SCALAR_CONST ? a.alpha[U.h] : 1.f;
+      for (int q = 0; q < U.nch; ++q, ++j) {
+        const int fb = j & 1;
+        if (j >= 2 && !wait_or_abort(&bar_fac_empty[fb], (uint32_t)(((j >> 1) - 1) & 1), &abort_flag, a.err)) {
+          stop = true;
+          break;
+        }
+        const int64_t t0 = U.beg + (int64_t)(U.nch - 1 - q) * C;
+        const int nvalid = (int)((U.end - t0) < C ? (U.end - t0) : C);
+        const int ta = 2 * lane, tb = 2 * lane + 1;
+        float g0 = 1.f, g1 = 1.f;
+        if (a.fam == HYPIC_FAM_SCALAR_CONST) {
+          g0 = ta < nvalid ? gc : 1.f;
+          g1 = tb < nvalid ? gc : 1.f;
+        } else {
+          if (ta < nvalid) g0 = a.alpha[(t0 + ta) * a.H + U.h];
+          if (tb < nvalid) g1 = a.alpha[(t0 + tb) * a.H + U.h];
+        }
+        float suf = g0 * g1;  // inclusive suffix product over lanes >= lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_down_sync(0xffffffffu, suf, o);
+          if (lane + o < 32) suf *= y;
+        }
+        float after = __shfl_down_sync(0xffffffffu, suf, 1);
+        if (lane == 31) after = 1.f;
+        const float total = __shfl_sync(0xffffffffu, suf, 0);
+        s_f[fb][tb] = tb < nvalid ? carry * after : 0.f;
+        s_f[fb][ta] = ta < nvalid ? carry * after * g1 : 0.f;
+        carry *= total;
+        mbar_arrive(&bar_fac_full[fb]);
+      }
+      if (!stop && lane == 0) a.T_out[(size_t)U.s * a.H + U.h] = carry;
+    }
+  } else if (warp < 4) {
+    // ---------------- diagonal converters (tid = key channel) ----------------
+    if constexpr (DIAG) {
+      int j = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(a, u);
+        if (!U.ok) {
+          if (tid == 0) set_error(a.err, HYPIC_EDEVICE);
+          continue;
+        }
+        float carry = 1.f;  // product of the gates passed, channel tid
+        bool stop = false;
+        for (int q = 0; q < U.nch; ++q, ++j) {
+          const int st = j % NS;
+          uint8_t *base = sm + st * G::STAGE;
+          const int64_t t0 = U.beg + (int64_t)(U.nch - 1 - q) * C;
+          const int nvalid = (int)((U.end - t0) < C ? (U.end - t0) : C);
+          const bool ok = wait_or_abort(&bar_full[st], (uint32_t)((j / NS) & 1), &abort_flag, a.err);
+          if (bar_or_named(BAR_CONV, 128, !ok)) {
             stop = true;
             break;
           }
-          tc_fence_after();
-          const int i = tid;
-          const uint8_t *kcol = base + (uint32_t)(i >> 6) * 8192u + (uint32_t)(i & 7) * 2u;
-          const uint32_t ck = (uint32_t)((i & 63) >> 3);
-          const float *ft = s_f[j & 1];
-          float hw[32], lw[32];
-#pragma unroll
-          for (int t = 0; t < C; t += 2) {
-            const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t, ck)));
-            const float k1 =
-                __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kcol + sw128_offset((uint32_t)t + 1, ck)));
-            const float x0 = ft[t] * k0, x1 = ft[t + 1] * k1;
-            const __nv_bfloat162 hp = __floats2bfloat162_rn(x0, x1);
-            const float2 hf = __bfloat1622float2(hp);
-            const __nv_bfloat162 lp = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-            hw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hp));
-            lw[t / 2] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&lp));
+          // (1) suffix factors, in place over the gate tile
+          {
+            float *g = reinterpret_cast<float *>(base + OFF_G);
+            float acc = carry;
+#pragma unroll 8
+            for (int t = C - 1; t >= 0; --t) {
+              const float gv = g[t * D + tid];
+              const bool v = t < nvalid;
+              g[t * D + tid] = v ? acc : 0.f;
+              acc = v ? acc * gv : acc;
+            }
+            carry = acc;
           }
-          const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-          tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64, hw);
-          tmem_st32(tmem + lane_base + TM_KH + (uint32_t)buf * 64 + 32, lw);
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&bar_conv[st]);
-          continue;
-        }
-        // (2) Khat = f * k: hi over K in place, lo into the lo slot.  On the diagonal path the
-        // lo slot overlaps the factor tile, so all factors are read before any lo is written.
-        uint32_t lo_w[8][4];
+          bar_sync_named(BAR_CONV, 128);
+          // (2) Khat = f * k: hi over K in place, lo into the lo slot.  The lo slot overlaps the
+          // factor tile, so all factors are read before any lo is written.
+          uint32_t lo_w[8][4];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int e = tid + r * 128;
-          const int t = e >> 4, c8 = e & 15;  // token t, key channels 8 c8 .. 8 c8 + 7
-          const uint32_t off = (uint32_t)(c8 >> 3) * 8192 + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
-          const uint4 kr = *reinterpret_cast<const uint4 *>(base + off);
-          const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
-          float f[8];
-          if (DIAG) {
+          for (int r = 0; r < 8; ++r) {
+            const int e = tid + r * 128;
+            const int t = e >> 4, c8 = e & 15;  // token t, key channels 8 c8 .. 8 c8 + 7
+            const uint32_t off = (uint32_t)(c8 >> 3) * 8192 + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
+            const uint4 kr = *reinterpret_cast<const uint4 *>(base + off);
+            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
             const float *fp = reinterpret_cast<const float *>(base + OFF_G) + t * D + 8 * c8;
             const float4 f0 = *reinterpret_cast<const float4 *>(fp);
             const float4 f1 = *reinterpret_cast<const float4 *>(fp + 4);
-            f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
-            f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
-          } else {
-            const float ft = s_f[j & 1][t];
+            const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            uint32_t hi[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = ft;
+            for (int i = 0; i < 4; ++i) {
+              const float2 kv = __bfloat1622float2(k2[i]);
+              const float x0 = kv.x * f[2 * i], x1 = kv.y * f[2 * i + 1];
+              const __nv_bfloat162 hp = __floats2bfloat162_rn(x0, x1);
+              const float2 hf = __bfloat1622float2(hp);
+              const __nv_bfloat162 lp = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+              hi[i] = *reinterpret_cast<const uint32_t *>(&hp);
+              lo_w[r][i] = *reinterpret_cast<const uint32_t *>(&lp);
+            }
+            *reinterpret_cast<uint4 *>(base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           }
-          uint32_t hi[4];
+          bar_sync_named(BAR_CONV, 128);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 kv = __bfloat1622float2(k2[i]);
-            const float x0 = kv.x * f[2 * i], x1 = kv.y * f[2 * i + 1];
-            const __nv_bfloat162 hp = __floats2bfloat162_rn(x0, x1);
-            const float2 hf = __bfloat1622float2(hp);
-            const __nv_bfloat162 lp = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-            hi[i] = *reinterpret_cast<const uint32_t *>(&hp);
-            lo_w[r][i] = *reinterpret_cast<const uint32_t *>(&lp);
+          for (int r = 0; r < 8; ++r) {
+            const int e = tid + r * 128;
+            const int t = e >> 4, c8 = e & 15;
+            const uint32_t off = (uint32_t)(c8 >> 3) * 8192 + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
+            *reinterpret_cast<uint4 *>(base + OFF_G + off) =
+                make_uint4(lo_w[r][0], lo_w[r][1], lo_w[r][2], lo_w[r][3]);
           }
-          *reinterpret_cast<uint4 *>(base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          fence_proxy_async();
+          mbar_arrive(&bar_conv[st]);
         }
-        if (DIAG) bar_sync_named(BAR_CONV, 128);
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int e = tid + r * 128;
-          const int t = e >> 4, c8 = e & 15;
-          const uint32_t off = (uint32_t)(c8 >> 3) * 8192 + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
-          *reinterpret_cast<uint4 *>(base + OFF_G + off) =
-              make_uint4(lo_w[r][0], lo_w[r][1], lo_w[r][2], lo_w[r][3]);
-        }
-        fence_proxy_async();
-        mbar_arrive(&bar_conv[st]);
+        if (stop) break;
+        a.T_out[((size_t)U.s * a.H + U.h) * D + tid] = carry;
       }
-      if (stop) break;
-      if (DIAG) a.T_out[((size_t)U.s * a.H + U.h) * D + tid] = carry;
-      else if (tid == 0) a.T_out[(size_t)U.s * a.H + U.h] = carry;
     }
   } else {
     // ---------------- store (warps 4-7; row = TMEM lane = et) ----------------
@@ -447,7 +480,7 @@ cudaError_t launch_one(const CUtensorMap &mk, const CUtensorMap &mv, const CUten
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  build_decay_tc_kernel<DIAG><<<grid, NT, Cfg<DIAG>::SMEM, st>>>(mk, mv, ma, a);
+  build_decay_tc_kernel<DIAG><<<grid, Cfg<DIAG>::NT, Cfg<DIAG>::SMEM, st>>>(mk, mv, ma, a);
   return cudaGetLastError();
 }
 

@@ -232,39 +232,36 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr bool TCD = std::is_same<Tin, __nv_bfloat16>::value;
   const bool kda = a.fam == HYPIC_FAM_KDA;
   const bool want_o = a.o_out != nullptr;
-  // Tokens [t0, t0 + SG) of the seam window that follows composition step `st`, this thread's share.
-  auto load_seam = [&](int st, int t0, float (&lk)[NL], float (&lv)[NL], float (&lq)[NL], float (&lg)[NL],
-                       float &la, float &lb) {
+  // Tokens [t0, t0 + SG) of the seam window that follows composition step `st`, this thread's share,
+  // as the stored values: nothing here uses a loaded register, so the loads stay in flight until
+  // the values are stored to shared memory (after a block barrier, which no instruction crosses).
+  auto load_seam = [&](int st, int t0, Tin (&lk)[NL], Tin (&lv)[NL], Tin (&lq)[NL], float (&lg)[NL], float &la,
+                       float &lb) {
     const int ng = a.w - t0 < SG ? a.w - t0 : SG;
     const size_t tok0 = ((size_t)b * (a.n - 1) + st) * a.w + t0;
     la = 1.f;
     lb = 0.f;
     if (tid < ng) {
       const size_t tok = tok0 + tid;
-      la = a.fam == HYPIC_FAM_GATED_DELTA ? a.seam_alpha[tok * H + h] : 1.f;
+      if (a.fam == HYPIC_FAM_GATED_DELTA) la = a.seam_alpha[tok * H + h];
       lb = a.seam_beta[tok * H + h];
     }
 #pragma unroll
     for (int it = 0; it < NL; ++it) {
       const int e = tid + it * NT, t = e / D, i = e % D;
-      lk[it] = lv[it] = lq[it] = 0.f;
+      lk[it] = lv[it] = lq[it] = Tin(0.f);
       lg[it] = 1.f;
       if (t < ng) {
         const size_t g = ((tok0 + t) * H + h) * D + i;
-        lk[it] = ld_tok<Tin>(SK, g);
-        lv[it] = ld_tok<Tin>(SV, g);
-        lq[it] = want_o ? ld_tok<Tin>(SQ, g) : 0.f;
-        lg[it] = kda ? a.seam_alpha[g] : 1.f;
+        lk[it] = SK[g];
+        lv[it] = SV[g];
+        if (want_o) lq[it] = SQ[g];
+        if (kda) lg[it] = a.seam_alpha[g];
       }
     }
   };
 
   for (int step = 0; step < a.n; ++step) {
-    // The first token group of the seam window after this step is loaded now: the state lives in
-    // tensor memory until the epilogue, so these registers are free, and the loads' latency hides
-    // behind the step's T split and products.
-    float pk[NL], pv[NL], pq[NL], pg[NL], pa = 1.f, pb = 0.f;
-    if (a.w > 0 && step + 1 < a.n) load_seam(step, 0, pk, pv, pq, pg, pa, pb);
     // (1) T of this step: fp32 staging -> three bf16 B pieces [128 i][128 k], K-major, swizzled.
     // Thread (row i, half) converts k in [64 half, 64 half + 64).  bf16 pairs: already in place.
     if (tid == 0) {
@@ -303,6 +300,12 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_before();
       __syncthreads();
     }
+    // The first token group of the seam window after this step is loaded now: the state lives in
+    // tensor memory until the epilogue, so these registers are free, and the loads' latency hides
+    // behind the step's products.
+    Tin pk[NL], pv[NL], pq[NL];
+    float pg[NL], pa = 1.f, pb = 0.f;
+    if (a.w > 0 && step + 1 < a.n) load_seam(step, 0, pk, pv, pq, pg, pa, pb);
     if (tid == 0) {
       tc_fence_after();
       // fp32: the staging buffer is consumed.  bf16: the other buffer's MMAs (step - 1) are done.
@@ -398,7 +401,8 @@ __global__ void __launch_bounds__(NT, 1)
           {
             // the first group was loaded at the top of the step; later groups load here, all of a
             // group's loads issued before the first store (one memory latency)
-            float lk[NL], lv[NL], lq[NL], lg[NL], la, lb;
+            Tin lk[NL], lv[NL], lq[NL];
+            float lg[NL], la, lb;
             if (t0 == 0) {
 #pragma unroll
               for (int it = 0; it < NL; ++it) {
@@ -416,9 +420,9 @@ __global__ void __launch_bounds__(NT, 1)
             for (int it = 0; it < NL; ++it) {
               const int e = tid + it * NT;
               if (e / D < ng) {
-                sK[e] = lk[it];
-                sV[e] = lv[it];
-                sQ[e] = lq[it];
+                sK[e] = to_f32<Tin>(lk[it]);
+                sV[e] = to_f32<Tin>(lv[it]);
+                sQ[e] = to_f32<Tin>(lq[it]);
                 sGc[e] = lg[it];
               }
             }

@@ -52,23 +52,24 @@ TRAFFIC = {
     "build_outputs_tc": {"bytes": 5_339_999_232, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
                          "commit": "2fc0e60"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
-    "decay_scalar_const": {"bytes": 645_460_138, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
-                           "digest": "5f8476ae66e0", "commit": "edc1dcb"},
-    "decay_diag": {"bytes": 1_193_407_829, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "5f8476ae66e0",
-                   "commit": "edc1dcb"},
+    "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
+                           "digest": "6453c37efead", "commit": "1b1b1f2"},
+    "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
+                   "commit": "1b1b1f2"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
     "decay_kda": {"bytes": 3_970_323_882, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9bf23969ba4a",
                   "commit": "edc1dcb"},
-    # compose_pipe32_kernel / compose_pipe_kernel on the warm-cache workload (fp32 and bf16 pools):
+    # compose_pipe32_kernel / compose_pipe_kernel (the kernels composition without seam windows runs)
+    # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each
     # head's pool entries and requests are independent, the grid head-major)
-    "compose_f32": {"bytes": 46_612_121_600, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"),
-                    "digest": "1492692e731a", "commit": "1234e70"},
-    "compose_bf16": {"bytes": 19_925_423_360, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"),
-                     "digest": "1492692e731a", "commit": "1234e70"},
+    "compose_f32": {"bytes": 46_612_121_600, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
+                    "digest": "60ec2b5f6540", "commit": "1234e70"},
+    "compose_bf16": {"bytes": 19_925_423_360, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
+                     "digest": "60ec2b5f6540", "commit": "1234e70"},
     # compose_pipe32_kernel in scan mode, 64 pairs: captured at 128 heads (--scan-heads 128) and
     # scaled by 7.5 to 960 heads
-    "scan": {"bytes": 15_815_274_880, "src": ("compose_pipe.cu", "compose_tc.cu", "tc_ptx.cuh"), "digest": "1492692e731a",
+    "scan": {"bytes": 15_815_274_880, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "60ec2b5f6540",
              "commit": "1234e70"},
     # staged RoPE shift and state re-rotation
     "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",

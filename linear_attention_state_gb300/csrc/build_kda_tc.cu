@@ -177,48 +177,67 @@ __global__ void __launch_bounds__(NT, 2)
   const uint8_t *sK = sm + KP_K;
   float *sG = reinterpret_cast<float *>(sm + KP_G);  // [64 t][128 i]
 
-  // Thread = key channel i: G_t = log2-cumsum of the channel's gates, in place over the gates
-  // (tokens past the body count as gate 1), with G at the middle token and at the end.
-  float GC, gm;
+  // Thread = key channel i: Gamma_t = running product of the channel's gates (tokens past the body
+  // count as gate 1), in registers.  Gamma_0 / Gamma_{C-1} <= 1 / Gamma_{C-1}: factors around the
+  // middle stay within 2^100 when Gamma_{C-1} >= 2^-100 in every channel (separable).  Then the tile
+  // holds E_t = Gamma_t / M with M = 2^round(log2 Gamma_m) at the middle token, a power of two, so
+  // E_t and the rescaling of Wk^T's rows by M are exact.  Otherwise (the fallback) the tile holds
+  // the log2-cumsum G_t of the gates, and every factor is taken as one exponential.
+  float GamC, wk_scale;
+  bool separable;
   {
-    float g = 0.f;
-    gm = 0.f;
-#pragma unroll 16
+    float gv[C];
+#pragma unroll
+    for (int t = 0; t < C; ++t) gv[t] = sG[t * D + tid];
+    float pr = 1.f;
+#pragma unroll
     for (int t = 0; t < C; ++t) {
-      g += t < nvalid ? log2f(sG[t * D + tid]) : 0.f;
-      sG[t * D + tid] = g;
-      if (t == C / 2) gm = g;
+      pr = t < nvalid ? pr * gv[t] : pr;
+      gv[t] = pr;
     }
-    GC = g;
+    GamC = pr;
+    separable = __syncthreads_and(GamC >= 0x1p-100f) != 0;
+    if (separable) {
+      const int em = (int)rintf(log2f(gv[C / 2]));
+      const float Minv = ldexpf(1.f, -em);
+      wk_scale = ldexpf(1.f, em);
+#pragma unroll
+      for (int t = 0; t < C; ++t) sG[t * D + tid] = gv[t] * Minv;
+    } else {
+      wk_scale = 1.f;
+      float g = 0.f;
+#pragma unroll 16
+      for (int t = 0; t < C; ++t) {
+        g += t < nvalid ? log2f(sG[t * D + tid]) : 0.f;
+        sG[t * D + tid] = g;
+      }
+    }
   }
-  // G_0 - G_{C-1} <= -GC (G_0 <= 0): factors around the middle stay within about 2^100 when GC > -100.
-  // The middle reference G_m is rounded to an integer, so that rescaling by 2^{G_m} is exact; in the
-  // fallback it is 0 and (K o E) is K o Gamma itself.
-  const bool separable = __syncthreads_and(GC > -100.f) != 0;
-  const float wk_scale = separable ? exp2f(rintf(gm)) : 1.f;  // row tid of Wk^T, below
+  __syncthreads();  // the pass below reads other channels' entries
 
   // One pass over the chunk, eight channels of one token per item: the Gram's operands
-  // (K o E) = K o 2^{G - G_m} (also Wk^T's, rescaled by 2^{G_m} per channel afterwards) and
-  // (K o F) = K o 2^{G_m - G} in hi and lo pieces, and Khat = K o 2^{G_C - G} straight to the record.
+  // (K o E) (also Wk^T's, rescaled by M per channel afterwards) and (K o F), F = 1 / E, in hi and
+  // lo pieces, and Khat = K o Gamma_C / Gamma = (K o F) E_{C-1} straight to the record.  A thread's
+  // items all cover the same eight channels (8 c8 ..), whose last-token entries are read once.
+  // Fallback: (K o E) = K o 2^G, Khat = K o 2^{G_{C-1} - G}.
   uint8_t *rec = krec(a, s, c, hh);
+  const int c8 = tid & 15;
+  float L8[8];
+  {
+    const float4 e0 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8);
+    const float4 e1 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8 + 4);
+    L8[0] = e0.x; L8[1] = e0.y; L8[2] = e0.z; L8[3] = e0.w;
+    L8[4] = e1.x; L8[5] = e1.y; L8[6] = e1.z; L8[7] = e1.w;
+  }
 #pragma unroll 2
   for (int j = 0; j < 8; ++j) {
-    const int e = tid + j * NT;
-    const int t = e >> 4, c8 = e & 15;  // token t, channels 8 c8 .. 8 c8 + 7
+    const int t = (tid >> 4) + 8 * j;  // token of item tid + 128 j
     const uint32_t off = (uint32_t)(c8 >> 3) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
     const uint4 kr = *reinterpret_cast<const uint4 *>(sK + off);
     const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
     const float4 g0 = *reinterpret_cast<const float4 *>(sG + t * D + 8 * c8);
     const float4 g1 = *reinterpret_cast<const float4 *>(sG + t * D + 8 * c8 + 4);
-    const float4 m0 = *reinterpret_cast<const float4 *>(sG + (C / 2) * D + 8 * c8);
-    const float4 m1 = *reinterpret_cast<const float4 *>(sG + (C / 2) * D + 8 * c8 + 4);
-    const float4 e0 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8);
-    const float4 e1 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8 + 4);
     const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    float M8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    const float E8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-    for (int q = 0; q < 8; ++q) M8[q] = separable ? rintf(M8[q]) : 0.f;
     float k8[8], p1[8], p2[8], kh[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -226,11 +245,20 @@ __global__ void __launch_bounds__(NT, 2)
       k8[2 * q] = kv.x;
       k8[2 * q + 1] = kv.y;
     }
+    if (separable) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      p1[q] = k8[q] * exp2f(G8[q] - M8[q]);
-      p2[q] = k8[q] * exp2f(M8[q] - G8[q]);
-      kh[q] = k8[q] * exp2f(E8[q] - G8[q]);
+      for (int q = 0; q < 8; ++q) {
+        p1[q] = k8[q] * G8[q];
+        p2[q] = k8[q] * __frcp_rn(G8[q]);
+        kh[q] = p2[q] * L8[q];
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        p1[q] = k8[q] * exp2f(G8[q]);
+        p2[q] = 0.f;
+        kh[q] = k8[q] * exp2f(L8[q] - G8[q]);
+      }
     }
     uint4 hi, lo;
     ksplit8(p1, hi, lo);
@@ -245,7 +273,7 @@ __global__ void __launch_bounds__(NT, 2)
     *reinterpret_cast<uint4 *>(rec + KR_KH + off) = hi;
     *reinterpret_cast<uint4 *>(rec + KR_KL + off) = lo;
   }
-  reinterpret_cast<float *>(rec + KR_GC)[tid] = exp2f(GC);
+  reinterpret_cast<float *>(rec + KR_GC)[tid] = GamC;
   fence_proxy_async();
   __syncthreads();
 

@@ -1,5 +1,7 @@
 // Tensor-core composition chain for the delta families at d = 128: compose, fused request
-// assembly (seam advance + compose) and the affine scan.
+// assembly (seam advance + compose) and the affine scan.  Plain composition and the scan (no seam
+// windows) are dispatched from here to the pipelined kernels of compose_pipe.cu; this kernel runs
+// the assembly, whose seam windows need the whole column state between two steps.
 //
 // Composition applies the cached pairs in prompt order, S <- T_C S + S_{C|0} (HYPIC reading
 // notes, Method 2, paper Eq. (6)); assembly first advances the running state through the w

@@ -57,8 +57,8 @@ TRAFFIC = {
     "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
                    "commit": "1b1b1f2"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
-    "decay_kda": {"bytes": 3_970_323_882, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9bf23969ba4a",
-                  "commit": "edc1dcb"},
+    "decay_kda": {"bytes": 3_971_162_965, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "ea58d4e3d555",
+                  "commit": "5a713f2"},
     # compose_pipe32_kernel / compose_pipe_kernel (the kernels composition without seam windows runs)
     # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each

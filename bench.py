@@ -63,14 +63,14 @@ TRAFFIC = {
     # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each
     # head's pool entries and requests are independent, the grid head-major)
-    "compose_f32": {"bytes": 46_612_121_600, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                    "digest": "60ec2b5f6540", "commit": "1234e70"},
-    "compose_bf16": {"bytes": 19_925_423_360, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                     "digest": "60ec2b5f6540", "commit": "1234e70"},
+    "compose_f32": {"bytes": 46_755_327_360, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
+                    "digest": "8c3124594fff", "commit": "two-level scan"},
+    "compose_bf16": {"bytes": 19_951_943_680, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
+                     "digest": "8c3124594fff", "commit": "two-level scan"},
     # compose_pipe32_kernel in scan mode, 64 pairs: captured at 128 heads (--scan-heads 128) and
     # scaled by 7.5 to 960 heads
-    "scan": {"bytes": 15_815_274_880, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "60ec2b5f6540",
-             "commit": "1234e70"},
+    "scan": {"bytes": 15_826_974_720, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "8c3124594fff",
+             "commit": "two-level scan"},
     # staged RoPE shift and state re-rotation
     "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",
                                     "commit": "ae9cc2f"},
@@ -437,6 +437,23 @@ def scan_measure(steps, warmup, dev, peaks, heads=None):
            "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": by / t / 1e9 / peaks["hbm_gbs"], "traffic": traffic("scan")},
            "status": hy.stream_status()}
+    del T, S
+    # Few heads, a long chain: the two-level scan against one sequential chain per head.
+    n2, H2 = 1024, 4
+    T, S = W.random_pairs(n2, H2, d, dev, key=12)
+    small = {"workload": f"scan_{n2}x{H2}heads_d{d}_fp32"}
+    for name, two in (("two_level", True), ("plain", False)):
+        def fn2(ev):
+            if ev is not None:
+                ev[0].record()
+            hy.affine_scan(T, S, family="gated_delta", two_level=two)
+            if ev is not None:
+                ev[1].record()
+                ev[2].record()
+        _, k2, _ = run_timed(fn2, steps, warmup, torch.cuda.synchronize)
+        small[f"ms_{name}"] = sum(k2) / len(k2)
+    small["status"] = hy.stream_status()
+    res["few_heads"] = small
     del T, S
     torch.cuda.empty_cache()
     return res

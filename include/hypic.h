@@ -250,8 +250,13 @@ hypic_status hypic_compose(const hypic_shape *shape, int32_t B, int32_t n, const
  * (T2,S2) o (T1,S1) = (T2 T1, T2 S1 + S2), associative, not commutative):
  *   (Tp_0, Sp_0) = (T_0, S_0),  (Tp_i, Sp_i) = (T_i, S_i) o (Tp_{i-1}, Sp_{i-1}).
  *   T, T_prefix [n, H, t_size];  S, S_prefix [n, H, d_k, d_v].
- *   Outputs must not overlap inputs.  ws may be NULL when
- *   hypic_scan_workspace_bytes() returns 0.
+ *   Outputs must not overlap inputs.  ws is optional (NULL: one sequential
+ *   chain per head).  Given at least hypic_scan_workspace_bytes() bytes
+ *   (16-byte aligned), the delta families at d_k = d_v = 128 with fewer heads
+ *   than fill the device run a two-level scan instead, using the composition
+ *   rule's associativity: chunk totals, a scan of the totals, then every chunk
+ *   again from its carry; about twice the work in far fewer sequential steps.
+ *   hypic_scan_workspace_bytes() returns 0 when no workspace would be used.
  */
 hypic_status hypic_affine_scan(const hypic_shape *shape, int32_t n, const float *T, const float *S,
                                float *T_prefix, float *S_prefix, void *ws, size_t ws_bytes,

@@ -242,15 +242,16 @@ def compose(pool_T, pool_S, idx, S_init=None, family="gated_delta", out=None, st
     return S_out
 
 
-def affine_scan(T, S, family="gated_delta", stream=None):
-    """Inclusive prefix scan of n pairs: T [n, H, ...], S [n, H, d, d]."""
+def affine_scan(T, S, family="gated_delta", stream=None, two_level=True):
+    """Inclusive prefix scan of n pairs: T [n, H, ...], S [n, H, d, d].  two_level=False passes no
+    workspace, so every head's scan runs as one sequential chain."""
     lib = L.load()
     _cuda(T, "T", torch.float32), _cuda(S, "S", torch.float32)
     n, H, d, _ = S.shape
     sh = L.shape(H, d, family, "f32")
     Tp = torch.empty_like(T)
     Sp = torch.empty_like(S)
-    ws_bytes = lib.hypic_scan_workspace_bytes(ctypes.byref(sh), n)
+    ws_bytes = lib.hypic_scan_workspace_bytes(ctypes.byref(sh), n) if two_level else 0
     ws = torch.empty(ws_bytes, device=S.device, dtype=torch.uint8) if ws_bytes else None
     st = lib.hypic_affine_scan(ctypes.byref(sh), n, _p(T), _p(S), _p(Tp), _p(Sp), _p(ws), ws_bytes,
                                _stream(stream))

@@ -155,9 +155,9 @@ size_t hypic_build_workspace_bytes_outputs(const hypic_shape *sh, int32_t n_seg,
 }
 
 size_t hypic_scan_workspace_bytes(const hypic_shape *sh, int32_t n) {
-  (void)sh;
-  (void)n;
-  return 0;
+  if (check_shape(sh) != HYPIC_OK || n <= 0 || sh->d_k != sh->d_v) return 0;
+  if (!compose_tc_supported(sh->d_k, sh->family)) return 0;
+  return scan_pipe32_workspace_bytes(sh->H, n);
 }
 
 hypic_status hypic_segment_build(const hypic_shape *sh, const void *k, const void *v, const void *q,
@@ -416,8 +416,6 @@ hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T,
   hypic_status r = check_shape(sh);
   if (r != HYPIC_OK) return r;
   if (n < 0) return HYPIC_EINVAL;
-  if (ws_bytes < hypic_scan_workspace_bytes(sh, n)) return HYPIC_ENOSPACE;
-  (void)ws;
   if (n == 0 || sh->H == 0) return HYPIC_OK;
   if (!ok_ptr(T) || !ok_ptr(S) || !ok_ptr(T_prefix) || !ok_ptr(S_prefix)) return HYPIC_EINVAL;
   int *err = nullptr;
@@ -442,6 +440,8 @@ hypic_status hypic_affine_scan(const hypic_shape *sh, int32_t n, const float *T,
   a.seam = TokenSrc{nullptr, nullptr, nullptr, nullptr, nullptr, sh->in_dtype};
   a.o_out = nullptr;
   a.err = err;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
   return from_cuda(launch_chain(a, (cudaStream_t)stream));
 }
 

@@ -89,12 +89,15 @@ struct ChainArgs {
   TokenSrc seam;  // seam tokens [B, n-1, w, H, D]
   float *o_out;   // [B, n-1, w, H, D] or null
   int *err;
+  void *ws;         // scan: optional workspace for the two-level scan (null: one chain per head)
+  size_t ws_bytes;
 };
 cudaError_t launch_chain(const ChainArgs &a, cudaStream_t st);
 
 // tcgen05 composition chain (d = 128, delta families): compose, assemble and scan.
 bool compose_tc_supported(int D, int fam);
 cudaError_t launch_compose_tc(const ChainArgs &a, cudaStream_t st);
+size_t scan_pipe32_workspace_bytes(int H, int n);  // two-level tensor-core scan (0: none used)
 
 // fp32 pairs -> bf16 storage, round to nearest even (element counts; 16-byte aligned pointers).
 cudaError_t launch_pairs_to_bf16(const float *T, const float *S, void *T_lp, void *S_lp, int64_t t_elems,

@@ -297,6 +297,10 @@ __global__ void __launch_bounds__(NTH, 1)
 //     hi.hi, output half 1 (N = 64)  -> commit e1, and the step's B buffer is free
 // as the bf16-pair kernel does.  In scan mode (one block per head and column half of the
 // augmented state [T | S], as the unpipelined chain has it) every step's state is written out.
+// The scan may be cut into P chunks of m pairs (one block pair per chunk and head): a chunk then
+// starts from a given carry state instead of [I | 0], and either writes every prefix at its global
+// row or only its last one (the chunk's total) to a separate array; the two-level scan below
+// combines these.
 constexpr uint32_t BUF_B = 3 * 32768;          // B pieces of one T: hi, mid, lo x two k-blocks
 constexpr uint32_t SMEM32 = 2 * BUF_B + 1024;  // two buffers by step parity
 
@@ -311,8 +315,19 @@ struct Pipe32Args {
   float *T_rec, *S_rec;
   int *err;
 };
+// Scan chunks: chunk c covers pairs [c m, min(n, c m + m)); chunk c > 0 starts from the carry
+// (Tc, Sc)[c - 1] when Tc is set; with Tlast set only each chunk's last prefix is written, to
+// (Tlast, Slast)[c].  Arrays [chunk][H][D][D].
+struct ScanChunks {
+  int m, P;
+  const float *Tc, *Sc;
+  float *Tlast, *Slast;
+};
 
-__global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
+// CHUNK: the scan chunk fields of Pipe32Args are read (the two-level scan's launches); without it
+// the kernel is the plain composition or scan, compiled without them.
+template <bool CHUNK>
+__global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a, ScanChunks q) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_b[2];  // the B pieces of the step with this parity are written
   __shared__ uint64_t bar_f[2];  // the products of the step with this parity are done
@@ -323,18 +338,28 @@ __global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int H = a.H, n = a.n;
-  int b, h;
+  const int H = a.H;
+  int b, h, ck = 0, s0 = 0, n = a.n;  // n: the steps of this block's chain, from pool row s0
   bool isT = false;  // scan: the T half (starts at I, no addend)
   if (a.scan) {
     isT = (blockIdx.x & 1) == 0;
-    h = blockIdx.x >> 1;
     b = 0;
+    if (CHUNK) {
+      h = (blockIdx.x >> 1) % H;
+      ck = (blockIdx.x >> 1) / H;
+      s0 = ck * q.m;
+      n = a.n - s0 < q.m ? a.n - s0 : q.m;
+      if (n < 0) n = 0;
+    } else {
+      h = blockIdx.x >> 1;
+    }
   } else {
     b = blockIdx.x % a.B;
     h = blockIdx.x / a.B;
   }
   const bool addend = !isT;
+  const float *carry =
+      (CHUNK && a.scan && q.Tc && ck > 0) ? (isT ? q.Tc : q.Sc) + ((size_t)(ck - 1) * H + h) * D * D : nullptr;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -358,7 +383,8 @@ __global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int i = i0 + r;
-      if (a.scan) x[r] = (isT && i == j) ? 1.f : 0.f;
+      if (carry) x[r] = carry[(size_t)i * D + j];
+      else if (a.scan) x[r] = (isT && i == j) ? 1.f : 0.f;
       else x[r] = a.S_init ? a.S_init[base_bh + (size_t)i * D + j] : 0.f;
     }
   }
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
   const uint32_t tmem = tmem_slot;
 
   auto entry = [&](int s) -> int64_t {
-    int64_t p = a.idx ? (int64_t)a.idx[(size_t)b * n + s] : (int64_t)s;
+    int64_t p = a.idx ? (int64_t)a.idx[(size_t)b * a.n + s] : (int64_t)(s0 + s);
     if (p < 0 || p >= a.pool_size) {
       set_error(a.err, HYPIC_EDEVICE);
       p = 0;
@@ -528,8 +554,11 @@ __global__ void __launch_bounds__(NTH, 1) compose_pipe32_kernel(Pipe32Args a) {
 #pragma unroll
         for (int r = 0; r < 32; ++r) x[hb + r] += dv[r];
       }
-      if (a.scan) {
-        float *rec = (isT ? a.T_rec : a.S_rec) + ((size_t)s * H + h) * D * D + (size_t)i0 * D + j;
+      if (a.scan && (!CHUNK || !q.Tlast || s == n - 1)) {
+        // (one expression per case: computing the row offset separately measured 2.5% slower)
+        float *rec = (CHUNK && q.Tlast)
+                         ? (isT ? q.Tlast : q.Slast) + ((size_t)ck * H + h) * D * D + (size_t)i0 * D + j
+                         : (isT ? a.T_rec : a.S_rec) + ((size_t)(s0 + s) * H + h) * D * D + (size_t)i0 * D + j;
 #pragma unroll
         for (int r = 0; r < R; ++r) rec[(size_t)r * D] = x[r];
       }
@@ -578,11 +607,39 @@ cudaError_t launch_compose_pipe(const CUtensorMap &mT, const CUtensorMap &mS, in
   return cudaGetLastError();
 }
 
-// Pairs in fp32, no seam window: the pipelined composition or, with scan set, the affine scan
-// (T_rec and S_rec receive every prefix).
+namespace {
+template <bool CHUNK>
+cudaError_t launch_pipe32(const Pipe32Args &a, const ScanChunks &q, long long blocks, cudaStream_t st) {
+  if (blocks <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(a.pool_T) & 15) != 0) return cudaErrorInvalidValue;  // rows read as float4
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e =
+      cudaFuncSetAttribute(compose_pipe32_kernel<CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM32);
+  if (e != cudaSuccess) return e;
+  compose_pipe32_kernel<CHUNK><<<(unsigned)blocks, NTH, SMEM32, st>>>(a, q);
+  return cudaGetLastError();
+}
+
+// Two-level scan plan for H heads and n pairs: P chunks of m pairs, enough block pairs to fill the
+// device once and at least 16 pairs a chunk (P = 1: the plain scan, one chain per head).
+void scan_plan(int H, int n, int &P, int &m) {
+  P = 1;
+  m = n;
+  int dev = 0, sms = 0;
+  if (H <= 0 || n < 32 || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return;
+  const int fill = (sms + 2 * H - 1) / (2 * H);
+  const int p = fill < n / 16 ? fill : n / 16;
+  if (p < 2) return;
+  m = (n + p - 1) / p;
+  P = (n + m - 1) / m;  // every chunk holds at least one pair
+}
+}  // namespace
+
+// Pairs in fp32, no seam window: the pipelined composition (one chain per request and head).
 cudaError_t launch_compose_pipe32(int H, int B, int n, const int32_t *idx, int64_t pool_size, const float *pool_T,
-                                  const float *pool_S, const float *S_init, float *S_out, int scan, float *T_rec,
-                                  float *S_rec, int *err, cudaStream_t st) {
+                                  const float *pool_S, const float *S_init, float *S_out, int *err, cudaStream_t st) {
   Pipe32Args a{};
   a.H = H;
   a.B = B;
@@ -593,18 +650,70 @@ cudaError_t launch_compose_pipe32(int H, int B, int n, const int32_t *idx, int64
   a.pool_S = pool_S;
   a.S_init = S_init;
   a.S_out = S_out;
-  a.scan = scan;
-  a.T_rec = T_rec;
-  a.S_rec = S_rec;
   a.err = err;
-  const long long blocks = scan ? (long long)H * 2 : (long long)B * H;
-  if (blocks <= 0) return cudaSuccess;
-  if ((reinterpret_cast<uintptr_t>(pool_T) & 15) != 0) return cudaErrorInvalidValue;  // rows read as float4
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(compose_pipe32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM32);
+  return launch_pipe32<false>(a, ScanChunks{}, (long long)B * H, st);
+}
+
+// Workspace of the two-level scan (0 when the plan is the plain scan): the chunks' totals and the
+// carries into chunks 1 .., T and S, [chunk][H][D][D] fp32.
+size_t scan_pipe32_workspace_bytes(int H, int n) {
+  int P = 1, m = n;
+  scan_plan(H, n, P, m);
+  return P < 2 ? 0 : (size_t)(2 * P - 1) * 2 * (size_t)H * D * D * sizeof(float);
+}
+
+// Inclusive affine scan over fp32 pairs (T, S [n, H, D, D]) into (Tp, Sp).  With fewer heads than
+// fill the device and a workspace of scan_pipe32_workspace_bytes(), a two-level scan: (1) every
+// chunk of m pairs is scanned from [I | 0] and only its total kept; (2) the totals are scanned,
+// giving the carry into each chunk; (3) every chunk is scanned again from its carry, writing its
+// prefixes.  The prefixes are those of the composition rule's associativity; the work is about
+// twice the plain scan's, the depth about 2 m + P steps instead of n.  Otherwise the plain scan.
+cudaError_t launch_scan_pipe32(int H, int n, const float *T, const float *S, float *Tp, float *Sp, void *ws,
+                               size_t ws_bytes, int *err, cudaStream_t st) {
+  int P = 1, m = n;
+  scan_plan(H, n, P, m);
+  const size_t need = P < 2 ? 0 : (size_t)(2 * P - 1) * 2 * (size_t)H * D * D * sizeof(float);
+  Pipe32Args a{};
+  a.H = H;
+  a.B = 1;
+  a.n = n;
+  a.pool_size = n;
+  a.pool_T = T;
+  a.pool_S = S;
+  a.scan = 1;
+  a.err = err;
+  if (P < 2 || ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15) != 0) {
+    a.T_rec = Tp;
+    a.S_rec = Sp;
+    return launch_pipe32<false>(a, ScanChunks{}, 2LL * H, st);
+  }
+  const size_t blk = (size_t)H * D * D;
+  float *totT = static_cast<float *>(ws), *totS = totT + P * blk;
+  float *carT = totS + P * blk, *carS = carT + (P - 1) * blk;
+  // (1) chunk totals
+  ScanChunks q{};
+  q.m = m;
+  q.P = P;
+  q.Tlast = totT;
+  q.Slast = totS;
+  cudaError_t e = launch_pipe32<true>(a, q, 2LL * H * P, st);
   if (e != cudaSuccess) return e;
-  compose_pipe32_kernel<<<(unsigned)blocks, NTH, SMEM32, st>>>(a);
-  return cudaGetLastError();
+  // (2) carries: the inclusive scan of the first P - 1 totals
+  Pipe32Args c = a;
+  c.n = P - 1;
+  c.pool_size = P;
+  c.pool_T = totT;
+  c.pool_S = totS;
+  c.T_rec = carT;
+  c.S_rec = carS;
+  if ((e = launch_pipe32<false>(c, ScanChunks{}, 2LL * H, st)) != cudaSuccess) return e;
+  // (3) every chunk again, from its carry
+  q.Tlast = q.Slast = nullptr;
+  q.Tc = carT;
+  q.Sc = carS;
+  a.T_rec = Tp;
+  a.S_rec = Sp;
+  return launch_pipe32<true>(a, q, 2LL * H * P, st);
 }
 
 }  // namespace hypic

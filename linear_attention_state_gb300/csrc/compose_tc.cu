@@ -816,17 +816,20 @@ cudaError_t launch_compose_pipe(const CUtensorMap &mT, const CUtensorMap &mS, in
                                 cudaStream_t st);
 
 cudaError_t launch_compose_pipe32(int H, int B, int n, const int32_t *idx, int64_t pool_size, const float *pool_T,
-                                  const float *pool_S, const float *S_init, float *S_out, int scan, float *T_rec,
-                                  float *S_rec, int *err, cudaStream_t st);
+                                  const float *pool_S, const float *S_init, float *S_out, int *err, cudaStream_t st);
+cudaError_t launch_scan_pipe32(int H, int n, const float *T, const float *S, float *Tp, float *Sp, void *ws,
+                               size_t ws_bytes, int *err, cudaStream_t st);
 
 cudaError_t launch_compose_tc(const ChainArgs &c, cudaStream_t st) {
   const uint64_t rows = (uint64_t)c.pool_size * c.H * D;
   if (rows >= ((uint64_t)1 << 31)) return cudaErrorInvalidValue;
   const bool pb = c.pair_bf16 != 0;
+  if (!pb && c.w == 0 && c.scan)
+    return launch_scan_pipe32(c.H, c.n, static_cast<const float *>(c.pool_T), static_cast<const float *>(c.pool_S),
+                              c.T_rec, c.S_rec, c.ws, c.ws_bytes, c.err, st);
   if (!pb && c.w == 0)
     return launch_compose_pipe32(c.H, c.B, c.n, c.idx, c.pool_size, static_cast<const float *>(c.pool_T),
-                                 static_cast<const float *>(c.pool_S), c.S_init, c.S_out, c.scan, c.T_rec, c.S_rec,
-                                 c.err, st);
+                                 static_cast<const float *>(c.pool_S), c.S_init, c.S_out, c.err, st);
   CUtensorMap mT, mS;
   if (pb) {
     if (!make_tmap_bf16_2d(&mT, c.pool_T, rows, D, D, 64, 128)) return cudaErrorInvalidValue;

@@ -221,6 +221,35 @@ def test_long_chains_and_scan_fp32_pairs():
                 assert relerr(np64(Sp[i, h]), Sr[i]) <= TOL_F32, (n, h, i)
 
 
+@pytest.mark.parametrize("H,n", [(2, 64), (1, 48), (3, 40), (2, 200)])
+def test_two_level_scan(H, n):
+    """With few heads the scan runs in two levels (chunk totals, a scan of the totals, every chunk
+    again from its carry).  Transitions are orthogonal matrices, so the prefixes keep norm 1 and
+    the relative error stays meaningful over long chains; every prefix is checked against the
+    oracle, for the two-level scan and for the plain one (no workspace).  Chains up to 64 pairs
+    (the workloads' lengths) are held to the fp32 tolerance.  Beyond that each fp32 composition step
+    adds its own rounding (about sqrt(128) units of 2^-24 for a 128-term product), so a chain of n
+    steps is held to n * 6.7e-7 and both scans must stay within it."""
+    d = 128
+    g = torch.Generator().manual_seed(1000 * H + n)
+    Q, _ = torch.linalg.qr(torch.randn((n, H, d, d), generator=g, dtype=torch.float64))
+    T = Q.to(torch.float32).contiguous().to(DEV)
+    S = torch.randn((n, H, d, d), generator=g).to(DEV)
+    outs = {"two-level": hy.affine_scan(T, S, family="delta"),
+            "plain": hy.affine_scan(T, S, family="delta", two_level=False)}
+    assert hy.stream_status() == 0
+    tol = TOL_F32 if n <= 64 else n * 6.7e-7
+    worst = {name: 0.0 for name in outs}
+    for h in range(H):
+        Tr, Sr = oracle.affine_scan("delta", np64(T[:, h]).reshape(n, -1), np64(S[:, h]))
+        for name, (Tp, Sp) in outs.items():
+            for i in range(n):
+                worst[name] = max(worst[name], relerr(np64(Tp[i, h]), Tr[i].reshape(d, d)),
+                                  relerr(np64(Sp[i, h]), Sr[i]))
+    print(f"two-level scan H={H} n={n}: {worst}")
+    assert max(worst.values()) <= tol, worst
+
+
 @pytest.mark.parametrize("family", FAMS)
 @pytest.mark.parametrize("d,in_dtype", [(16, "f32"), (128, "bf16")])
 def test_seam_advance(family, d, in_dtype):

@@ -64,13 +64,13 @@ TRAFFIC = {
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each
     # head's pool entries and requests are independent, the grid head-major)
     "compose_f32": {"bytes": 46_755_327_360, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                    "digest": "8c3124594fff", "commit": "two-level scan"},
+                    "digest": "8c3124594fff", "commit": "ae10944"},
     "compose_bf16": {"bytes": 19_951_943_680, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                     "digest": "8c3124594fff", "commit": "two-level scan"},
+                     "digest": "8c3124594fff", "commit": "ae10944"},
     # compose_pipe32_kernel in scan mode, 64 pairs: captured at 128 heads (--scan-heads 128) and
     # scaled by 7.5 to 960 heads
     "scan": {"bytes": 15_826_974_720, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "8c3124594fff",
-             "commit": "two-level scan"},
+             "commit": "ae10944"},
     # staged RoPE shift and state re-rotation
     "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",
                                     "commit": "ae9cc2f"},

@@ -1091,26 +1091,30 @@ __global__ void __launch_bounds__(NT2, 1)
 // Wm^T in bf16 hi + lo pieces (A, tensor memory) and M from the prep kernel's record (B).  The
 // outputs of chunk c are read out (scaled by gamma_t, summed) while chunk c + 1's P product runs;
 // gamma_t is read from the workspace record, which stays unchanged while the stage is refilled.
+// The state chain's products (U, P, the update) and the two output products are issued by two
+// threads (warps 8 and 10): one thread issues an MMA only about every 90 cycles, and the output
+// products are off the state's serial path.
 // T_C comes from chain_tc_kernel, run for the T half only; this kernel writes S_{C|0} and o.
 constexpr uint32_t SO_K = 0, SO_V = 16384, SO_Q = 32768, SO_REC = 49152, SO_M = SO_REC + WS_TILES;
 constexpr uint32_t SO_STAGE = SO_M + 16384;  // 112 KB
 constexpr uint32_t SO_SMEM = 2 * SO_STAGE + 1024;
 constexpr uint32_t SO_X = 0, SO_XH = 128, SO_XL = 192, SO_P = 256, SO_OI = 320, SO_OA = 384, SO_WM = 448;
-constexpr int SO_NT = 256 + 64;  // converters + MMA warp + TMA warp
+constexpr int SO_NT = 256 + 96;  // converters + state MMA warp + TMA warp + output MMA warp
 
 __global__ void __launch_bounds__(SO_NT, 1)
     chain_so_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     const __grid_constant__ CUtensorMap mapQ, BuildTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  // rd: the converters have read chunk c's outputs out (the output accumulators may be reused)
-  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1, bar_r2, bar_p, bar_x, bar_o, bar_rd;
+  // rd: the converters have read chunk c's outputs out (the output accumulators may be reused);
+  // oi: the inter-chunk output product has read the state pieces (they may be rewritten)
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1, bar_r2, bar_p, bar_x, bar_o, bar_rd, bar_oi;
   __shared__ __align__(16) float s_sc[2][WS_SCG_BYTES / 4];  // scales, gamma_C, gamma_t per stage
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const bool issuer = warp == 8, producer = warp == 9;
+  const bool issuer = warp == 8, producer = warp == 9, out_issuer = warp == 10;
   const int row = tid & 127, part = (tid >> 7) & 1;
   const int hh = blockIdx.x % a.Hb;
   const int s = blockIdx.x / a.Hb;
@@ -1122,7 +1126,7 @@ __global__ void __launch_bounds__(SO_NT, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], 1);
+      mbar_init(&bar_empty[i], 2);  // both MMA threads read the stage
     }
     mbar_init(&bar_r1, 256);
     mbar_init(&bar_r2, 256);
@@ -1130,6 +1134,7 @@ __global__ void __launch_bounds__(SO_NT, 1)
     mbar_init(&bar_x, 1);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_rd, 256);
+    mbar_init(&bar_oi, 1);
     mbar_fence_init();
     abort_flag = 0;
   }
@@ -1172,7 +1177,6 @@ __global__ void __launch_bounds__(SO_NT, 1)
     if (lane == 0) {
       const uint32_t id_u = idesc_f32acc(1, 1, 1, 0, 128, 64);   // A = V^T (MN-major), B K-major
       const uint32_t id_p = idesc_f32acc(1, 1, 0, 1, 128, 64);   // A = X^T pieces, B = Wk^T (MN-major)
-      const uint32_t id_k = idesc_f32acc(1, 1, 0, 0, 128, 64);   // A = TMEM pieces, B K-major (Q, M)
       const uint32_t id_x = idesc_f32acc(1, 1, 0, 1, 128, 128);  // A = R^T pieces, B = K (MN-major)
       auto stage_ready = [&](int c) -> bool {
         const uint32_t stg = sb + (c & 1) * SO_STAGE;
@@ -1192,7 +1196,7 @@ __global__ void __launch_bounds__(SO_NT, 1)
         const uint32_t stg = sb + (c & 1) * SO_STAGE;
         if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
         tc_fence_after();
-        // P^T += X^T Wk^T (hi.hi + hi.lo + lo.hi), then O_inter^T = X^T Q^T (hi + lo; Q exact)
+        // P^T += X^T Wk^T (hi.hi + hi.lo + lo.hi)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t wh = sdesc_sw128(stg + SO_REC + WS_WH + kk * 2048, 16384, 1024);
@@ -1202,18 +1206,9 @@ __global__ void __launch_bounds__(SO_NT, 1)
           mma_f16_tmem_a(tmem + SO_P, tmem + SO_XL + kk * 8, wh, id_p, 1);
         }
         mma_commit(&bar_p);
-        // the previous chunk's outputs must have been read out before the accumulators are reused
-        if (c > 0 && !(ok = mbar_wait_cycles(&bar_rd, par ^ 1u, a.err))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bq = sdesc_sw128(stg + SO_Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XH + kk * 8, bq, id_k, kk > 0);
-          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XL + kk * 8, bq, id_k, 1);
-        }
         if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
         tc_fence_after();
-        // X^T += R^T K, then O_intra^T = Wm^T M^T (hi.hi + hi.lo + lo.hi)
+        // X^T += R^T K
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bk = sdesc_sw128(stg + SO_K + kk * 2048, 8192, 1024);
@@ -1222,6 +1217,36 @@ __global__ void __launch_bounds__(SO_NT, 1)
           mma_f16_tmem_a(tmem + SO_X, pc + 16, bk, id_x, 1);
         }
         mma_commit(&bar_x);
+        mma_commit(&bar_empty[c & 1]);
+        if (c + 1 < nchunks && !(ok = stage_ready(c + 1))) break;
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (out_issuer) {
+    // the output products of every chunk, beside the state chain
+    if (lane == 0) {
+      const uint32_t id_k = idesc_f32acc(1, 1, 0, 0, 128, 64);  // A = TMEM pieces, B K-major (Q, M)
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const uint32_t par = (uint32_t)c & 1u;
+        const uint32_t stg = sb + (c & 1) * SO_STAGE;
+        // the chunk's state pieces are written (and its stage landed, which r1 follows)
+        if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
+        // the previous chunk's outputs must have been read out before the accumulators are reused
+        if (c > 0 && !(ok = mbar_wait_cycles(&bar_rd, par ^ 1u, a.err))) break;
+        tc_fence_after();
+        // O_inter^T = X^T Q^T (hi + lo; Q exact)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bq = sdesc_sw128(stg + SO_Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XH + kk * 8, bq, id_k, kk > 0);
+          mma_f16_tmem_a(tmem + SO_OI, tmem + SO_XL + kk * 8, bq, id_k, 1);
+        }
+        mma_commit(&bar_oi);
+        if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
+        tc_fence_after();
+        // O_intra^T = Wm^T M^T (hi.hi + hi.lo + lo.hi)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t mh = sdesc_sw128(stg + SO_M + kk * 32, 16, 1024);
@@ -1233,7 +1258,6 @@ __global__ void __launch_bounds__(SO_NT, 1)
         }
         mma_commit(&bar_o);
         mma_commit(&bar_empty[c & 1]);
-        if (c + 1 < nchunks && !(ok = stage_ready(c + 1))) break;
       }
       if (!ok) abort_flag = 1;
     }
@@ -1266,6 +1290,8 @@ __global__ void __launch_bounds__(SO_NT, 1)
       const int st = c & 1;
       const uint32_t par = (uint32_t)c & 1u;
       if (c > 0 && !(ok = mbar_wait_cycles(&bar_x, par ^ 1u, a.err))) break;  // previous update done
+      // and the previous chunk's inter-chunk output product has read the state pieces
+      if (c > 0 && !(ok = mbar_wait_cycles(&bar_oi, par ^ 1u, a.err))) break;
       if (!(ok = mbar_wait_cycles(&bar_full[st], ((uint32_t)c >> 1) & 1u, a.err))) break;
       tc_fence_after();
       const float *sR = s_sc[st];
@@ -1350,6 +1376,7 @@ __global__ void __launch_bounds__(SO_NT, 1)
   if (abort_flag && tid == 0) {
     for (int k = 0; k < 2; ++k) {
       mbar_wait_cycles(&bar_o, (uint32_t)k, nullptr, 100000000LL);
+      mbar_wait_cycles(&bar_oi, (uint32_t)k, nullptr, 100000000LL);
       mbar_wait_cycles(&bar_rd, (uint32_t)k, nullptr, 100000000LL);
       mbar_wait_cycles(&bar_x, (uint32_t)k, nullptr, 100000000LL);
       mbar_wait_cycles(&bar_p, (uint32_t)k, nullptr, 100000000LL);

@@ -46,11 +46,11 @@ BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S
 # the bench reports a figure only while those sources are unchanged, and null once they differ.
 TRAFFIC = {
     # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
-    "build_tc": {"bytes": 2_431_883_776, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
-                 "commit": "edc1dcb"},
+    "build_tc": {"bytes": 2_432_236_288, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7a72687bc0a9",
+                 "commit": "e0b2fb2"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
-    "build_outputs_tc": {"bytes": 5_339_999_232, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "bb105be507ae",
-                         "commit": "2fc0e60"},
+    "build_outputs_tc": {"bytes": 5_337_654_613, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7a72687bc0a9",
+                         "commit": "e0b2fb2"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
     "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
                            "digest": "6453c37efead", "commit": "1b1b1f2"},

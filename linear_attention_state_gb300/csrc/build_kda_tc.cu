@@ -546,7 +546,8 @@ constexpr int KNT = KNC + 64;    // + MMA warp + copy warp
 __global__ void __launch_bounds__(KNT, 1)
     chain_kda_kernel(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ KdaArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1, bar_r2, bar_p, bar_x;
+  // r1[b]: the state pieces of column block b written (block 0: each thread's first 32 columns)
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_r1[2], bar_r2, bar_p, bar_x;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -575,7 +576,8 @@ __global__ void __launch_bounds__(KNT, 1)
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
     }
-    mbar_init(&bar_r1, KNC);
+    mbar_init(&bar_r1[0], KNC);
+    mbar_init(&bar_r1[1], KNC);
     mbar_init(&bar_r2, KNC);
     mbar_init(&bar_p, 1);
     mbar_init(&bar_x, 1);
@@ -652,16 +654,24 @@ __global__ void __launch_bounds__(KNT, 1)
       for (int j = 0; j < nch && ok; ++j) {
         const uint64_t so = (j & 1) ? DST : 0;
         const uint32_t par = (uint32_t)j & 1u;
-        if (!(ok = mbar_wait_cycles(&bar_r1, par, a.err))) break;
-        tc_fence_after();
+        // P^T in two halves of the contraction, each as soon as its column block is split:
+        // block b holds rows i in [32 b, 32 b + 32) and [64 + 32 b, 96 + 32 b), so k-steps
+        // {0, 1, 4, 5} then {2, 3, 6, 7}
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t wh = dWH + so + kk * 128;
-          const uint64_t wl = dWL + so + kk * 128;
-          mma_f16_tmem_a(tmem + TP, tmem + TXH + kk * 8, wh, id_p, (half == 1 || kk > 0) ? 1u : 0u);
-          mma_f16_tmem_a(tmem + TP, tmem + TXH + kk * 8, wl, id_p, 1);
-          mma_f16_tmem_a(tmem + TP, tmem + TXL + kk * 8, wh, id_p, 1);
+        for (int blk = 0; blk < 2; ++blk) {
+          if (!(ok = mbar_wait_cycles(&bar_r1[blk], par, a.err))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 2 * blk + (q & 1) + 4 * (q >> 1);
+            const uint64_t wh = dWH + so + kk * 128;
+            const uint64_t wl = dWL + so + kk * 128;
+            mma_f16_tmem_a(tmem + TP, tmem + TXH + kk * 8, wh, id_p, (half == 1 || blk > 0 || q > 0) ? 1u : 0u);
+            mma_f16_tmem_a(tmem + TP, tmem + TXH + kk * 8, wl, id_p, 1);
+            mma_f16_tmem_a(tmem + TP, tmem + TXL + kk * 8, wh, id_p, 1);
+          }
         }
+        if (!ok) break;
         mma_commit(&bar_p);
         if (!(ok = mbar_wait_cycles(&bar_r2, par, a.err))) break;
         tc_fence_after();
@@ -674,9 +684,11 @@ __global__ void __launch_bounds__(KNT, 1)
           mma_f16_tmem_a(tmem + TX, pc, bkl, id_x, 1);
           mma_f16_tmem_a(tmem + TX, pc + 16, bkh, id_x, 1);
         }
-        if (j + 1 < nch && !(ok = stage_ready(j + 1))) break;
+        // The update's completion frees the state for the next split and this stage for the next
+        // copy; the next chunk's U products (S half) follow them, so the split does not wait for U.
         mma_commit(&bar_x);
         mma_commit(&bar_empty[j & 1]);
+        if (j + 1 < nch && !(ok = stage_ready(j + 1))) break;
       }
       if (!ok) abort_flag = 1;
     }
@@ -720,10 +732,10 @@ __global__ void __launch_bounds__(KNT, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) xv[q] *= gC[64 * part + cb + q];
         tmem_st32(tx + 64 * part + cb, xv);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_r1[cb / 32]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_r1);
       // (2) R^T = -(P^T - U^T): this thread's tokens [32 part, 32 part + 32) as 16 hi then 16 lo columns.
       if (!(ok = mbar_wait_sleep(&bar_p, par, a.err))) break;
       tc_fence_after();

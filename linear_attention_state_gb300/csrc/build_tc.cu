@@ -1359,6 +1359,12 @@ __global__ void __launch_bounds__(SO_NT, 1)
         readout(nchunks - 1);
       }
     }
+    // the last update has landed: its commit is the state MMA thread's, which the output products'
+    // commit does not order
+    if (ok && nchunks > 0) {
+      ok = mbar_wait_cycles(&bar_x, (uint32_t)(nchunks - 1) & 1u, a.err);
+      tc_fence_after();
+    }
     if (ok) {
       // S_{C|0}: X^T lane j holds column j; this thread's 64 rows i.
       float *out = a.S_out + ((size_t)s * a.H + h) * D * D;

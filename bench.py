@@ -46,19 +46,19 @@ BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S
 # the bench reports a figure only while those sources are unchanged, and null once they differ.
 TRAFFIC = {
     # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
-    "build_tc": {"bytes": 2_432_236_288, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7a72687bc0a9",
-                 "commit": "e0b2fb2"},
+    "build_tc": {"bytes": 2_431_951_360, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
+                 "commit": "e1375dd"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
-    "build_outputs_tc": {"bytes": 5_337_654_613, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7a72687bc0a9",
-                         "commit": "e0b2fb2"},
+    "build_outputs_tc": {"bytes": 5_337_207_296, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
+                         "commit": "e1375dd"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
     "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
                            "digest": "6453c37efead", "commit": "1b1b1f2"},
     "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
                    "commit": "1b1b1f2"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
-    "decay_kda": {"bytes": 3_971_162_965, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "ea58d4e3d555",
-                  "commit": "5a713f2"},
+    "decay_kda": {"bytes": 3_970_903_125, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "b914048c2809",
+                  "commit": "e1375dd"},
     # compose_pipe32_kernel / compose_pipe_kernel (the kernels composition without seam windows runs)
     # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each

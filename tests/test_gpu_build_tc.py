@@ -167,6 +167,48 @@ def test_fewer_units_than_sms_cut_several_times(family, gate_div):
     assert torch.equal(T[3], torch.eye(128, device=DEV).expand(H, 128, 128))
 
 
+@pytest.mark.parametrize("family,gate_div,with_split", [("delta", None, False), ("gated_delta", 1024.0, True)])
+def test_head_blocks_in_a_one_head_workspace(family, gate_div, with_split):
+    """A workspace that holds one head's records (and, with_split, the split schedule's slots for
+    one head's units) makes the build run over the heads one block at a time; every head is checked
+    against the oracle, and the result against the build with the full preferred workspace."""
+    lens = [640, 0, 64, 129, 1000]
+    H = 3
+    tok, bounds, T, S = run_case(family, lens, H, key=43, gate_div=gate_div)
+    one_head = hy.build_workspace_bytes(1, 128, len(lens), max(lens), family=family)
+    records = len(lens) * ((max(lens) + 63) // 64) * 49664
+    ws_bytes = one_head if with_split else records
+    assert ws_bytes >= records and ws_bytes < 2 * records
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    T1, S1 = hy.segment_build_batched(tok["k"], tok["v"], torch.tensor(bounds, device=DEV), tok["alpha"],
+                                      tok["beta"], family=family, ws=ws)
+    assert hy.stream_status() == 0
+    eT, eS = check(family, tok, bounds, T1, S1, H)
+    print(f"{family} head by head: max rel err T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+    for s, (b, e) in enumerate(bounds):
+        if e > b:
+            assert relerr(np64(S1[s]), np64(S[s])) <= 1e-4
+        else:
+            assert torch.equal(T1[s], torch.eye(128, device=DEV).expand(H, 128, 128))
+            assert float(S1[s].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("family,gate_div", [("delta", None), ("gated_delta", 1024.0)])
+def test_one_long_body_cut_into_many_pieces(family, gate_div):
+    """Two units of 32,768 tokens (512 chunks each): the split schedule cuts each into about 64
+    pieces of eight chunks, and the CTA holding a unit's head composes some 63 published pairs onto
+    it in order.  Over the whole body T_C decays far below one even with a = 1 or slow decay, so the
+    check rests on S_{C|0}: every composed piece's T_B (512 tokens, far from underflow) multiplies
+    the S of the pieces before it."""
+    lens = [32768]
+    H = 2
+    tok, bounds, T, S = run_case(family, lens, H, key=47, gate_div=gate_div, gap=3)
+    eT, eS = check(family, tok, bounds, T, S, H)
+    print(f"{family} one 32k body in pieces: max rel err T {eT:.2e} S {eS:.2e}")
+    assert eT <= TOL_BF16 and eS <= TOL_BF16
+
+
 def test_tensor_core_path_agrees_with_recurrent_path(monkeypatch):
     lens = [300, 64, 5]
     H = 2

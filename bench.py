@@ -56,6 +56,9 @@ TRAFFIC = {
                            "digest": "6453c37efead", "commit": "1b1b1f2"},
     "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
                    "commit": "1b1b1f2"},
+    # wy_prep_kernel + chain_tc_kernel on the decay-family shape (--decay-only, plain gated delta)
+    "decay_gated_delta": {"bytes": 2_690_876_757, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
+                          "commit": "2a0698c"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
     "decay_kda": {"bytes": 3_970_903_125, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "b914048c2809",
                   "commit": "e1375dd"},
@@ -387,7 +390,7 @@ def decay_build_measure(steps, warmup, dev, peaks):
             entry["roofline"] = {"bound": "tensor", "achieved": fl / tb / 1e12, "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": fl / tb / 1e12 / peaks["bf16_tflops"],
                                  "flop_per_unit": FLOP_PER_HEAD_TOKEN_WY,
-                                 "traffic": traffic("decay_kda") if fam == "kda" else None,
+                                 "traffic": traffic("decay_kda" if fam == "kda" else "decay_gated_delta"),
                                  "kernel": ("kda_prep_kernel + chain_kda_kernel" if fam == "kda" else
                                             "wy_prep_kernel + chain_tc_kernel")}
         elif fam == "kda":

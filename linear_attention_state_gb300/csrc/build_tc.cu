@@ -969,14 +969,27 @@ __global__ void __launch_bounds__(NT2, 1)
     uint8_t *xlo = sm + OFF_XLO + half * 32768 + part * 16384;
     const bool idle = T_ONLY && half == 1;  // the T-only chain has no S half
     if (!idle) conv_empty_units(a);
-    // Only the current unit and the step where its piece ends stay live across the chunk loop.
+    // The current piece and the next busy one stay in registers as a unit index, kind | n_fix << 2
+    // and (next) length: the next is looked up during a piece's first step, while its P^T products
+    // run, so a piece boundary does no lookup of its own (the walks read the segment bounds from
+    // global memory).
     bool ok = true;
     const int my_steps = idle ? 0 : J;
-    int u = 0, piece_end = 0;
+    int u = 0, piece_end = 0, cur_kf = 0, nu = 0, nxt_kf = 0, nxt_len = 0;
+    bool need_next = false;
+    auto look_ahead = [&]() {
+      need_next = false;
+      nu = next_busy_unit(a, u + 1);
+      const Piece q = piece_at(a, nu);
+      nxt_kf = q.kind | (q.n_fix << 2);
+      nxt_len = q.c_hi - q.c_lo;
+    };
     if (my_steps > 0) {
       u = next_busy_unit(a, units_begin(a));
-      const Piece p = piece_at(a, u);
-      piece_end = p.c_hi - p.c_lo;
+      const Piece q = piece_at(a, u);
+      cur_kf = q.kind | (q.n_fix << 2);
+      piece_end = q.c_hi - q.c_lo;
+      need_next = piece_end < my_steps;
       conv_init_x(tx);
     }
     for (int j = 0; j < my_steps; ++j) {
@@ -1016,6 +1029,9 @@ __global__ void __launch_bounds__(NT2, 1)
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&bar_r1[half]);
+        // (the T-only chain, whose units are the long request bodies, looks up at the boundary)
+        if constexpr (!T_ONLY)
+          if (need_next) look_ahead();
         // (2) R^T = -(P^T - U^T) diag(exp(G_C - G_t)) -> bf16 hi/lo pieces in place: this thread's
         // columns t in [32 part, 32 part + 32) become 16 hi columns then 16 lo columns.
         if (!(ok = mbar_wait_sleep(&bar_p[half], par, a.err))) break;
@@ -1043,7 +1059,15 @@ __global__ void __launch_bounds__(NT2, 1)
       // ---- end of a piece: the half's last update has landed
       if (ok) ok = mbar_wait_cycles(&bar_x[half], (uint32_t)j & 1u, a.err);
       tc_fence_after();
-      const Piece p = piece_at(a, u);
+      Piece p{};
+      if constexpr (T_ONLY) {
+        p = piece_at(a, u);
+      } else {
+        p.s = u / a.Hb;
+        p.hh = u % a.Hb;
+        p.kind = cur_kf & 3;
+        p.n_fix = cur_kf >> 2;
+      }
       if (p.kind == PIECE_WHOLE) {
         if (ok) conv_write_x(tx, unit_out(a, p, half));
       } else if constexpr (!T_ONLY) {
@@ -1053,9 +1077,17 @@ __global__ void __launch_bounds__(NT2, 1)
           ok = conv_compose_head(a, p, tx, txp, xlo, sm, &bar_r1[half], &bar_x[half], J, ok);
       }
       if (j + 1 < my_steps) {
-        u = next_busy_unit(a, u + 1);
-        const Piece q = piece_at(a, u);
-        piece_end += q.c_hi - q.c_lo;
+        if constexpr (T_ONLY) {
+          u = next_busy_unit(a, u + 1);
+          const Piece q = piece_at(a, u);
+          piece_end += q.c_hi - q.c_lo;
+        } else {
+          if (need_next) look_ahead();  // the piece's steps ended early (an error): look it up now
+          u = nu;
+          cur_kf = nxt_kf;
+          piece_end += nxt_len;
+          need_next = piece_end < my_steps;
+        }
         if (ok) conv_init_x(tx);  // the previous piece's X^T has been read out
       }
     }

@@ -46,19 +46,19 @@ BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S
 # the bench reports a figure only while those sources are unchanged, and null once they differ.
 TRAFFIC = {
     # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
-    "build_tc": {"bytes": 2_431_951_360, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
-                 "commit": "e1375dd"},
+    "build_tc": {"bytes": 2_428_635_733, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+                 "commit": "606b45c"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
-    "build_outputs_tc": {"bytes": 5_337_207_296, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
-                         "commit": "e1375dd"},
+    "build_outputs_tc": {"bytes": 5_337_370_283, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+                         "commit": "606b45c"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
     "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
                            "digest": "6453c37efead", "commit": "1b1b1f2"},
     "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
                    "commit": "1b1b1f2"},
     # wy_prep_kernel + chain_tc_kernel on the decay-family shape (--decay-only, plain gated delta)
-    "decay_gated_delta": {"bytes": 2_690_876_757, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "7c1a397c8739",
-                          "commit": "2a0698c"},
+    "decay_gated_delta": {"bytes": 2_676_607_403, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+                          "commit": "606b45c"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
     "decay_kda": {"bytes": 3_970_903_125, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "b914048c2809",
                   "commit": "e1375dd"},

@@ -115,20 +115,22 @@ __device__ __forceinline__ void ksplit2(float a, float b, uint32_t &hi, uint32_t
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel 1: per (segment, chunk, head).
+// Kernel 1: per (segment, chunk, head).  Shared memory is held to 72 KB, three CTAs per SM: the
+// gates are read straight into registers (thread = key channel), and the key channels are worked
+// through in two halves of 64, each with its key box and its E (or G) half in shared memory; the
+// Gram accumulates over the halves, (K o E) is kept whole for Wk^T, (K o F) one half at a time.
 constexpr int LS = 68;  // row stride of L (floats)
-constexpr uint32_t KP_K = 0;         // key chunk, two [64 t][64 i] boxes (TMA)
-constexpr uint32_t KP_G = 16384;     // gates [64 t][128 i] fp32 (TMA), then G in place; then L, A,
-                                     // A diag(b) hi and lo (tensor-core Gram)
-constexpr uint32_t KP_P1H = 49152;   // (K o E) hi, lo: the Gram's first operand and Wk^T's; then Wk^T
-constexpr uint32_t KP_P1L = 65536;
-constexpr uint32_t KP_P2H = 81920;   // (K o F) hi, lo: the Gram's second operand; L, A, ... (fallback)
-constexpr uint32_t KP_P2L = 98304;
-constexpr uint32_t KP_SMEM = 114688;  // 1024-aligned base (declared alignment), no slack
+constexpr uint32_t KP_KB = 0;        // key box of the current channel half, [64 t][64 i] bf16 (TMA)
+constexpr uint32_t KP_EH = 8192;     // E (or G) of the current channel half, fp32 [64 t][64 i];
+                                     // after both halves L, A, then A diag(b) hi and lo (from KP_KB)
+constexpr uint32_t KP_P1H = 24576;   // (K o E) hi, lo: two boxes each; the Gram's first operand and
+constexpr uint32_t KP_P1L = 40960;   // Wk^T's; then Wk^T hi, lo staged for the store
+constexpr uint32_t KP_P2H = 57344;   // (K o F) hi, lo of the current half: the Gram's second operand;
+constexpr uint32_t KP_P2L = 65536;   // fallback: L (s < t) accumulated over the halves, row stride 64
+constexpr uint32_t KP_SMEM = 73728;  // 1024-aligned base (declared alignment), no slack
 
-__global__ void __launch_bounds__(NT, 2)
-    kda_prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapG,
-                    const __grid_constant__ KdaArgs a) {
+__global__ void __launch_bounds__(NT, 3)
+    kda_prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ KdaArgs a) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
@@ -154,154 +156,189 @@ __global__ void __launch_bounds__(NT, 2)
     mbar_init(&bar_mma, 1);
     mbar_fence_init();
     ok_flag = 1;
-    mbar_arrive_expect_tx(&bar_tma, 16384 + 32768);
-    tma_load_2d(sm + KP_K, &mapK, &bar_tma, h * D, (int)t0);
-    tma_load_2d(sm + KP_K + 8192, &mapK, &bar_tma, h * D + 64, (int)t0);
-    tma_load_2d(sm + KP_G, &mapG, &bar_tma, h * D, (int)t0);
+    mbar_arrive_expect_tx(&bar_tma, 8192);
+    tma_load_2d(sm + KP_KB, &mapK, &bar_tma, h * D, (int)t0);
   }
   if (warp == 0) {
     tmem_alloc(&tmem_slot, 64);
     tmem_relinquish();
   }
   if (tid < C) sBv[tid] = tid < nvalid ? a.beta[(t0 + tid) * a.H + h] : 0.f;
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-  // every thread reads the key chunk and the gates with plain loads below, so every thread waits
-  if (!mbar_wait_cycles(&bar_tma, 0, tid == 0 ? a.err : nullptr)) ok_flag = 0;
-  __syncthreads();
-  if (!ok_flag) {
-    if (warp == 0) tmem_dealloc(tmem, 64);
-    return;
-  }
-  const uint8_t *sK = sm + KP_K;
-  float *sG = reinterpret_cast<float *>(sm + KP_G);  // [64 t][128 i]
 
   // Thread = key channel i: Gamma_t = running product of the channel's gates (tokens past the body
-  // count as gate 1), in registers.  Gamma_0 / Gamma_{C-1} <= 1 / Gamma_{C-1}: factors around the
-  // middle stay within 2^100 when Gamma_{C-1} >= 2^-100 in every channel (separable).  Then the tile
-  // holds E_t = Gamma_t / M with M = 2^round(log2 Gamma_m) at the middle token, a power of two, so
-  // E_t and the rescaling of Wk^T's rows by M are exact.  Otherwise (the fallback) the tile holds
-  // the log2-cumsum G_t of the gates, and every factor is taken as one exponential.
-  float GamC, wk_scale;
-  bool separable;
-  {
-    float gv[C];
+  // count as gate 1), in registers, the gates read row by row (each row coalesced over the
+  // channels).  Gamma_0 / Gamma_{C-1} <= 1 / Gamma_{C-1}: factors around the middle stay within
+  // 2^100 when Gamma_{C-1} >= 2^-100 in every channel (separable).  Then E_t = Gamma_t / M with
+  // M = 2^round(log2 Gamma_m) at the middle token, a power of two, so E_t and the rescaling of
+  // Wk^T's rows by M are exact.  Otherwise (the fallback) G_t, the log2-cumsum of the gates, and
+  // every factor is one exponential.
+  const int ch = tid;
+  const float *gp = a.alpha + ((size_t)t0 * a.H + h) * D + ch;
+  const size_t gstride = (size_t)a.H * D;
+  float gv[C];
 #pragma unroll
-    for (int t = 0; t < C; ++t) gv[t] = sG[t * D + tid];
+  for (int t = 0; t < C; ++t) gv[t] = t < nvalid ? __ldg(gp + (size_t)t * gstride) : 1.f;
+  float GamC;
+  {
     float pr = 1.f;
 #pragma unroll
     for (int t = 0; t < C; ++t) {
-      pr = t < nvalid ? pr * gv[t] : pr;
+      pr *= gv[t];
       gv[t] = pr;
     }
     GamC = pr;
-    separable = __syncthreads_and(GamC >= 0x1p-100f) != 0;
-    if (separable) {
-      const int em = (int)rintf(log2f(gv[C / 2]));
-      const float Minv = ldexpf(1.f, -em);
-      wk_scale = ldexpf(1.f, em);
-#pragma unroll
-      for (int t = 0; t < C; ++t) sG[t * D + tid] = gv[t] * Minv;
-    } else {
-      wk_scale = 1.f;
-      float g = 0.f;
-#pragma unroll 16
-      for (int t = 0; t < C; ++t) {
-        g += t < nvalid ? log2f(sG[t * D + tid]) : 0.f;
-        sG[t * D + tid] = g;
-      }
-    }
   }
-  __syncthreads();  // the pass below reads other channels' entries
-
-  // One pass over the chunk, eight channels of one token per item: the Gram's operands
-  // (K o E) (also Wk^T's, rescaled by M per channel afterwards) and (K o F), F = 1 / E, in hi and
-  // lo pieces, and Khat = K o Gamma_C / Gamma = (K o F) E_{C-1} straight to the record (the quotient
-  // by the fast reciprocal: its error, about 2^-22, is far below the hi + lo split's).  A thread's
-  // items all cover the same eight channels (8 c8 ..), whose last-token entries are read once.
-  // Fallback: (K o E) = K o 2^G, Khat = K o 2^{G_{C-1} - G}.
-  uint8_t *rec = krec(a, s, c, hh);
-  const int c8 = tid & 15;
-  float L8[8];
-  {
-    const float4 e0 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8);
-    const float4 e1 = *reinterpret_cast<const float4 *>(sG + (C - 1) * D + 8 * c8 + 4);
-    L8[0] = e0.x; L8[1] = e0.y; L8[2] = e0.z; L8[3] = e0.w;
-    L8[4] = e1.x; L8[5] = e1.y; L8[6] = e1.z; L8[7] = e1.w;
-  }
-#pragma unroll 2
-  for (int j = 0; j < 8; ++j) {
-    const int t = (tid >> 4) + 8 * j;  // token of item tid + 128 j
-    const uint32_t off = (uint32_t)(c8 >> 3) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(c8 & 7));
-    const uint4 kr = *reinterpret_cast<const uint4 *>(sK + off);
-    const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
-    const float4 g0 = *reinterpret_cast<const float4 *>(sG + t * D + 8 * c8);
-    const float4 g1 = *reinterpret_cast<const float4 *>(sG + t * D + 8 * c8 + 4);
-    const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    float k8[8], p1[8], p2[8], kh[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 kv = __bfloat1622float2(k2[q]);
-      k8[2 * q] = kv.x;
-      k8[2 * q + 1] = kv.y;
-    }
-    if (separable) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        p1[q] = k8[q] * G8[q];
-        p2[q] = __fdividef(k8[q], G8[q]);
-        kh[q] = p2[q] * L8[q];
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        p1[q] = k8[q] * exp2f(G8[q]);
-        p2[q] = 0.f;
-        kh[q] = k8[q] * exp2f(L8[q] - G8[q]);
-      }
-    }
-    uint4 hi, lo;
-    ksplit8(p1, hi, lo);
-    *reinterpret_cast<uint4 *>(sm + KP_P1H + off) = hi;
-    *reinterpret_cast<uint4 *>(sm + KP_P1L + off) = lo;
-    if (separable) {
-      ksplit8(p2, hi, lo);
-      *reinterpret_cast<uint4 *>(sm + KP_P2H + off) = hi;
-      *reinterpret_cast<uint4 *>(sm + KP_P2L + off) = lo;
-    }
-    ksplit8(kh, hi, lo);
-    *reinterpret_cast<uint4 *>(rec + KR_KH + off) = hi;
-    *reinterpret_cast<uint4 *>(rec + KR_KL + off) = lo;
-  }
-  reinterpret_cast<float *>(rec + KR_GC)[tid] = GamC;
-  fence_proxy_async();
-  __syncthreads();
-
-  float *sL = reinterpret_cast<float *>(sm + (separable ? KP_G : KP_P2H));
-  float *sA = sL;
-  float *sT = sL + 32;
+  const bool separable = __syncthreads_and(GamC >= 0x1p-100f) != 0;
+  float wk_scale = 1.f;
   if (separable) {
+    const int em = (int)rintf(log2f(gv[C / 2]));
+    const float Minv = ldexpf(1.f, -em);
+    wk_scale = ldexpf(1.f, em);
+#pragma unroll
+    for (int t = 0; t < C; ++t) gv[t] *= Minv;
+  } else {
+    float g = 0.f;
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+      g += t < nvalid ? log2f(__ldg(gp + (size_t)t * gstride)) : 0.f;
+      gv[t] = g;
+    }
+  }
+  uint8_t *rec = krec(a, s, c, hh);
+  reinterpret_cast<float *>(rec + KR_GC)[ch] = GamC;
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;  // written before the barrier above
+  const uint8_t *sK = sm + KP_KB;
+  float *sE = reinterpret_cast<float *>(sm + KP_EH);  // [64 t][64 i], the current half
+  float *sLacc = reinterpret_cast<float *>(sm + KP_P2H);  // fallback: [64 t][64 s]
+
+  // The two channel halves.  Per half: E (or G) to shared memory, then one pass over the half's
+  // 64 x 64 entries, eight channels of one token per item: the Gram's operands (K o E) (also
+  // Wk^T's, rescaled by M per channel afterwards) and (K o F), F = 1 / E, in hi and lo pieces, and
+  // Khat = K o Gamma_C / Gamma = (K o F) E_{C-1} straight to the record (the quotient by the fast
+  // reciprocal: its error, about 2^-22, is far below the hi + lo split's); then the half's Gram
+  // products.  Fallback: (K o E) = K o 2^G, Khat = K o 2^{G_{C-1} - G}, and the half's share of
+  // L_ts = b_t sum_i k_ti k_si 2^{G_ti - G_si} term by term.
+#pragma unroll 1
+  for (int hf = 0; hf < 2; ++hf) {
+    if ((ch >> 6) == hf) {
+#pragma unroll
+      for (int t = 0; t < C; ++t) sE[t * 64 + (ch & 63)] = gv[t];
+    }
+    __syncthreads();
+    // every thread reads the key box (and, before the second half's pass overwrites (K o F), the
+    // first half's Gram products must have read it)
+    bool got = mbar_wait_cycles(&bar_tma, (uint32_t)hf, tid == 0 ? a.err : nullptr);
+    if (separable && hf == 1) got = got && mbar_wait_cycles(&bar_mma, 0u, tid == 0 ? a.err : nullptr);
+    if (!got) ok_flag = 0;
+    __syncthreads();
+    if (!ok_flag) break;
+    const int c8 = tid & 7;  // channel octet within the half
+    float L8[8];
+    {
+      const float4 e0 = *reinterpret_cast<const float4 *>(sE + (C - 1) * 64 + 8 * c8);
+      const float4 e1 = *reinterpret_cast<const float4 *>(sE + (C - 1) * 64 + 8 * c8 + 4);
+      L8[0] = e0.x; L8[1] = e0.y; L8[2] = e0.z; L8[3] = e0.w;
+      L8[4] = e1.x; L8[5] = e1.y; L8[6] = e1.z; L8[7] = e1.w;
+    }
+#pragma unroll 2
+    for (int j = 0; j < 4; ++j) {
+      const int t = (tid >> 3) + 16 * j;  // token of item tid + 128 j
+      const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)c8);
+      const uint4 kr = *reinterpret_cast<const uint4 *>(sK + off);
+      const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
+      const float4 g0 = *reinterpret_cast<const float4 *>(sE + t * 64 + 8 * c8);
+      const float4 g1 = *reinterpret_cast<const float4 *>(sE + t * 64 + 8 * c8 + 4);
+      const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      float k8[8], p1[8], p2[8], kh[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 kv = __bfloat1622float2(k2[q]);
+        k8[2 * q] = kv.x;
+        k8[2 * q + 1] = kv.y;
+      }
+      if (separable) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          p1[q] = k8[q] * G8[q];
+          p2[q] = __fdividef(k8[q], G8[q]);
+          kh[q] = p2[q] * L8[q];
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          p1[q] = k8[q] * exp2f(G8[q]);
+          p2[q] = 0.f;
+          kh[q] = k8[q] * exp2f(L8[q] - G8[q]);
+        }
+      }
+      const uint32_t boff = (uint32_t)hf * 8192u + off;
+      uint4 hi, lo;
+      ksplit8(p1, hi, lo);
+      *reinterpret_cast<uint4 *>(sm + KP_P1H + boff) = hi;
+      *reinterpret_cast<uint4 *>(sm + KP_P1L + boff) = lo;
+      if (separable) {
+        ksplit8(p2, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + KP_P2H + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + KP_P2L + off) = lo;
+      }
+      ksplit8(kh, hi, lo);
+      *reinterpret_cast<uint4 *>(rec + KR_KH + boff) = hi;
+      *reinterpret_cast<uint4 *>(rec + KR_KL + boff) = lo;
+    }
+    if (!separable) {
+      // thread pair (t, half of the half's channels), adjacent lanes: sum over 32 channels each,
+      // the pair reduced by a shuffle; only the strict lower triangle is kept (the inverse reads
+      // nothing else)
+      const int t = tid >> 1, ih = tid & 1;
+      for (int s2 = 0; s2 < C; ++s2) {
+        float acc = 0.f;
+        if (s2 < t) {
+          for (int i = 32 * ih; i < 32 * ih + 32; ++i) {
+            const float kk = kt_get(sK, t, i) * kt_get(sK, s2, i);
+            acc = fmaf(kk, exp2f(sE[t * 64 + i] - sE[s2 * 64 + i]), acc);
+          }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (ih == 0 && s2 < t) sLacc[t * 64 + s2] = hf ? sLacc[t * 64 + s2] + acc : acc;
+      }
+    }
+    fence_proxy_async();
+    __syncthreads();  // the half's operands are written; its key box and E are read
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id = idesc_f32acc(1, 1, 0, 0, 64, 64);
-      const uint32_t p1h = smem_u32(sm + KP_P1H), p1l = smem_u32(sm + KP_P1L);
-      const uint32_t p2h = smem_u32(sm + KP_P2H), p2l = smem_u32(sm + KP_P2L);
+      if (separable) {
+        // Gram += (K o E)(K o F)^T over the half's channels (M = 64, N = 64, K = 64); three products
+        const uint32_t id = idesc_f32acc(1, 1, 0, 0, 64, 64);
+        const uint32_t p1h = smem_u32(sm + KP_P1H) + hf * 8192, p1l = smem_u32(sm + KP_P1L) + hf * 8192;
+        const uint32_t p2h = smem_u32(sm + KP_P2H), p2l = smem_u32(sm + KP_P2L);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t o = (kk >> 2) * 8192 + (kk & 3) * 32;
-        const uint64_t ah = sdesc_sw128(p1h + o, 16, 1024), al = sdesc_sw128(p1l + o, 16, 1024);
-        const uint64_t bh = sdesc_sw128(p2h + o, 16, 1024), bl = sdesc_sw128(p2l + o, 16, 1024);
-        mma_f16(tmem, ah, bh, id, kk > 0);
-        mma_f16(tmem, ah, bl, id, 1);
-        mma_f16(tmem, al, bh, id, 1);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t o = kk * 32;
+          const uint64_t ah = sdesc_sw128(p1h + o, 16, 1024), al = sdesc_sw128(p1l + o, 16, 1024);
+          const uint64_t bh = sdesc_sw128(p2h + o, 16, 1024), bl = sdesc_sw128(p2l + o, 16, 1024);
+          mma_f16(tmem, ah, bh, id, (hf | kk) != 0);
+          mma_f16(tmem, ah, bl, id, 1);
+          mma_f16(tmem, al, bh, id, 1);
+        }
+        mma_commit(&bar_mma);
       }
-      mma_commit(&bar_mma);
-      if (!mbar_wait_cycles(&bar_mma, 0, a.err)) ok_flag = 0;
+      if (hf == 0) {
+        // the second key box, into the first one's buffer (all of its reads are done)
+        mbar_arrive_expect_tx(&bar_tma, 8192);
+        tma_load_2d(sm + KP_KB, &mapK, &bar_tma, h * D + 64, (int)t0);
+      }
     }
-    __syncthreads();  // the MMAs have read the operands; G (under L) is no longer needed
-    tc_fence_after();
-    if (ok_flag) {
+  }
+  if (separable && tid == 0 && ok_flag && !mbar_wait_cycles(&bar_mma, 1u, a.err)) ok_flag = 0;
+  __syncthreads();  // the Gram (or the fallback's L) is complete
+  tc_fence_after();
+
+  float *sL = reinterpret_cast<float *>(sm + KP_KB);  // over the key box and E, both read
+  float *sA = sL;
+  float *sT = sL + 32;
+  if (ok_flag) {
+    if (separable) {
       // L_ts = b_t Gram_ts (s < t).  Gram row t sits in lane 32 (t / 16) + t % 16 (16x256b load).
       const int ta = warp * 16 + (lane >> 2), tb = ta + 8, cq = 2 * (lane & 3);
       float v[32];
@@ -315,22 +352,12 @@ __global__ void __launch_bounds__(NT, 2)
         *reinterpret_cast<float2 *>(sL + tb * LS + sc) =
             make_float2(sc < tb ? bb * v[4 * m + 2] : 0.f, sc + 1 < tb ? bb * v[4 * m + 3] : 0.f);
       }
-    }
-  } else {
-    // L_ts = b_t sum_i k_ti k_si 2^{G_ti - G_si} term by term: thread pair (t, half of the channels).
-    const int t = tid & 63, ih = tid >> 6;
-    float *red = sT;  // rows 0..31, columns 32..63 of L's frame (never part of L) hold partial sums
-    for (int s2 = 0; s2 < C; ++s2) {
-      float acc = 0.f;
-      if (s2 < t) {
-        for (int i = 64 * ih; i < 64 * ih + 64; ++i)
-          acc = fmaf(kt_get(sK, t, i) * kt_get(sK, s2, i), exp2f(sG[t * D + i] - sG[s2 * D + i]), acc);
+    } else {
+      // L_ts = b_t (sum over both halves), s < t, from the accumulated rows
+      for (int e = tid; e < C * C; e += NT) {
+        const int t = e >> 6, s2 = e & 63;
+        if (s2 < t) sL[t * LS + s2] = sBv[t] * sLacc[t * 64 + s2];
       }
-      if (ih == 1) red[(t & 31) * LS + (t >> 5) * 16 + (s2 & 15)] = acc;
-      __syncthreads();
-      // only the strict lower triangle is written (the inverse reads nothing else)
-      if (ih == 0 && s2 < t) sL[t * LS + s2] = sBv[t] * (acc + red[(t & 31) * LS + (t >> 5) * 16 + (s2 & 15)]);
-      __syncthreads();
     }
   }
   __syncthreads();
@@ -441,7 +468,7 @@ __global__ void __launch_bounds__(NT, 2)
 
   // A diag(b) split hi + lo: K-major [64 t][64 s] tiles, to shared memory (over A, once all of A
   // is read) for the Wk^T product, and negated to the record for the chain's U product.
-  uint8_t *ab_tiles = reinterpret_cast<uint8_t *>(sL);  // 1024-aligned: KP_G or KP_P2H
+  uint8_t *ab_tiles = reinterpret_cast<uint8_t *>(sL);  // 1024-aligned: KP_KB
   uint4 abh[4], abl[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -492,8 +519,9 @@ __global__ void __launch_bounds__(NT, 2)
       mma_f16(tmem, akl, bh, id, 1);
     }
     mma_commit(&bar_mma);
-    // the Gram, when formed on the tensor cores, took the barrier's first phase
-    if (!mbar_wait_cycles(&bar_mma, separable ? 1u : 0u, a.err)) ok_flag = 0;
+    // the Gram, when formed on the tensor cores, took the barrier's first two phases: this is
+    // phase 2 then (or 0), parity 0 either way
+    if (!mbar_wait_cycles(&bar_mma, 0u, a.err)) ok_flag = 0;
   }
   __syncthreads();
   tc_fence_after();
@@ -831,11 +859,9 @@ cudaError_t launch_build_kda_tc(const RecurrentArgs &r, void *ws, size_t ws_byte
   a.ws = static_cast<uint8_t *>(ws);
   a.err = r.err;
   const uint64_t n_tok = r.seg.n_tokens < 0 ? (uint64_t)1 << 31 : (uint64_t)r.seg.n_tokens;
-  CUtensorMap mk, mv, mg;
+  CUtensorMap mk, mv;
   if (!make_tmap_bf16_2d(&mk, r.src.k, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
     return cudaErrorInvalidValue;
-  // channel gates [tokens, H, D] fp32: one [64 t][128 i] box per chunk and head
-  if (!make_tmap_f32_rows(&mg, r.src.alpha, n_tok, (uint64_t)r.H * D, 128, 64)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&mv, r.src.v, n_tok, (uint64_t)r.H * D, (uint64_t)r.H * D, 64, 64))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KP_SMEM);
@@ -848,7 +874,7 @@ cudaError_t launch_build_kda_tc(const RecurrentArgs &r, void *ws, size_t ws_byte
     const long long g1 = (long long)r.n_seg * a.max_chunks * a.Hb;
     const long long g2 = 2LL * r.n_seg * a.Hb;
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kda_prep_kernel<<<(unsigned)g1, NT, KP_SMEM, st>>>(mk, mg, a);
+    kda_prep_kernel<<<(unsigned)g1, NT, KP_SMEM, st>>>(mk, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     chain_kda_kernel<<<(unsigned)g2, KNT, KC_SMEM, st>>>(mv, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

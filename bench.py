@@ -60,8 +60,8 @@ TRAFFIC = {
     "decay_gated_delta": {"bytes": 2_676_607_403, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
                           "commit": "606b45c"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
-    "decay_kda": {"bytes": 3_970_903_125, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "b914048c2809",
-                  "commit": "e1375dd"},
+    "decay_kda": {"bytes": 3_970_410_325, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9f51d8f1e755",
+                  "commit": "6d2df0b"},
     # compose_pipe32_kernel / compose_pipe_kernel (the kernels composition without seam windows runs)
     # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each

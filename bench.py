@@ -19,6 +19,7 @@ import argparse
 import functools
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,53 +42,65 @@ FLOP_PER_HEAD_TOKEN_KDA_RECURRENT = FLOP_PER_HEAD_TOKEN_RECURRENT + D * (2 * D) 
 BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S_{C|0}, fp32
 
 # Captured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch, from the ncu
-# captures summarised under profiles/.  Each entry carries the digest of the kernel sources it was
-# captured on (sha1 of the listed csrc files, first 12 hex digits) and the commit of the capture;
-# the bench reports a figure only while those sources are unchanged, and null once they differ.
+# captures summarised under profiles/.  Each entry carries the digest of the kernel code it was
+# captured on (sha1 of the listed csrc files without comments and with whitespace runs made one
+# space, first 12 hex digits) and the commit of the capture; the bench reports a figure only while
+# that code is unchanged, and null once it differs.
 TRAFFIC = {
     # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
-    "build_tc": {"bytes": 2_428_635_733, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+    "build_tc": {"bytes": 2_428_635_733, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
                  "commit": "606b45c"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
-    "build_outputs_tc": {"bytes": 5_337_370_283, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+    "build_outputs_tc": {"bytes": 5_337_370_283, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
                          "commit": "606b45c"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
     "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
-                           "digest": "6453c37efead", "commit": "1b1b1f2"},
-    "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "6453c37efead",
+                           "digest": "75f0a1f85a8e", "commit": "1b1b1f2"},
+    "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "75f0a1f85a8e",
                    "commit": "1b1b1f2"},
     # wy_prep_kernel + chain_tc_kernel on the decay-family shape (--decay-only, plain gated delta)
-    "decay_gated_delta": {"bytes": 2_676_607_403, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "c4402767e0ae",
+    "decay_gated_delta": {"bytes": 2_676_607_403, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
                           "commit": "606b45c"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
-    "decay_kda": {"bytes": 3_970_410_325, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "9f51d8f1e755",
+    "decay_kda": {"bytes": 3_970_410_325, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "1ede637113ef",
                   "commit": "6d2df0b"},
     # compose_pipe32_kernel / compose_pipe_kernel (the kernels composition without seam windows runs)
     # on the warm-cache workload (fp32 and bf16 pools):
     # captured at 4 layers (128 heads, --compose-layers 4) and scaled by 7.5 to 960 heads (each
     # head's pool entries and requests are independent, the grid head-major)
     "compose_f32": {"bytes": 46_755_327_360, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                    "digest": "8c3124594fff", "commit": "ae10944"},
+                    "digest": "b2832f896031", "commit": "ae10944"},
     "compose_bf16": {"bytes": 19_951_943_680, "src": ("compose_pipe.cu", "tc_ptx.cuh"),
-                     "digest": "8c3124594fff", "commit": "ae10944"},
+                     "digest": "b2832f896031", "commit": "ae10944"},
     # compose_pipe32_kernel in scan mode, 64 pairs: captured at 128 heads (--scan-heads 128) and
     # scaled by 7.5 to 960 heads
-    "scan": {"bytes": 15_826_974_720, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "8c3124594fff",
+    "scan": {"bytes": 15_826_974_720, "src": ("compose_pipe.cu", "tc_ptx.cuh"), "digest": "b2832f896031",
              "commit": "ae10944"},
     # staged RoPE shift and state re-rotation
-    "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "59ea01fe4941",
+    "rope_shift_32768x8x128_bf16": {"bytes": 82_962_944, "src": ("boundary.cu",), "digest": "12e85b19d684",
                                     "commit": "ae9cc2f"},
-    "state_rerotate_64x32_128x128_fp32": {"bytes": 206_485_504, "src": ("boundary.cu",), "digest": "59ea01fe4941",
+    "state_rerotate_64x32_128x128_fp32": {"bytes": 206_485_504, "src": ("boundary.cu",), "digest": "12e85b19d684",
                                           "commit": "ae9cc2f"},
 }
 
 
+_CODE_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def code_text(src: str) -> str:
+    """A source's code alone: comments dropped (string and character literals kept as they are) and
+    every run of whitespace made one space, so that comment or layout edits keep the digest."""
+    out = _CODE_TOKENS.sub(lambda m: " " if m.group(0)[0] == "/" else m.group(0), src)
+    return " ".join(out.split())
+
+
 def src_digest(names) -> str:
+    """sha1 (first 12 hex digits) of the listed csrc files' code (see code_text)."""
     import hashlib
     h = hashlib.sha1()
     for n in names:
-        with open(os.path.join(ROOT, "linear_attention_state_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "linear_attention_state_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:12]
 
 

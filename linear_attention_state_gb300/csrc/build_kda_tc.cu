@@ -16,11 +16,13 @@
 // each of those products takes hi and lo pieces; the state's rows are scaled by the vector Gamma_C.
 //
 // Two kernels per block of heads:
-//   kda_prep_kernel  (one CTA per chunk and head): gates and their per-channel log-cumsum, the
-//     decayed Gram on tcgen05 (M = 64, three split products), L, A = (I + L)^{-1} in fp32 (the same
-//     blocked inverse as the gated-delta build), Wk^T = (K o Gamma)^T (A diag(b))^T on tcgen05, and
-//     Khat.  Stored as a record of ready-made 128-byte-swizzled operand tiles: Wk^T hi + lo,
-//     -A diag(b) hi + lo, Khat hi + lo, and Gamma_C.
+//   kda_prep_kernel  (one CTA per chunk and head, three per SM): the gates' per-channel running
+//     products in registers, then the key channels in two halves of 64 (one key box and one E half
+//     in shared memory at a time): the decayed Gram on tcgen05 (M = 64, three split products,
+//     accumulated over the halves), L, A = (I + L)^{-1} in fp32 (the same blocked inverse as the
+//     gated-delta build), Wk^T = (K o Gamma)^T (A diag(b))^T on tcgen05, and Khat.  Stored as a
+//     record of ready-made 128-byte-swizzled operand tiles: Wk^T hi + lo, -A diag(b) hi + lo,
+//     Khat hi + lo, and Gamma_C.
 //   chain_kda_kernel (one CTA per segment, head and column half): the state-dependent chain with
 //     that half's X^T (and its hi and lo pieces) in tensor memory: per chunk P^T = X^T Wk^T (minus
 //     U^T = V^T (A diag(b))^T for the S half), X^T <- X^T diag(Gamma_C) + R^T Khat with

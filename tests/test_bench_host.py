@@ -70,6 +70,16 @@ def test_traffic_is_reported_only_for_the_sources_it_was_captured_on(monkeypatch
     assert bench.traffic("build_tc") is None
 
 
+def test_traffic_digest_covers_code_not_comments():
+    """Comment and layout edits leave a source's code, and so its captured traffic, in force; a change
+    to the code (a string literal included) does not."""
+    base = 'asm volatile("tcgen05.commit; // not a comment");\nint x = a + b;  // sum\n'
+    same = '/* the sum */ asm volatile("tcgen05.commit; // not a comment");\n\n  int x  =  a + b;\n'
+    assert bench.code_text(base) == bench.code_text(same)
+    assert bench.code_text(base) != bench.code_text(base.replace("a + b", "a - b"))
+    assert bench.code_text(base) != bench.code_text(base.replace("// not a comment", "// changed"))
+
+
 def test_summary_is_compact_and_tolerates_missing_legs():
     import json
     line = {"value": 45977012.07, "e2e": {"value": 11924399.0}, "build": {"ms": 0.70312},

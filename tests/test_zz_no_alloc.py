@@ -62,11 +62,12 @@ def test_outputs_limit_uses_the_larger_record(lib):
         assert r == L.HYPIC_ENOSPACE, chunks
 
 
-def _tokens(dev, key, H, lens, gap, need_q):
+def _tokens(dev, key, H, lens, gap, need_q, family="gated_delta"):
     import workloads as W
     n = sum(lens) + gap * (len(lens) + 1)
     g = W.generator(dev, 7100, key)
-    tok = W.draw_tokens(g, n, H, 128, "gated_delta", "bf16", dev, need_q=need_q)
+    tok = W.draw_tokens(g, n, H, 128, family, "bf16", dev, need_q=need_q,
+                        gate_div=16.0 if family == "kda" else None)
     bounds, off = [], gap
     for L_ in lens:
         bounds.append((off, off + L_))
@@ -189,3 +190,44 @@ def test_noalloc_build_with_outputs_matches_the_workspace_build_twice(lib):
     for b, e in bounds:
         _, o_or = ref_run("gated_delta", host, 0, b, e, want_o=True)
         assert relerr(np64(o[b:e, 1]), o_or) <= TOL_BF16
+
+
+@pytest.mark.gpu
+def test_noalloc_kda_build_in_head_blocks_against_the_oracle(lib):
+    """The KDA family keeps its larger records (82,432 bytes per chunk and head): 16 heads of four
+    bodies take two head blocks of the scratch.  Two calls in a row against the workspace build,
+    and one head against the oracle."""
+    import linear_attention_state_gb300 as hy
+
+    dev = "cuda"
+    H, d = 16, 128
+    lens = [1000, 937, 1024, 64]
+    tok, bounds, n = _tokens(dev, 4, H, lens, 5, need_q=False, family="kda")
+    b_dev = torch.tensor(bounds, dtype=torch.int64, device=dev)
+    max_len = max(lens)
+    assert len(lens) * ((max_len + 63) // 64) * 82432 * H > SCRATCH
+    T_ref, S_ref = hy.segment_build_batched(tok["k"], tok["v"], b_dev, tok["alpha"], tok["beta"], family="kda",
+                                            max_len=max_len)
+    assert hy.stream_status() == 0
+    sh = L.shape(H, d, "kda", "bf16")
+    T = torch.empty((len(lens), H, d, d), device=dev)
+    S = torch.empty((len(lens), H, d, d), device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        T.fill_(float("nan"))
+        S.fill_(float("nan"))
+        r = _call(lib, sh, len(lens), b_dev, max_len, n, tok["k"], tok["v"], None, tok["alpha"], tok["beta"], T, S,
+                  None, stream)
+        assert r == L.HYPIC_OK, (call, r)
+        assert hy.stream_status() == 0
+        worst = 0.0
+        for s_ in range(len(lens)):
+            for h in range(H):
+                worst = max(worst, relerr(np64(T[s_, h]), np64(T_ref[s_, h])),
+                            relerr(np64(S[s_, h]), np64(S_ref[s_, h])))
+        assert worst <= 1e-6, (call, worst)
+    h = H - 1
+    host = host_tokens(tok, [h])
+    for s_, (b, e) in enumerate(bounds):
+        Tr, Sr = ref_pair("kda", host, 0, b, e)
+        assert relerr(np64(T[s_, h]), Tr) <= TOL_BF16 and relerr(np64(S[s_, h]), Sr) <= TOL_BF16, s_

@@ -1127,6 +1127,24 @@ __global__ void __launch_bounds__(NT2, 1)
 // threads (warps 8 and 10): one thread issues an MMA only about every 90 cycles, and the output
 // products are off the state's serial path.
 // T_C comes from chain_tc_kernel, run for the T half only; this kernel writes S_{C|0} and o.
+// Two 32-column TMEM loads of this thread's lane, then one wait for both.
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+  uint32_t r[32], u[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(u[i]);
+  }
+}
+
 constexpr uint32_t SO_K = 0, SO_V = 16384, SO_Q = 32768, SO_REC = 49152, SO_M = SO_REC + WS_TILES;
 constexpr uint32_t SO_STAGE = SO_M + 16384;  // 112 KB
 constexpr uint32_t SO_SMEM = 2 * SO_STAGE + 1024;
@@ -1304,17 +1322,17 @@ __global__ void __launch_bounds__(SO_NT, 1)
       tmem_st16(tx + c0, v);
     }
     tmem_st_wait();
-    // Outputs of chunk cc: o_t[j] = gamma_t O_inter[j][t] + O_intra[j][t], this thread's 32 t.
+    // Outputs of chunk cc: o_t[j] = gamma_t O_inter[j][t] + O_intra[j][t], this thread's 32 t, with
+    // gamma_t taken from the staged scales while the chunk's stage still held them.
+    float gam[32];
     auto readout = [&](int cc) {
       float oi[32], oa[32];
-      tmem_ld32(tmem + lane_base + SO_OI + 32 * part, oi);
-      tmem_ld32(tmem + lane_base + SO_OA + 32 * part, oa);
+      tmem_ld32_pair(tmem + lane_base + SO_OI + 32 * part, tmem + lane_base + SO_OA + 32 * part, oi, oa);
       const int64_t t0 = beg + (int64_t)cc * C;
-      const float *gam = reinterpret_cast<const float *>(ws_rec(a, s, cc, hh) + WS_GAM);
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int t = 32 * part + q;
-        if (t0 + t < end) a.o_out[((size_t)(t0 + t) * a.H + h) * D + row] = fmaf(gam[t], oi[q], oa[q]);
+        if (t0 + t < end) a.o_out[((size_t)(t0 + t) * a.H + h) * D + row] = fmaf(gam[q], oi[q], oa[q]);
       }
     };
     bool ok = true;
@@ -1358,6 +1376,10 @@ __global__ void __launch_bounds__(SO_NT, 1)
         tc_fence_before();
         mbar_arrive(&bar_rd);
       }
+      // this chunk's gamma_t for its readout in the next step (the stage is refilled only after
+      // this chunk's last products)
+#pragma unroll
+      for (int q = 0; q < 32; ++q) gam[q] = sR[(WS_GAM - WS_SC) / 4 + 32 * part + q];
       // (2) Wm^T = -(P^T - U^T): R^T = Wm^T diag(exp(G_C - G_t)) pieces in place, Wm^T pieces aside.
       if (!(ok = mbar_wait_cycles(&bar_p, par, a.err))) break;
       tc_fence_after();

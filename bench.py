@@ -48,19 +48,19 @@ BYTES_PER_COMPOSITION = 2 * D * D * 4                                # T_C and S
 # that code is unchanged, and null once it differs.
 TRAFFIC = {
     # wy_prep_kernel + chain_tc_kernel, one build of the 8 x 4096-token, 32-head request (--build-only)
-    "build_tc": {"bytes": 2_428_635_733, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
-                 "commit": "606b45c"},
+    "build_tc": {"bytes": 2_428_619_264, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "f58ecee7ded7",
+                 "commit": "3dd9139"},
     # wy_prep_kernel<1> + T-half chain_tc_kernel + chain_so_kernel, same request with outputs
-    "build_outputs_tc": {"bytes": 5_337_370_283, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
-                         "commit": "606b45c"},
+    "build_outputs_tc": {"bytes": 5_338_161_835, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "f58ecee7ded7",
+                         "commit": "3dd9139"},
     # build_decay_tc_kernel, 64 x 512-token, 32-head decay workloads (--decay-only)
     "decay_scalar_const": {"bytes": 645_570_645, "src": ("build_decay_tc.cu", "tc_ptx.cuh"),
                            "digest": "75f0a1f85a8e", "commit": "1b1b1f2"},
     "decay_diag": {"bytes": 1_193_678_251, "src": ("build_decay_tc.cu", "tc_ptx.cuh"), "digest": "75f0a1f85a8e",
                    "commit": "1b1b1f2"},
     # wy_prep_kernel + chain_tc_kernel on the decay-family shape (--decay-only, plain gated delta)
-    "decay_gated_delta": {"bytes": 2_676_607_403, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "586669d74d6f",
-                          "commit": "606b45c"},
+    "decay_gated_delta": {"bytes": 2_676_390_229, "src": ("build_tc.cu", "tc_ptx.cuh"), "digest": "f58ecee7ded7",
+                          "commit": "3dd9139"},
     # kda_prep_kernel + chain_kda_kernel on the decay-family shape (--decay-only)
     "decay_kda": {"bytes": 3_970_410_325, "src": ("build_kda_tc.cu", "tc_ptx.cuh"), "digest": "1ede637113ef",
                   "commit": "6d2df0b"},

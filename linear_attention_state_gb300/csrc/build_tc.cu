@@ -1122,7 +1122,7 @@ __global__ void __launch_bounds__(NT2, 1)
 // tensor memory here; B = the chunk's Q tile, exact bf16, K-major), the intra-chunk one takes
 // Wm^T in bf16 hi + lo pieces (A, tensor memory) and M from the prep kernel's record (B).  The
 // outputs of chunk c are read out (scaled by gamma_t, summed) while chunk c + 1's P product runs;
-// gamma_t is read from the workspace record, which stays unchanged while the stage is refilled.
+// gamma_t is kept in registers from the chunk's staged scales, taken before the stage is refilled.
 // The state chain's products (U, P, the update) and the two output products are issued by two
 // threads (warps 8 and 10): one thread issues an MMA only about every 90 cycles, and the output
 // products are off the state's serial path.
